@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Throughput of the chunked gated delta rule forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--algo auto|simt|tc]
+
+A step is one full forward (WY build, recompute_w_u, chunk_fwd_h, chunk_fwd_o)
+over one batch of the named synthetic workload, through the C ABI, with the
+inputs resident in HBM; the L2 is flushed (a 512 MiB write) before every timed
+step. The metric is tokens/s (B*T per step). Under torchrun each rank runs its
+own copy of the workload on its own GPU (weak scaling, no collective on the
+data path); the time is the max over ranks. Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0
+only), each step a bounded sample of the workload's (b, h) sequences.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+from gated_delta_rule_35_gb300.inputs import BENCH_WORKLOAD, WORKLOADS, make_workload, to_f64  # noqa: E402
+
+METRIC = "GDN chunked-fwd tokens/s on 1 GB300; % of roofline; vs CPU oracle"
+CHUNK = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+SMS, FP32_LANES = 152, 128          # GB300: SMs, fp32 FMA lanes per SM
+DSIZE = {"f32": 4, "bf16": 2}
+
+
+# --------------------------------------------------------------------------- cost model
+def flops_per_token_head(K, V, C=CHUNK):
+    """Algorithmic flops per token-head (triangular halves counted once):
+    Gram (C-1)K, w/u (C+1)(K+V), q k^T (C+1)K, P v_new (C+1)V, state terms
+    6KV (w@h, k^T@v_gated, q@h), triangular inverse ~C^2/3."""
+    return (C - 1) * K + (C + 1) * (K + V) + (C + 1) * K + (C + 1) * V + 6 * K * V + C * C / 3
+
+
+def bytes_per_token_head(K, V, d):
+    """Compulsory HBM bytes per token-head: read q, k, v, g, beta; write o."""
+    return d * (2 * K + 2 * V) + 8
+
+
+# Per kernel: (bound, algorithmic bytes per token-head, flops per token-head) as
+# functions of (K, V, element size). The SIMT kernels keep fp32 intermediates.
+def _simt_prepare(K, V, d):
+    return d * (K + V) + 8 + 4 * (CHUNK + K + V), (CHUNK - 1) * K + CHUNK * CHUNK / 3 + (CHUNK + 1) * (K + V)
+
+
+def _simt_h(K, V, d):
+    return 4 * (K + V) + d * K + 4 + 4 * K * V / CHUNK + 4 * V, 4 * K * V
+
+
+def _simt_o(K, V, d):
+    return 2 * d * K + 4 + 4 * K * V / CHUNK + 4 * V + d * V, 2 * K * V + (CHUNK + 1) * (K + V)
+
+
+def _fused(K, V, d):
+    return bytes_per_token_head(K, V, d), flops_per_token_head(K, V)
+
+
+KERNEL_MODEL = {
+    "wy_prepare_kernel": ("alu", _simt_prepare),
+    "chunk_h_kernel": ("alu", _simt_h),
+    "chunk_o_kernel": ("alu", _simt_o),
+}
+KERNEL_SOURCE = {
+    "wy_prepare_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
+    "chunk_h_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
+    "chunk_o_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
+}
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        d["_source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback"
+    return d
+
+
+def source_sha(rel_path):
+    return hashlib.sha256((ROOT / rel_path).read_bytes()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    f = ROOT / "profiles" / "dram_traffic.json"
+    if not f.exists():
+        return None
+    rec = json.loads(f.read_text()).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    src = KERNEL_SOURCE.get(kernel)
+    if not src or rec.get("source_sha") != source_sha(src):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        ident = None
+        try:
+            ident = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            ident = str(device.index or 0)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample(x, n_seq):
+    """fp64 views of the first n_seq (b, h) sequences, each as a [1,T,1,*] problem batch."""
+    B, T, H = x["g"].shape
+    seqs = [(s // H, s % H) for s in range(min(n_seq, B * H))]
+    out = []
+    for b, h in seqs:
+        sub = {n: to_f64(x[n][b:b + 1, :, h:h + 1].contiguous()) for n in ("q", "k", "v", "g", "beta")}
+        sub["h0"] = None if x["h0"] is None else to_f64(x["h0"][b:b + 1, h:h + 1].contiguous())
+        out.append(sub)
+    return out
+
+
+def run_oracle_sample(samples, threads):
+    """Runs the oracle over the sampled sequences as one batch (stacked over H)."""
+    import numpy as np
+
+    from oracle import recurrence
+    cat = lambda n: np.concatenate([s[n] for s in samples], axis=2)
+    h0 = None if samples[0]["h0"] is None else np.concatenate([s["h0"] for s in samples], axis=1)
+    t = time.perf_counter()
+    recurrence.forward(cat("q"), cat("k"), cat("v"), cat("g"), cat("beta"), 1.0, h0, nthreads=threads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(x, w, budget_s):
+    """The oracle on a bounded sample of the workload, on all host cores."""
+    threads = os.cpu_count() or 1
+    n_total = w.B * w.H
+    n = min(n_total, max(1, threads))
+    dt = run_oracle_sample(oracle_sample(x, n), threads)
+    # grow the sample (up to the whole workload) to fill about budget_s seconds
+    per_seq = dt / n
+    n2 = int(min(n_total, max(n, budget_s / max(per_seq, 1e-9))))
+    if n2 > n:
+        n = n2
+        dt = run_oracle_sample(oracle_sample(x, n), threads)
+    tokens = n * w.T / w.H            # B*T-equivalent tokens of the sample
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {n_total} (b,h) sequences of {w.name}, full T={w.T}, fp64 token "
+                      f"recurrence, {dt:.2f} s; tokens = sequences*T/H"}
+
+
+# --------------------------------------------------------------------------- arms
+def bench_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    x = make_workload(w.name)
+    threads = os.cpu_count() or 1
+    n_seq = min(w.B * w.H, max(1, threads))
+    samples = oracle_sample(x, n_seq)
+    for _ in range(args.warmup):
+        run_oracle_sample(samples, threads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += run_oracle_sample(samples, threads)
+    tokens = n_seq * w.T / w.H
+    value = tokens * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {n_seq} of {w.B * w.H} (b,h) sequences of {w.name}, "
+                                   f"full T={w.T}; tokens = sequences*T/H"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": CHUNK,
+            "io_dtype": w.dtype, "algo": args.algo, "l2": "flushed before every timed step (512 MiB write)",
+            "parallelism": f"replica x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def bench_ours(args, w, world, rank, local):
+    from gated_delta_rule_35_gb300 import chunk_fwd, chunk_fwd_host, native
+
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    x = make_workload(w.name)
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, args.algo)
+    kernels = native.launches(p)
+    nk = len(kernels)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
+    hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def make_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        for e in evs:
+            e.record(stream)          # creates the underlying cudaEvent_t
+        return evs
+
+    step_events = [make_events() for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=args.algo,
+                  workspace=ws, out=o, final_state=hf, stream=stream,
+                  events=None if evs is None else [e.cuda_event for e in evs])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(step_events[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+
+    per_kernel = [0.0] * nk
+    total_ms = 0.0
+    for evs in step_events:
+        total_ms += evs[0].elapsed_time(evs[nk])
+        for j in range(nk):
+            per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
+    total_s = max_over_ranks(total_ms / 1e3, world, dev)
+    tokens_step = w.B * w.T
+    value = tokens_step * args.steps * world / total_s
+    ms_per_step = 1e3 * total_s / args.steps
+
+    # roofline of the dominant kernel
+    peaks = load_peaks()
+    dom = max(range(nk), key=lambda j: per_kernel[j])
+    name = kernels[dom]
+    t_launch = per_kernel[dom] / args.steps / 1e3
+    units = w.B * w.T * w.H
+    bound, model = KERNEL_MODEL.get(name, ("hbm", _fused))
+    bpt, fpt = model(w.K, w.V, DSIZE[w.dtype])
+    traffic = ncu_traffic(name, w.name)
+    if bound == "hbm":
+        achieved, peak, unit = bpt * units / t_launch / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        achieved, peak, unit = fpt * units / t_launch / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:   # fp32 FMA pipe: SMs x lanes x 2 flop x max SM clock
+        peak = SMS * FP32_LANES * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        achieved, unit = fpt * units / t_launch / 1e12, "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic, "kernel": name,
+                "kernel_ms": 1e3 * t_launch, "share": per_kernel[dom] / max(sum(per_kernel), 1e-12),
+                "peak_source": peaks["_source"],
+                "algorithmic_per_token_head": {"bytes": bpt, "flops": fpt}}
+    # whole-pipeline roofline: max(flops / bf16 peak, compulsory bytes / HBM)
+    hbytes = (2 if d["h0"] is not None else 1) * w.B * w.H * w.K * w.V * 4
+    F = flops_per_token_head(w.K, w.V) * units
+    Bt = bytes_per_token_head(w.K, w.V, DSIZE[w.dtype]) * units + hbytes
+    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bt / (peaks["hbm_gbs"] * 1e9))
+    pipeline = {"t_roof_us": 1e6 * t_roof, "t_meas_us": 1e3 * ms_per_step,
+                "frac": t_roof / (ms_per_step / 1e3), "flops": F, "bytes": Bt,
+                "bound": "hbm" if Bt / (peaks["hbm_gbs"] * 1e9) >= F / (peaks["bf16_tflops"] * 1e12) else "tensor",
+                "peak_source": peaks["_source"]}
+
+    # end to end through the public host-tensor API: H2D inputs, forward, D2H o and h_final
+    hx = {n: (t.pin_memory() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    h2d = sum(t.numel() * t.element_size() for n, t in hx.items() if isinstance(t, torch.Tensor))
+    d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
+    e2e_steps = max(1, min(args.steps, 20))
+    for _ in range(2):
+        chunk_fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], 1.0, hx["h0"], algo=args.algo,
+                       device=dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        chunk_fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], 1.0, hx["h0"], algo=args.algo,
+                       device=dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": tokens_step * e2e_steps * world / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16-in/f32-acc" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_of(w, args),
+            "token_heads_per_s": value * w.H,
+            "roofline": roofline, "pipeline_roofline": pipeline,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
+            "kernels": kernels,
+            "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
+            "clocks": clk, "wall_timed_s": wall,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        bench_reference(args, w, world, rank)
+    else:
+        bench_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+// Host side of the C ABI declared in include/gdn.h: argument validation,
+// workspace carving, algorithm choice and the launch sequence.
+#include <cstring>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_problem(const gdn_problem *p) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->K <= 0 || p->V <= 0) return GDN_ERR_INVALID_ARG;
+    if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
+        return GDN_ERR_INVALID_ARG;
+    if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
+    if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
+    // Every index is computed in 64 bits; B*T*H rows must still fit a grid.
+    if (num_chunks(p->T) > 65535 * 64LL) return GDN_ERR_UNSUPPORTED;
+    if (p->H > 65535 || p->B > 65535) return GDN_ERR_UNSUPPORTED;
+    if (p->algo == GDN_ALGO_TC && !tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)))
+        return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_algo resolve_algo(const gdn_problem *p) {
+    if (p->algo != GDN_ALGO_AUTO) return static_cast<gdn_algo>(p->algo);
+    return tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)) ? GDN_ALGO_TC
+                                                                       : GDN_ALGO_SIMT;
+}
+
+size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
+    if (p->T == 0) return 0;
+    if (algo == GDN_ALGO_TC) return tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+    return simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+}
+
+gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+               const float *beta, float scale, const float *h0, void *o, float *h_final,
+               void *workspace, size_t workspace_bytes, const gdn_stage_exports *ex,
+               const Marks &marks, cudaStream_t stream) {
+    gdn_status st = check_problem(p);
+    if (st != GDN_OK) return st;
+    const bool empty = p->T == 0;
+    if (!empty && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, h0, o, h_final, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
+    const gdn_algo algo = resolve_algo(p);
+    if (ex && algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
+    const size_t need = kStatusBytes + body_bytes(p, algo);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+
+    Args a;
+    a.B = p->B; a.T = p->T; a.H = p->H; a.K = p->K; a.V = p->V;
+    a.NT = static_cast<int>(num_chunks(p->T));
+    a.T_pad = a.NT * kChunk;
+    a.dtype = static_cast<gdn_dtype>(p->dtype);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale; a.h0 = h0;
+    a.o = o; a.h_final = h_final;
+    a.status = static_cast<uint32_t *>(workspace);
+    void *body = static_cast<char *>(workspace) + kStatusBytes;
+
+    cudaError_t e;
+    if (empty) {
+        e = marks.mark(0, stream);
+        if (e == cudaSuccess) e = copy_state(a, stream);
+        if (e == cudaSuccess) e = marks.mark(1, stream);
+    } else if (algo == GDN_ALGO_TC) {
+        e = tc_forward(a, body, stream, marks);
+    } else {
+        const SimtWorkspace ws = simt_carve(body, a.B, a.T, a.H, a.K, a.V);
+        e = simt_forward(a, ws, stream, marks);
+        if (e == cudaSuccess && ex) {
+            const size_t rows = static_cast<size_t>(a.B) * a.T_pad * a.H;
+            struct { float *dst; const float *src; size_t n; } cp[] = {
+                {ex->A, ws.A, rows * kChunk},
+                {ex->w, ws.w, rows * a.K},
+                {ex->u, ws.u, rows * a.V},
+                {ex->v_new, ws.v_new, rows * a.V},
+                {ex->h, ws.h, static_cast<size_t>(a.B) * a.NT * a.H * a.K * a.V},
+            };
+            for (auto &c : cp)
+                if (c.dst && e == cudaSuccess)
+                    e = cudaMemcpyAsync(c.dst, c.src, c.n * sizeof(float), cudaMemcpyDeviceToDevice,
+                                        stream);
+        }
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int launches(const gdn_problem *p, const char **names, int max_names) {
+    if (check_problem(p) != GDN_OK) return 0;
+    if (p->T == 0) {
+        if (names && max_names > 0) names[0] = kCopyStateName;
+        return 1;
+    }
+    if (resolve_algo(p) == GDN_ALGO_TC) return tc_launches(names, max_names);
+    for (int i = 0; names && i < kSimtLaunches && i < max_names; ++i) names[i] = kSimtKernelNames[i];
+    return kSimtLaunches;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+GDN_API size_t gdn_chunk_fwd_workspace_bytes(const gdn_problem *p) {
+    if (gdn::check_problem(p) != GDN_OK) return 0;
+    return gdn::kStatusBytes + gdn::body_bytes(p, gdn::resolve_algo(p));
+}
+
+GDN_API gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float scale, const float *h0,
+                                 void *o, float *h_final, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    return gdn::run(p, q, k, v, g, beta, scale, h0, o, h_final, workspace, workspace_bytes,
+                    nullptr, gdn::Marks{}, static_cast<cudaStream_t>(stream));
+}
+
+GDN_API int32_t gdn_chunk_fwd_launches(const gdn_problem *p, const char **names,
+                                       int32_t max_names) {
+    return gdn::launches(p, names, max_names);
+}
+
+GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p, const void *q, const void *k,
+                                          const void *v, const float *g, const float *beta,
+                                          float scale, const float *h0, void *o, float *h_final,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *const *events, int32_t n_events, void *stream) {
+    const int n = gdn::launches(p, nullptr, 0);
+    if (n == 0) return GDN_ERR_INVALID_ARG;
+    if (!events || n_events < n + 1) return GDN_ERR_INVALID_ARG;
+    gdn::Marks m;
+    m.ev = reinterpret_cast<cudaEvent_t const *>(events);
+    m.n = n_events;
+    return gdn::run(p, q, k, v, g, beta, scale, h0, o, h_final, workspace, workspace_bytes,
+                    nullptr, m, static_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_chunk_fwd_stages(const gdn_problem *p, const void *q, const void *k,
+                                        const void *v, const float *g, const float *beta,
+                                        float scale, const float *h0, void *o, float *h_final,
+                                        void *workspace, size_t workspace_bytes,
+                                        const gdn_stage_exports *ex, void *stream) {
+    if (!ex) return GDN_ERR_INVALID_ARG;
+    return gdn::run(p, q, k, v, g, beta, scale, h0, o, h_final, workspace, workspace_bytes, ex,
+                    gdn::Marks{}, static_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream) {
+    if (!workspace) return GDN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word == 0) return GDN_OK;
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_ERR_DEVICE_TIMEOUT;
+}
+
+GDN_API const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported shape, dtype or algorithm";
+        case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+GDN_API uint32_t gdn_version(void) { return (0u << 16) | (1u << 8) | 0u; }
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the host launcher and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;
+
+inline int64_t num_chunks(int T) { return (static_cast<int64_t>(T) + kChunk - 1) / kChunk; }
+
+// Pointers of one call, already validated by the launcher.
+struct Args {
+    int B, T, H, K, V;
+    int NT;          // ceil(T / 64)
+    int T_pad;       // NT * 64
+    gdn_dtype dtype;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    float scale;
+    const float *h0;
+    void *o;
+    float *h_final;
+    uint32_t *status;   // device status word (first bytes of the workspace)
+};
+
+// Workspace of the SIMT pipeline: fp32 intermediates, every region 256-byte aligned.
+struct SimtWorkspace {
+    float *A, *w, *u, *v_new, *h;
+};
+
+// Optional timing markers: ev[0] before the first kernel, ev[i + 1] after kernel i.
+struct Marks {
+    cudaEvent_t const *ev = nullptr;
+    int n = 0;
+    cudaError_t mark(int i, cudaStream_t s) const {
+        return (ev && i < n) ? cudaEventRecord(ev[i], s) : cudaSuccess;
+    }
+};
+
+size_t simt_workspace_bytes(int B, int T, int H, int K, int V);
+SimtWorkspace simt_carve(void *base, int B, int T, int H, int K, int V);
+cudaError_t simt_forward(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Marks &m);
+constexpr int kSimtLaunches = 3;
+extern const char *const kSimtKernelNames[kSimtLaunches];
+
+// Tensor-core path.
+bool tc_supported(int K, int V, gdn_dtype dtype);
+size_t tc_workspace_bytes(int B, int T, int H, int K, int V);
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m);
+int tc_launches(const char **names, int max_names);
+
+// h_final = h0 (or 0) for T == 0.
+cudaError_t copy_state(const Args &a, cudaStream_t s);
+constexpr const char *kCopyStateName = "copy_state_kernel";
+
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+
+}  // namespace gdn

@@ -1,0 +1,347 @@
+// CUDA-core (SIMT) pipeline of the chunked gated delta rule forward, fp32
+// arithmetic throughout. It is the path for fp32 inputs (tensor-core TF32
+// would not hold 1e-4 relative error) and the stage-by-stage reference path
+// whose intermediates can be exported. Four kernels, as in the "WarpDrive"
+// page's pipeline (kernels 3-5): WY build + recompute_w_u, chunk_fwd_h,
+// chunk_fwd_o. Intermediates live in an fp32 workspace.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBV = 16;   // V columns of the state per chunk_fwd_h block
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_as(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_as(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Row index of token t of sequence (b, h) in a [B,T,H,*] tensor.
+__device__ __forceinline__ int64_t tok(int b, int t, int h, int T, int H) {
+    return (static_cast<int64_t>(b) * T + t) * H + h;
+}
+
+// ---------------------------------------------------------------------------
+// WY build + recompute_w_u ("WarpDrive" kernel 5). One block per (chunk, h, b).
+//   L_ij = beta_i (k_i . k_j) exp(g_i - g_j), i > j;  A = (I + L)^-1
+//   w = A (k * beta * exp(g)),  u = A (v * beta)
+// The inverse is a forward substitution: thread c owns column c of A and
+// walks rows i = c..63: A_ic = [i == c] - sum_{c <= j < i} L_ij A_jc.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__restrict__ g,
+                  const float *__restrict__ beta, int Tn, int H, int K, int V, int T_pad,
+                  float *__restrict__ A_ws, float *__restrict__ w_ws, float *__restrict__ u_ws) {
+    extern __shared__ float smem[];
+    __shared__ float gs[kChunk], bs[kChunk];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int t0 = c * kChunk;
+    const int n = min(kChunk, Tn - t0);
+    const int KP = K + 1;
+    float *ks = smem;                  // [64][K+1]
+    float *Ls = ks + kChunk * KP;      // [64][65]
+    float *As = Ls + kChunk * 65;      // [64][65]
+    float *xs = As + kChunk * 65;      // [64][65] slice of v * beta
+
+    if (tid < kChunk) {
+        gs[tid] = tid < n ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
+        bs[tid] = tid < n ? beta[tok(b, t0 + tid, h, Tn, H)] : 0.f;
+    }
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, kk = idx - i * K;
+        ks[i * KP + kk] = i < n ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        float val = 0.f;
+        if (i > j && i < n) {
+            float dot = 0.f;
+            for (int kk = 0; kk < K; ++kk) dot = fmaf(ks[i * KP + kk], ks[j * KP + kk], dot);
+            val = bs[i] * dot * expf(gs[i] - gs[j]);
+        }
+        Ls[i * 65 + j] = val;
+    }
+    __syncthreads();
+
+    if (tid < kChunk) {
+        const int col = tid;
+        for (int i = 0; i < col; ++i) As[i * 65 + col] = 0.f;
+        for (int i = col; i < kChunk; ++i) {
+            float acc = (i == col) ? 1.f : 0.f;
+            for (int j = col; j < i; ++j) acc = fmaf(-Ls[i * 65 + j], As[j * 65 + col], acc);
+            As[i * 65 + col] = acc;
+        }
+    }
+    // k <- k * beta * exp(g) (the Gram above used the unscaled rows)
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, kk = idx - i * K;
+        ks[i * KP + kk] *= (i < n) ? bs[i] * expf(gs[i]) : 0.f;
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        A_ws[tok(b, t0 + i, h, T_pad, H) * kChunk + j] = As[i * 65 + j];
+    }
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, kk = idx - i * K;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(As[i * 65 + j], ks[j * KP + kk], acc);
+        w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk] = acc;
+    }
+    for (int vs = 0; vs < V; vs += 64) {
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int j = idx >> 6, nn = idx & 63;
+            xs[j * 65 + nn] = j < n ? bs[j] * to_f32(v[tok(b, t0 + j, h, Tn, H) * V + vs + nn]) : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int i = idx >> 6, nn = idx & 63;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc = fmaf(As[i * 65 + j], xs[j * 65 + nn], acc);
+            u_ws[tok(b, t0 + i, h, T_pad, H) * V + vs + nn] = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// chunk_fwd_h ("WarpDrive" kernel 3). One block per (V tile of 16, h, b),
+// sequential over the chunks: store h; v_new = u - w @ h;
+// v_gated = v_new * exp(g_last - g_t); h = h * exp(g_last) + k^T @ v_gated.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float *__restrict__ w_ws,
+               const float *__restrict__ u_ws, const float *__restrict__ h0, int Tn, int H, int K,
+               int V, int NT, int T_pad, float *__restrict__ h_ws, float *__restrict__ vn_ws,
+               float *__restrict__ h_final) {
+    extern __shared__ float smem[];
+    __shared__ float gs[kChunk];
+    const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int KP = K + 1;
+    float *hs = smem;                   // [K][kBV]
+    float *ws = hs + K * kBV;           // [64][K+1]
+    float *ks = ws + kChunk * KP;       // [64][K+1]
+    float *vs = ks + kChunk * KP;       // [64][kBV + 1]: u, then v_new, then v_gated
+    constexpr int VP = kBV + 1;
+    const int64_t state = (static_cast<int64_t>(b) * H + h) * K * V;
+
+    for (int idx = tid; idx < K * kBV; idx += kThreads) {
+        const int kk = idx / kBV, nn = idx - kk * kBV;
+        hs[idx] = h0 ? h0[state + static_cast<int64_t>(kk) * V + v0 + nn] : 0.f;
+    }
+    for (int c = 0; c < NT; ++c) {
+        const int t0 = c * kChunk;
+        const int n = min(kChunk, Tn - t0);
+        __syncthreads();
+        const int64_t hslot = ((static_cast<int64_t>(b) * NT + c) * H + h) * K * V;
+        for (int idx = tid; idx < K * kBV; idx += kThreads) {
+            const int kk = idx / kBV, nn = idx - kk * kBV;
+            h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + nn] = hs[idx];
+        }
+        if (tid < kChunk) gs[tid] = tid < n ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
+        for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+            const int i = idx / K, kk = idx - i * K;
+            ws[i * KP + kk] = w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk];
+            ks[i * KP + kk] = i < n ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
+        }
+        for (int idx = tid; idx < kChunk * kBV; idx += kThreads) {
+            const int i = idx / kBV, nn = idx - i * kBV;
+            vs[i * VP + nn] = u_ws[tok(b, t0 + i, h, T_pad, H) * V + v0 + nn];
+        }
+        __syncthreads();
+        // v_new = u - w @ h
+        float vnew[kChunk * kBV / kThreads];
+#pragma unroll
+        for (int r = 0; r < kChunk * kBV / kThreads; ++r) {
+            const int idx = tid + r * kThreads;
+            const int i = idx / kBV, nn = idx - i * kBV;
+            float acc = vs[i * VP + nn];
+            for (int kk = 0; kk < K; ++kk) acc = fmaf(-ws[i * KP + kk], hs[kk * kBV + nn], acc);
+            vnew[r] = acc;
+            vn_ws[tok(b, t0 + i, h, T_pad, H) * V + v0 + nn] = acc;
+        }
+        __syncthreads();
+        const float glast = gs[n - 1];
+#pragma unroll
+        for (int r = 0; r < kChunk * kBV / kThreads; ++r) {
+            const int idx = tid + r * kThreads;
+            const int i = idx / kBV, nn = idx - i * kBV;
+            vs[i * VP + nn] = i < n ? vnew[r] * expf(glast - gs[i]) : 0.f;
+        }
+        __syncthreads();
+        // h = h * exp(g_last) + k^T @ v_gated
+        const float decay = expf(glast);
+        for (int idx = tid; idx < K * kBV; idx += kThreads) {
+            const int kk = idx / kBV, nn = idx - kk * kBV;
+            float acc = hs[idx] * decay;
+            for (int i = 0; i < n; ++i) acc = fmaf(ks[i * KP + kk], vs[i * VP + nn], acc);
+            hs[idx] = acc;
+        }
+    }
+    if (h_final) {
+        __syncthreads();
+        for (int idx = tid; idx < K * kBV; idx += kThreads) {
+            const int kk = idx / kBV, nn = idx - kk * kBV;
+            h_final[state + static_cast<int64_t>(kk) * V + v0 + nn] = hs[idx];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// chunk_fwd_o ("WarpDrive" kernel 4). One block per (chunk, h, b):
+//   P_ij = (q_i . k_j) exp(g_i - g_j) for j <= i (diagonal included), else 0
+//   o_i  = scale * (exp(g_i) q_i^T h_c + sum_j P_ij v_new_j)
+// with h_c the state entering the chunk and v_new the ungated values.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ g,
+               const float *__restrict__ h_ws, const float *__restrict__ vn_ws, int Tn, int H,
+               int K, int V, int NT, int T_pad, float scale, T *__restrict__ o) {
+    extern __shared__ float smem[];
+    __shared__ float gs[kChunk];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int t0 = c * kChunk;
+    const int n = min(kChunk, Tn - t0);
+    const int KP = K + 1;
+    float *qs = smem;                  // [64][K+1]
+    float *ks = qs + kChunk * KP;      // [64][K+1]
+    float *Ps = ks + kChunk * KP;      // [64][65]
+    float *hs = Ps + kChunk * 65;      // [K][65]
+    float *vs = hs + K * 65;           // [64][65]
+
+    if (tid < kChunk) gs[tid] = tid < n ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, kk = idx - i * K;
+        const bool ok = i < n;
+        qs[i * KP + kk] = ok ? to_f32(q[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
+        ks[i * KP + kk] = ok ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        float val = 0.f;
+        if (j <= i && i < n) {
+            float dot = 0.f;
+            for (int kk = 0; kk < K; ++kk) dot = fmaf(qs[i * KP + kk], ks[j * KP + kk], dot);
+            val = dot * expf(gs[i] - gs[j]);
+        }
+        Ps[i * 65 + j] = val;
+    }
+    const int64_t hslot = ((static_cast<int64_t>(b) * NT + c) * H + h) * K * V;
+    for (int v0 = 0; v0 < V; v0 += 64) {
+        __syncthreads();
+        for (int idx = tid; idx < K * 64; idx += kThreads) {
+            const int kk = idx >> 6, nn = idx & 63;
+            hs[kk * 65 + nn] = h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + nn];
+        }
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int j = idx >> 6, nn = idx & 63;
+            vs[j * 65 + nn] = vn_ws[tok(b, t0 + j, h, T_pad, H) * V + v0 + nn];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int i = idx >> 6, nn = idx & 63;
+            if (i >= n) continue;
+            float inter = 0.f;
+            for (int kk = 0; kk < K; ++kk) inter = fmaf(qs[i * KP + kk], hs[kk * 65 + nn], inter);
+            float intra = 0.f;
+            for (int j = 0; j <= i; ++j) intra = fmaf(Ps[i * 65 + j], vs[j * 65 + nn], intra);
+            store_as(&o[tok(b, t0 + i, h, Tn, H) * V + v0 + nn],
+                     scale * (expf(gs[i]) * inter + intra));
+        }
+    }
+}
+
+__global__ void copy_state_kernel(const float *__restrict__ h0, float *__restrict__ h_final,
+                                  int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        h_final[i] = h0 ? h0[i] : 0.f;
+}
+
+size_t prepare_smem(int K) { return sizeof(float) * (kChunk * (K + 1) + 3 * kChunk * 65); }
+size_t chunk_h_smem(int K) {
+    return sizeof(float) * (K * kBV + 2 * kChunk * (K + 1) + kChunk * (kBV + 1));
+}
+size_t chunk_o_smem(int K) { return sizeof(float) * (2 * kChunk * (K + 1) + kChunk * 65 + K * 65 + kChunk * 65); }
+
+template <typename T>
+cudaError_t run(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Marks &m) {
+    const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k),
+            *v = static_cast<const T *>(a.v);
+    cudaError_t e;
+    const size_t s1 = prepare_smem(a.K), s2 = chunk_h_smem(a.K), s3 = chunk_o_smem(a.K);
+    if ((e = cudaFuncSetAttribute(wy_prepare_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(s1))) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(chunk_h_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(s2))) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(chunk_o_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(s3))) != cudaSuccess)
+        return e;
+    const dim3 chunks(a.NT, a.H, a.B);
+    if ((e = m.mark(0, s)) != cudaSuccess) return e;
+    wy_prepare_kernel<T><<<chunks, kThreads, s1, s>>>(k, v, a.g, a.beta, a.T, a.H, a.K, a.V,
+                                                     a.T_pad, ws.A, ws.w, ws.u);
+    if ((e = m.mark(1, s)) != cudaSuccess) return e;
+    chunk_h_kernel<T><<<dim3(a.V / kBV, a.H, a.B), kThreads, s2, s>>>(
+        k, a.g, ws.w, ws.u, a.h0, a.T, a.H, a.K, a.V, a.NT, a.T_pad, ws.h, ws.v_new, a.h_final);
+    if ((e = m.mark(2, s)) != cudaSuccess) return e;
+    chunk_o_kernel<T><<<chunks, kThreads, s3, s>>>(q, k, a.g, ws.h, ws.v_new, a.T, a.H, a.K, a.V,
+                                                  a.NT, a.T_pad, a.scale, static_cast<T *>(a.o));
+    if ((e = m.mark(3, s)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(int B, int T, int H, int K, int V) {
+    const size_t NT = static_cast<size_t>(num_chunks(T));
+    const size_t rows = static_cast<size_t>(B) * NT * kChunk * H;
+    return align_up(rows * kChunk * 4) + align_up(rows * K * 4) + 2 * align_up(rows * V * 4) +
+           align_up(static_cast<size_t>(B) * NT * H * K * V * 4);
+}
+
+SimtWorkspace simt_carve(void *base, int B, int T, int H, int K, int V) {
+    const size_t NT = static_cast<size_t>(num_chunks(T));
+    const size_t rows = static_cast<size_t>(B) * NT * kChunk * H;
+    char *p = static_cast<char *>(base);
+    SimtWorkspace w;
+    w.A = reinterpret_cast<float *>(p);
+    p += align_up(rows * kChunk * 4);
+    w.w = reinterpret_cast<float *>(p);
+    p += align_up(rows * K * 4);
+    w.u = reinterpret_cast<float *>(p);
+    p += align_up(rows * V * 4);
+    w.v_new = reinterpret_cast<float *>(p);
+    p += align_up(rows * V * 4);
+    w.h = reinterpret_cast<float *>(p);
+    return w;
+}
+
+const char *const kSimtKernelNames[kSimtLaunches] = {"wy_prepare_kernel", "chunk_h_kernel",
+                                                     "chunk_o_kernel"};
+
+cudaError_t simt_forward(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Marks &m) {
+    if (a.dtype == GDN_BF16) return run<__nv_bfloat16>(a, ws, s, m);
+    return run<float>(a, ws, s, m);
+}
+
+cudaError_t copy_state(const Args &a, cudaStream_t s) {
+    if (!a.h_final) return cudaSuccess;
+    const int64_t n = static_cast<int64_t>(a.B) * a.H * a.K * a.V;
+    copy_state_kernel<<<152, 256, 0, s>>>(a.h0, a.h_final, n);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -14,8 +14,10 @@ Recipe (one ``torch.Generator('cpu')`` per workload, drawn in this order):
   h0 = h0_std * h0_raw. q, k, v are then cast to the compute dtype; g, beta and
   h0 stay fp32.
 
-The five named workloads are the ones the Gated DeltaNet chunked-forward
-benchmark is quoted on (page "WarpDrive", kernels 3-5, chunk size C=64).
+Five named workloads: a small fp32 case (one 256-token head, K=V=64), and
+four bf16 cases with K=128: a short batch, a long prefill with a non-zero
+initial state, a wide batch, and a V=256 case with near-zero decay and large
+beta. The chunk size is C=64 throughout ("WarpDrive" page, section "Pipeline").
 """
 from __future__ import annotations
 
@@ -71,10 +73,10 @@ TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 def chunk_local_cumsum(x: torch.Tensor, chunk: int = CHUNK) -> torch.Tensor:
     """Cumulative sum over dim 1 (time) restarted at every ``chunk`` tokens."""
     B, T = x.shape[:2]
-    out = torch.empty_like(x)
-    for s in range(0, T, chunk):
-        out[:, s:s + chunk] = torch.cumsum(x[:, s:s + chunk], dim=1)
-    return out
+    NT = (T + chunk - 1) // chunk
+    pad = torch.zeros((B, NT * chunk - T) + tuple(x.shape[2:]), dtype=x.dtype)
+    xp = torch.cat([x, pad], dim=1).reshape((B, NT, chunk) + tuple(x.shape[2:]))
+    return torch.cumsum(xp, dim=2).reshape((B, NT * chunk) + tuple(x.shape[2:]))[:, :T].contiguous()
 
 
 def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", seed: int = 0,

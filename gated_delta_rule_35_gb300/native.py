@@ -1,0 +1,207 @@
+"""ctypes binding of ``libgdn.so`` (include/gdn.h): argument marshalling only.
+
+Every step of the forward runs in the library's CUDA kernels; PyTorch only
+allocates device memory and supplies the current stream. There is no CPU or
+PyTorch fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "lib" / "libgdn.so"
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGNMENT = 0, 1, 2, 3
+GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = 4, 5, 6
+GDN_F32, GDN_BF16 = 0, 1
+ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
+CHUNK = 64
+
+# Every function include/gdn.h declares.
+EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stages",
+           "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
+           "gdn_status_string", "gdn_version")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("algo", ctypes.c_int32)]
+
+
+class StageExports(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("w", ctypes.c_void_p), ("u", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(str(LIB_PATH))
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        pp = ctypes.POINTER(Problem)
+        L.gdn_chunk_fwd_workspace_bytes.restype = sz
+        L.gdn_chunk_fwd_workspace_bytes.argtypes = [pp]
+        fwd_args = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, sz]
+        L.gdn_chunk_fwd.restype = ctypes.c_int
+        L.gdn_chunk_fwd.argtypes = fwd_args + [vp]
+        L.gdn_chunk_fwd_stages.restype = ctypes.c_int
+        L.gdn_chunk_fwd_stages.argtypes = fwd_args + [ctypes.POINTER(StageExports), vp]
+        L.gdn_chunk_fwd_launches.restype = ctypes.c_int32
+        L.gdn_chunk_fwd_launches.argtypes = [pp, ctypes.POINTER(ctypes.c_char_p), ctypes.c_int32]
+        L.gdn_chunk_fwd_profiled.restype = ctypes.c_int
+        L.gdn_chunk_fwd_profiled.argtypes = fwd_args + [ctypes.POINTER(ctypes.c_void_p),
+                                                        ctypes.c_int32, vp]
+        L.gdn_check_device_status.restype = ctypes.c_int
+        L.gdn_check_device_status.argtypes = [vp, vp]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_version.restype = ctypes.c_uint32
+        L.gdn_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().gdn_status_string(int(s)).decode()
+
+
+def problem(B, T, H, K, V, dtype, algo="auto") -> Problem:
+    d = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return Problem(int(B), int(T), int(H), int(K), int(V), d, ALGOS[algo] if isinstance(algo, str) else int(algo))
+
+
+def workspace_bytes(p: Problem) -> int:
+    return int(lib().gdn_chunk_fwd_workspace_bytes(ctypes.byref(p)))
+
+
+def launches(p: Problem) -> list[str]:
+    """Names of the kernels one call launches, in order."""
+    n = int(lib().gdn_chunk_fwd_launches(ctypes.byref(p), None, 0))
+    names = (ctypes.c_char_p * max(n, 1))()
+    lib().gdn_chunk_fwd_launches(ctypes.byref(p), names, n)
+    return [names[i].decode() for i in range(n)]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_inputs(q, k, v, g, beta, h0):
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors (use chunk_fwd_host for host tensors)")
+    if q.dtype not in DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or g.shape != (B, T, H) \
+            or beta.shape != (B, T, H):
+        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], g, beta [B,T,H]")
+    if h0 is not None and (h0.shape != (B, H, K, V) or h0.dtype != torch.float32):
+        raise ValueError("h0 must be float32 [B,H,K,V]")
+    for t in (q, k, v, g, beta, h0):
+        if t is not None and (not t.is_contiguous() or t.device != dev):
+            raise ValueError("all tensors must be contiguous and on the same device")
+    return B, T, H, K, V
+
+
+def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
+              algo: str = "auto", workspace=None, out=None, final_state=None, stream=None,
+              events=None):
+    """Chunked gated-delta-rule forward on CUDA tensors. Returns (o, h_final or None).
+
+    q, k [B,T,H,K] and v [B,T,H,V] (float32 or bfloat16), g and beta [B,T,H]
+    float32 (g: chunk-local cumulative log-decay), h0 [B,H,K,V] float32 or None.
+    ``workspace``/``out``/``final_state`` may be passed to reuse buffers."""
+    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
+    p = problem(B, T, H, K, V, q.dtype, algo)
+    need = workspace_bytes(p)
+    if need == 0:
+        raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_chunk_fwd_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    hf = None
+    if output_final_state:
+        hf = final_state if final_state is not None else \
+            torch.empty((B, H, K, V), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+            _ptr(h0), _ptr(o), _ptr(hf), _ptr(workspace), workspace.numel())
+    if events is None:
+        st = lib().gdn_chunk_fwd(*args, ctypes.c_void_p(s.cuda_stream))
+    else:
+        # events: raw cudaEvent_t handles (ints); markers between the kernels
+        arr = (ctypes.c_void_p * len(events))(*events)
+        st = lib().gdn_chunk_fwd_profiled(*args, arr, len(events), ctypes.c_void_p(s.cuda_stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd")
+    return o, hf
+
+
+def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = "simt"):
+    """Forward plus the exported intermediates (A, w, u, v_new, h), all fp32."""
+    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
+    p = problem(B, T, H, K, V, q.dtype, algo)
+    NT = (T + CHUNK - 1) // CHUNK
+    Tp = NT * CHUNK
+    f32 = dict(dtype=torch.float32, device=q.device)
+    st_bufs = {"A": torch.empty((B, Tp, H, CHUNK), **f32), "w": torch.empty((B, Tp, H, K), **f32),
+               "u": torch.empty((B, Tp, H, V), **f32), "v_new": torch.empty((B, Tp, H, V), **f32),
+               "h": torch.empty((B, NT, H, K, V), **f32)}
+    ex = StageExports(*(ctypes.c_void_p(st_bufs[n].data_ptr()) for n in ("A", "w", "u", "v_new", "h")))
+    need = workspace_bytes(p)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    hf = torch.empty((B, H, K, V), **f32)
+    s = torch.cuda.current_stream(q.device)
+    st = lib().gdn_chunk_fwd_stages(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                    _ptr(beta), float(scale), _ptr(h0), _ptr(o), _ptr(hf),
+                                    _ptr(ws), ws.numel(), ctypes.byref(ex),
+                                    ctypes.c_void_p(s.cuda_stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd_stages")
+    st_bufs.update(o=o, h_final=hf)
+    return st_bufs
+
+
+def check_device_status(workspace, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    return int(lib().gdn_check_device_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream)))
+
+
+def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
+                   algo: str = "auto", device=None):
+    """Host-tensor front end: copies the inputs to the GPU, runs chunk_fwd and
+    copies o (and h_final) back into pinned host tensors, synchronously."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dq, dk, dv, dg, db = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
+    dh0 = None if h0 is None else h0.to(dev, non_blocking=True)
+    o, hf = chunk_fwd(dq, dk, dv, dg, db, scale, dh0, output_final_state, algo)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    ho.copy_(o, non_blocking=True)
+    hhf = None
+    if hf is not None:
+        hhf = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
+        hhf.copy_(hf, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return ho, hhf

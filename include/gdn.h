@@ -1,0 +1,150 @@
+/*
+ * gdn.h — C ABI of the GB300 (sm_103a) chunked forward pass of the gated
+ * delta rule (Gated DeltaNet).
+ *
+ * The operation (page "WarpDrive", kernels 3-5 and section "Pipeline", chunk
+ * size C = 64): for every batch b and head h, with a per-head state h of shape
+ * [K, V] carried across the sequence in chunks of 64 tokens,
+ *
+ *   A      = (I + L)^-1, L_ij = beta_i (k_i . k_j) exp(g_i - g_j) for i > j
+ *            (the chunk's "[64,64] WY matrix", kernel 5),
+ *   u      = A (v * beta),  w = A (k * beta * exp(g))          (recompute_w_u, kernel 5)
+ *   per chunk, in order (chunk_fwd_h, kernel 3):
+ *            store h; v_new = u - w @ h; v_gated = v_new * exp(g_last - g_t);
+ *            h *= exp(g_last); h += k^T @ v_gated
+ *   o      = scale * (q @ h * exp(g)) + causal(q @ k^T * exp(g_i - g_j)) @ v_new
+ *            with the causal mask i >= j                     (chunk_fwd_o, kernel 4)
+ *
+ * which equals, token by token, S <- exp(gamma_t) S; S += k_t (beta_t (v_t - S^T k_t))^T;
+ * o_t = scale S^T q_t with h0 the state before the first token and h_final
+ * the state after the last.
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor argument is a DEVICE pointer on the current CUDA device,
+ *    contiguous, row-major, 16-byte aligned. The caller owns all memory; the
+ *    library allocates nothing and keeps no mutable global state between
+ *    calls. Calls on different streams are independent as long as each has its
+ *    own workspace.
+ *  - Layouts: q, k [B,T,H,K]; v, o [B,T,H,V]; g, beta [B,T,H] fp32;
+ *    h0, h_final [B,H,K,V] fp32.
+ *  - g is the per-token log-decay summed cumulatively *within each 64-token
+ *    chunk* (restarting at t = 0, 64, 128, ...). Values should be <= 0 and
+ *    non-increasing inside a chunk; exp(g_i - g_j) is only evaluated for i >= j.
+ *  - T need not be a multiple of 64: the last chunk is partial and g_last is
+ *    the g of its last valid token. T = 0 is valid: h_final = h0 (or zeros).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously. Argument errors are reported
+ *    synchronously before anything is enqueued; a launch error is reported as
+ *    GDN_ERR_CUDA. No C++ exception crosses this boundary.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,    /* NULL required pointer, negative size, bad enum */
+    GDN_ERR_UNSUPPORTED = 2,    /* shape or dtype/algorithm combination not built */
+    GDN_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+    GDN_ERR_WORKSPACE = 4,      /* workspace NULL or smaller than required */
+    GDN_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+    GDN_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait gave up */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum {
+    GDN_ALGO_AUTO = 0,   /* fastest built path for the problem */
+    GDN_ALGO_SIMT = 1,   /* CUDA-core fp32 pipeline, four kernels, any dtype */
+    GDN_ALGO_TC = 2      /* tensor-core (tcgen05/TMEM, TMA) path, bf16 only */
+} gdn_algo;
+
+/* Problem description. K in {64, 128}; V a multiple of 64 in [64, 256];
+ * dtype is the element type of q, k, v and o. */
+typedef struct {
+    int32_t B, T, H, K, V;
+    int32_t dtype;   /* gdn_dtype */
+    int32_t algo;    /* gdn_algo */
+} gdn_problem;
+
+/* Bytes of device workspace gdn_chunk_fwd needs for this problem (0 if the
+ * problem is invalid). The workspace is scratch: its contents on entry do not
+ * matter and are undefined on exit, except where gdn_chunk_fwd_stages says. */
+GDN_API size_t gdn_chunk_fwd_workspace_bytes(const gdn_problem *p);
+
+/* Chunked forward. q, k, v, g, beta, o are required; h0 == NULL means a zero
+ * initial state; h_final == NULL means the final state is not written.
+ * scale multiplies both the inter-chunk (q @ h) and intra-chunk terms of o.
+ * o is written in `dtype` (round to nearest even from fp32); h_final in fp32. */
+GDN_API gdn_status gdn_chunk_fwd(const gdn_problem *p,
+                                 const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float scale,
+                                 const float *h0, void *o, float *h_final,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Stage export for testing: same computation as gdn_chunk_fwd, then copies the
+ * intermediates of the four-stage pipeline into the given device buffers
+ * (each may be NULL = not exported), all fp32 and indexed with T_pad =
+ * ceil(T/64)*64 rows per (b, h) (rows >= T are padding):
+ *   A     [B,T_pad,H,64]  the chunk's WY matrix, row t, column = token index in its chunk
+ *   w     [B,T_pad,H,K]   u [B,T_pad,H,V]   v_new [B,T_pad,H,V] (ungated)
+ *   h     [B,NT,H,K,V]    the state entering each chunk, NT = ceil(T/64)
+ * Returns GDN_ERR_UNSUPPORTED for an algorithm that never materialises the
+ * requested stage. */
+typedef struct {
+    float *A, *w, *u, *v_new, *h;
+} gdn_stage_exports;
+
+GDN_API gdn_status gdn_chunk_fwd_stages(const gdn_problem *p,
+                                        const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta, float scale,
+                                        const float *h0, void *o, float *h_final,
+                                        void *workspace, size_t workspace_bytes,
+                                        const gdn_stage_exports *ex, void *stream);
+
+/* Number of kernels one gdn_chunk_fwd call on this problem launches, in launch
+ * order (0 if the problem is invalid); names[i] receives a static name of
+ * kernel i when names != NULL and i < max_names. */
+GDN_API int32_t gdn_chunk_fwd_launches(const gdn_problem *p, const char **names,
+                                       int32_t max_names);
+
+/* gdn_chunk_fwd with timing markers for measurement: `events` holds
+ * n_events >= gdn_chunk_fwd_launches(p) + 1 cudaEvent_t handles created by the
+ * caller; events[0] is recorded on `stream` before the first kernel and
+ * events[i + 1] right after kernel i. Same results as gdn_chunk_fwd. */
+GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p,
+                                          const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta, float scale,
+                                          const float *h0, void *o, float *h_final,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *const *events, int32_t n_events, void *stream);
+
+/* Waits for `stream`, then reads and clears the device status word kept in the
+ * first bytes of `workspace`: GDN_ERR_DEVICE_TIMEOUT if a bounded device wait
+ * of an earlier call on this workspace gave up, GDN_OK otherwise (or
+ * GDN_ERR_CUDA if the stream itself reports an error). */
+GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream);
+
+/* Static description of a status code. Never NULL. */
+GDN_API const char *gdn_status_string(gdn_status s);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+GDN_API uint32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,99 @@
+"""The C-ABI library on the CPU: it loads, exports every function include/gdn.h
+declares, sizes its workspace and rejects bad arguments before touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from gated_delta_rule_35_gb300 import native
+
+HEADER = Path(__file__).resolve().parents[1] / "include" / "gdn.h"
+FAKE = 0x10000   # an aligned non-NULL address; never dereferenced by validation
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "gdn_chunk_fwd" in names and len(names) >= 5
+    lib = native.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(native.EXPORTS) >= set(names)
+
+
+def test_version_and_status_strings():
+    assert native.lib().gdn_version() > 0
+    for s in range(7):
+        assert native.status_string(s)
+    assert native.status_string(99) == "unknown status"
+
+
+def _call(p, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, o=FAKE, hf=None, ws=FAKE,
+          ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = 0
+    vp = ctypes.c_void_p
+    return native.lib().gdn_chunk_fwd(ctypes.byref(p) if p is not None else None, vp(q), vp(k),
+                                      vp(v), vp(g), vp(beta), 1.0, vp(h0), vp(o), vp(hf), vp(ws),
+                                      ws_bytes, None)
+
+
+def test_workspace_bytes():
+    p = native.problem(4, 2048, 16, 128, 128, native.GDN_BF16, "simt")
+    n = native.workspace_bytes(p)
+    # fp32 A, w, u, v_new, per-chunk h, plus the status word
+    rows = 4 * 2048 * 16
+    assert n >= rows * (64 + 128 + 128 + 128) * 4 + 4 * 32 * 16 * 128 * 128 * 4
+    assert native.workspace_bytes(native.problem(4, 2048, 16, 96, 128, 1)) == 0   # K unsupported
+    assert native.workspace_bytes(native.problem(1, 0, 1, 64, 64, 0)) > 0          # T = 0 valid
+
+
+@pytest.mark.parametrize("shape,status", [
+    ((0, 64, 1, 64, 64), native.GDN_ERR_INVALID_ARG),
+    ((1, -1, 1, 64, 64), native.GDN_ERR_INVALID_ARG),
+    ((1, 64, 0, 64, 64), native.GDN_ERR_INVALID_ARG),
+    ((1, 64, 1, 32, 64), native.GDN_ERR_UNSUPPORTED),
+    ((1, 64, 1, 64, 96), native.GDN_ERR_UNSUPPORTED),
+    ((1, 64, 1, 64, 320), native.GDN_ERR_UNSUPPORTED),
+])
+def test_rejects_bad_shapes(shape, status):
+    assert _call(native.problem(*shape, native.GDN_F32, "simt")) == status
+
+
+def test_rejects_bad_enums_and_null():
+    assert _call(None) == native.GDN_ERR_INVALID_ARG
+    p = native.Problem(1, 64, 1, 64, 64, 7, 0)
+    assert _call(p) == native.GDN_ERR_INVALID_ARG
+    p = native.Problem(1, 64, 1, 64, 64, 0, 9)
+    assert _call(p) == native.GDN_ERR_INVALID_ARG
+    p = native.problem(1, 64, 1, 64, 64, native.GDN_F32, "simt")
+    for field in ("q", "k", "v", "g", "beta", "o"):
+        assert _call(p, **{field: None}) == native.GDN_ERR_INVALID_ARG, field
+
+
+def test_rejects_misaligned_pointers():
+    p = native.problem(1, 64, 1, 64, 64, native.GDN_F32, "simt")
+    for field in ("q", "k", "v", "g", "beta", "o", "h0", "hf", "ws"):
+        assert _call(p, **{field: FAKE + 4}) == native.GDN_ERR_ALIGNMENT, field
+
+
+def test_rejects_small_workspace():
+    p = native.problem(2, 100, 3, 64, 64, native.GDN_BF16, "simt")
+    need = native.workspace_bytes(p)
+    assert _call(p, ws_bytes=need - 1) == native.GDN_ERR_WORKSPACE
+    assert _call(p, ws=None, ws_bytes=need) == native.GDN_ERR_WORKSPACE
+
+
+def test_stage_export_needs_exports():
+    p = native.problem(1, 64, 1, 64, 64, native.GDN_F32, "simt")
+    vp = ctypes.c_void_p
+    st = native.lib().gdn_chunk_fwd_stages(ctypes.byref(p), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                           vp(FAKE), 1.0, None, vp(FAKE), None, vp(FAKE), 1 << 30,
+                                           None, None)
+    assert st == native.GDN_ERR_INVALID_ARG
+    assert native.lib().gdn_check_device_status(None, None) == native.GDN_ERR_INVALID_ARG
