@@ -23,7 +23,7 @@ CHUNK = 64
 # Every function include/gdn.h declares.
 EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stages",
            "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
-           "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_noalloc", "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -205,3 +205,25 @@ def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_s
         hhf.copy_(hf, non_blocking=True)
     torch.cuda.current_stream(dev).synchronize()
     return ho, hhf
+
+
+def chunk_fwd_noalloc(q, k, v, g, beta, scale: float = 1.0, h0=None, out=None, final_state=None,
+                      stream=None):
+    """gdn_chunk_fwd_noalloc: the forward with the library's fixed device scratch
+    instead of a workspace, for callers that cannot allocate device memory. The
+    caller passes preallocated ``out`` [B,T,H,V] and ``final_state`` [B,H,K,V]
+    (or None to skip h_final); without ``out`` this wrapper allocates it."""
+    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
+    L = lib()
+    f = L.gdn_chunk_fwd_noalloc
+    vp = ctypes.c_void_p
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+    p = problem(B, T, H, K, V, q.dtype, "simt")
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    st = f(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
+           _ptr(o), _ptr(final_state), ctypes.c_void_p(s.cuda_stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd_noalloc")
+    return o, final_state

@@ -137,6 +137,34 @@ GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p,
  * GDN_ERR_CUDA if the stream itself reports an error). */
 GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream);
 
+/* gdn_chunk_fwd without a workspace argument, for callers that cannot allocate
+ * device memory at all: code running where cudaMalloc is unavailable or
+ * forbidden (a plugin handed only its input and output buffers by a host
+ * framework that owns every allocation, or code that must not allocate after
+ * start-up). The method's pages have no counterpart to this call; it is a
+ * deployment convenience.
+ *
+ * The scratch lives in a fixed 64 MiB array inside the library's device image,
+ * present on every GPU that loads the library until the process exits. It runs
+ * the CUDA-core (SIMT) pipeline; p->algo must be GDN_ALGO_AUTO or
+ * GDN_ALGO_SIMT (else GDN_ERR_UNSUPPORTED). Problems whose SIMT workspace
+ * (gdn_chunk_fwd_workspace_bytes with algo SIMT) exceeds 64 MiB are rejected
+ * with GDN_ERR_WORKSPACE before anything is enqueued. Nothing here calls
+ * cudaMalloc, cudaFree or an allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current) and may load the library's device code,
+ * so make that first call before any stream capture. Every call on a device
+ * shares the one array: calls whose work overlaps on the GPU (on different
+ * streams, or from different threads) race and give wrong results; serialise
+ * them. The array keeps the last call's contents; no call depends on them.
+ * Pointer conventions, layouts and other errors are those of gdn_chunk_fwd. */
+GDN_API gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p,
+                                         const void *q, const void *k, const void *v,
+                                         const float *g, const float *beta, float scale,
+                                         const float *h0, void *o, float *h_final,
+                                         void *stream);
+
 /* Static description of a status code. Never NULL. */
 GDN_API const char *gdn_status_string(gdn_status s);
 
