@@ -73,11 +73,13 @@ def _fused(K, V, d):
 
 
 KERNEL_MODEL = {
+    "gdn_fused_tc_kernel": ("hbm", _fused),
     "wy_prepare_kernel": ("alu", _simt_prepare),
     "chunk_h_kernel": ("alu", _simt_h),
     "chunk_o_kernel": ("alu", _simt_o),
 }
 KERNEL_SOURCE = {
+    "gdn_fused_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc.cu",
     "wy_prepare_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
     "chunk_h_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
     "chunk_o_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
