@@ -49,7 +49,9 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
     const gdn_algo algo = resolve_algo(p);
-    if (ex && algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
+    if (ex && algo == GDN_ALGO_TC && (ex->A || ex->w || ex->u || ex->v_new || ex->h))
+        return GDN_ERR_UNSUPPORTED;
+    if (ex && algo == GDN_ALGO_SIMT && ex->A_beta) return GDN_ERR_UNSUPPORTED;
     const size_t need = kStatusBytes + body_bytes(p, algo);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
 
@@ -70,6 +72,7 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         if (e == cudaSuccess) e = marks.mark(1, stream);
     } else if (algo == GDN_ALGO_TC) {
         e = tc_forward(a, body, stream, marks);
+        if (e == cudaSuccess && ex && ex->A_beta) e = tc_export_abeta(a, body, ex->A_beta, stream);
     } else {
         const SimtWorkspace ws = simt_carve(body, a.B, a.T, a.H, a.K, a.V);
         e = simt_forward(a, ws, stream, marks);

@@ -53,6 +53,10 @@ bool tc_supported(int K, int V, gdn_dtype dtype);
 size_t tc_workspace_bytes(int B, int T, int H, int K, int V);
 cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m);
 int tc_launches(const char **names, int max_names);
+// WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.
+cudaError_t wy_tc_forward(const Args &a, void *abeta, cudaStream_t s);
+// Converts the workspace's A diag(beta) to fp32 [B, T_pad, H, 64].
+cudaError_t tc_export_abeta(const Args &a, const void *ws, float *dst, cudaStream_t s);
 
 // h_final = h0 (or 0) for T == 0.
 cudaError_t copy_state(const Args &a, cudaStream_t s);

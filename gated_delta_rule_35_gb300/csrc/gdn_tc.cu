@@ -1,21 +1,22 @@
 // Tensor-core path of the chunked gated delta rule forward for bf16 q, k, v.
 //
-// One kernel fuses the whole pipeline of the "WarpDrive" page (kernel 5
-// recompute_w_u with its WY matrix, kernel 3 chunk_fwd_h, kernel 4
-// chunk_fwd_o). One CTA owns one (b, h, 64-wide V tile) and walks the chunks in
-// order with the [K, 64] slice of the state in registers (fp32) and in shared
-// memory (bf16, the MMA operand), so neither h, A, w, u nor v_new ever reaches
-// HBM: per token it reads q, k, v, g, beta and writes o.
+// Two kernels, following the "WarpDrive" page's pipeline (kernel 5
+// recompute_w_u takes the chunk's WY matrix A as given; kernels 3 chunk_fwd_h
+// and 4 chunk_fwd_o follow it):
+//   1. gdn_wy_tc_kernel (gdn_tc_wy.cu): A diag(beta) for every chunk, in
+//      parallel over all chunks, to a bf16 workspace [B, T, H, 64].
+//   2. gdn_fused_tc_kernel (this file): recompute_w_u, chunk_fwd_h and
+//      chunk_fwd_o fused. One CTA owns one (b, h, 64-wide V tile) and walks the
+//      chunks in order with its [K, 64] slice of the state in registers (fp32)
+//      and in shared memory (bf16, the MMA operand); h, w, u and v_new never
+//      reach HBM.
 //
-// Per chunk (C = 64 tokens), with D_* accumulators in tensor memory:
-//   TMA      q, k [64 x K] and the v tile [64 x 64] (rows past T read as 0)
-//   MMA_G    D_G[128 x 64] = [k; q] k^T                      (Gram and q k^T)
-//   epi G    L_ij = beta_i G_ij exp(g_i - g_j), i > j (fp32, smem)
-//            P_ij = scale (q_i.k_j) exp(g_i - g_j), i >= j (bf16 operand)
-//   inverse  A = (I + L)^-1: 16x16 diagonal blocks by forward substitution,
-//            then two block-merge levels, fp32 on the CUDA cores
-//            A' = A diag(beta exp(g)), A'' = A diag(beta) (bf16 operands)
-//   MMA_W    D_W = A' k   (= w)       MMA_U  D_U = A'' v (= u)
+// Per chunk (C = 64 tokens), D_* accumulators in tensor memory:
+//   TMA      q, k [64 x K], the v tile [64 x 64], A diag(beta) [64 x 64] (rows past T read 0)
+//   MMA_QK   D_QK = q k^T
+//   epi P    P_ij = scale (q_i.k_j) exp(g_i - g_j), i >= j  -> bf16 operand
+//            k_hat = exp(g) * k                             -> bf16 operand
+//   MMA_W    D_W = A diag(beta) k_hat   (= w)    MMA_U  D_U = A diag(beta) v (= u)
 //   MMA_QH   D_QH = q h
 //   epi W    w -> bf16 operand
 //   MMA_X    D_U += (-w) h            (= v_new, negated-A MMA)
@@ -23,14 +24,8 @@
 //   MMA_PV   D_PV = P v_new           MMA_H  D_H = k^T (v_new * exp(g_last - g_t))
 //   epi H    h = h * exp(g_last) + D_H (fp32 registers), bf16 copy for the next chunk
 //   epi O    o = scale exp(g_t) D_QH + D_PV -> bf16 -> TMA store
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_bf16.h>
-
-#include <mutex>
-
 #include "gdn_internal.h"
-#include "sm100_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gdn {
 namespace {
@@ -43,130 +38,29 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 
 // Shared-memory map (bytes from a 1024-aligned base). Regions reused within a
-// chunk are listed with every role they take, in order.
+// chunk list every role they take, in order.
 template <int K>
 struct TcLayout {
     static constexpr int KB = K / 64;                        // 64-feature blocks
     static constexpr uint32_t kKQ = 0;                       // per block: k rows 0-63 | q rows 0-63
     static constexpr uint32_t kVT = kKQ + KB * 16384;        // v tile -> o staging
-    static constexpr uint32_t kAP = kVT + 8192;              // inverse temps -> A' -> v_new
-    static constexpr uint32_t kAU = kAP + 8192;              // A'' -> v_gated
+    static constexpr uint32_t kAP = kVT + 8192;              // A diag(beta) -> v_new
+    static constexpr uint32_t kAU = kAP + 8192;              // v_gated
     static constexpr uint32_t kPS = kAU + 8192;              // P
-    static constexpr uint32_t kWS = kPS + 8192;              // L/A fp32 (16 KB) -> w bf16
-    static constexpr uint32_t kHS = kWS + 16384;             // h bf16 [K rows x 64]
-    static constexpr uint32_t kMisc = kHS + K * 128;         // g, beta exp(g), beta, barriers
+    static constexpr uint32_t kWS = kPS + 8192;              // k_hat -> w (K/64 blocks of 8 KB)
+    static constexpr uint32_t kHS = kWS + KB * 8192;         // h bf16 [K rows x 64]
+    static constexpr uint32_t kMisc = kHS + K * 128;         // g, barriers
     static constexpr uint32_t kBytes = kMisc + 1024;
 };
 
 // TMEM columns (one 256-column allocation).
-constexpr uint32_t kColW = 0, kColPV = 0, kColH = 64, kColG = 128, kColU = 128, kColQH = 192;
-
-// Strictly-lower fp32 64x64 matrix with an XOR swizzle on the column so that
-// both row-parallel and column-parallel accesses are free of bank conflicts.
-struct Tri64 {
-    float *p;
-    __device__ __forceinline__ float &operator()(int i, int j) const {
-        return p[i * 64 + (j ^ (i & 31))];
-    }
-};
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ void st_shared_v4(unsigned char *p, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b),
-                 "r"(c), "r"(d)
-                 : "memory");
-}
-// Eight fp32 values -> one 16-byte chunk of bf16 at `dst`.
-__device__ __forceinline__ void st_bf16x8(unsigned char *dst, const float *v) {
-    st_shared_v4(dst, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                 pack_bf16(v[6], v[7]));
-}
-
-// A = (I + L)^-1 in place in `L` (strictly lower on entry, unit lower on exit),
-// 128 threads. `tmp` holds >= 32*33 floats.
-__device__ __forceinline__ void invert_unit_lower64(const Tri64 &L, float *tmp, int tid) {
-    // 1) the four 16x16 diagonal blocks: thread (blk, c) solves (I + L_bb) x = e_c
-    float x[16];
-    const int blk = tid >> 4, c = tid & 15, base = blk * 16;
-    if (tid < 64) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < 15; ++j)
-#pragma unroll
-            for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-L(base + i, base + j), x[j], x[i]);
-    }
-    __syncthreads();
-    if (tid < 64) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) L(base + i, base + c) = x[i];
-    }
-    __syncthreads();
-    // 2) blocks (1,0) and (3,2): X_21 = -X_22 L_21 X_11
-    {
-        const int p = tid >> 6, idx = tid & 63, i = idx >> 2, j0 = (idx & 3) * 4;
-        const int rb = 16 * (2 * p + 1), cb = 32 * p;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float l = L(rb + i, cb + k);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(l, L(cb + k, cb + j0 + e), acc[e]);
-        }
-        float *T1 = tmp + p * 16 * 17;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) T1[i * 17 + j0 + e] = acc[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float xh = L(rb + i, rb + k);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(xh, T1[k * 17 + j0 + e], acc[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) L(rb + i, cb + j0 + e) = -acc[e];
-    }
-    __syncthreads();
-    // 3) bottom-left 32x32: X_BL = -X_BR L_BL X_TL
-    {
-        const int i = tid >> 2, j0 = (tid & 3) * 8;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float l = L(32 + i, k);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(l, L(k, j0 + e), acc[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tmp[i * 33 + j0 + e] = acc[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float xb = L(32 + i, 32 + k);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(xb, tmp[k * 33 + j0 + e], acc[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) L(32 + i, j0 + e) = -acc[e];
-    }
-    __syncthreads();
-}
+constexpr uint32_t kColW = 0, kColPV = 0, kColH = 64, kColQK = 128, kColU = 128, kColQH = 192;
 
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const float *__restrict__ g, const float *__restrict__ beta,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ g,
                     const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V,
                     float scale, uint32_t *status) {
     using Lay = TcLayout<K>;
@@ -174,9 +68,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);   // g
-    float *s1_s = g_s + 64;                                      // beta exp(g)
-    float *s2_s = g_s + 128;                                     // beta
+    float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);   // g (0 past T)
+    float *eg_s = g_s + 64;                                      // exp(g)
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 768);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
@@ -196,6 +89,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_o);
     }
     tc_fence_before_sync();
@@ -208,7 +102,6 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t s_ap = smem_u32(sm + Lay::kAP), s_au = smem_u32(sm + Lay::kAU);
     const uint32_t s_ps = smem_u32(sm + Lay::kPS), s_ws = smem_u32(sm + Lay::kWS);
     const uint32_t s_hs = smem_u32(sm + Lay::kHS);
-    const Tri64 L{reinterpret_cast<float *>(sm + Lay::kWS)};
 
     // Row of the state this thread owns: the M = 128 accumulator puts row i in
     // TMEM lane i; the M = 64 one puts row i in lane 32 (i / 16) + i % 16.
@@ -231,98 +124,79 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int t0 = c * 64, n = min(64, T - t0);
         if (tid == 0) {
             bulk_wait_group_read0();   // the previous o store has left the v-tile region
-            mbar_arrive_expect_tx(bar_tma, KB * 16384 + 8192);
+            mbar_arrive_expect_tx(bar_tma, KB * 16384 + 8192 + 8192);
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
                 tma_load_4d(sm + Lay::kKQ + kb * 16384, &tm_k, bar_tma, kb * 64, h, t0, b);
                 tma_load_4d(sm + Lay::kKQ + kb * 16384 + 8192, &tm_q, bar_tma, kb * 64, h, t0, b);
             }
             tma_load_4d(sm + Lay::kVT, &tm_v, bar_tma, vt * kTcBV, h, t0, b);
+            tma_load_4d(sm + Lay::kAP, &tm_a, bar_tma, 0, h, t0, b);
         }
         if (tid < 64) {
-            float gv = 0.f, bv = 0.f;
-            if (tid < n) {
-                const int64_t r = (static_cast<int64_t>(b) * T + t0 + tid) * H + h;
-                gv = g[r];
-                bv = beta[r];
-            }
+            float gv = 0.f;
+            if (tid < n) gv = g[(static_cast<int64_t>(b) * T + t0 + tid) * H + h];
             g_s[tid] = gv;
-            s1_s[tid] = bv * __expf(gv);
-            s2_s[tid] = bv;
+            eg_s[tid] = tid < n ? __expf(gv) : 0.f;
         }
         fail |= !mbar_wait(bar_tma, ph_tma, kWaitNs);
         ph_tma ^= 1;
         if (__syncthreads_or(fail)) break;
 
-        // ---- MMA_G: [k; q] k^T
+        // ---- MMA_QK: q k^T (M = 64)
         if (tid == 0) {
             tc_fence_after_sync();
-            constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t id = idesc_bf16(64, 64, false, false);
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks) {
                 const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem + kColG, smem_desc(s_kq + off, 16, 1024, kLayoutSw128),
+                mma_bf16(tmem + kColQK, smem_desc(s_kq + off + 8192, 16, 1024, kLayoutSw128),
                          smem_desc(s_kq + off, 16, 1024, kLayoutSw128), id, ks > 0);
             }
             mma_commit(bar_mma);
+        }
+        // ---- k_hat = exp(g) k while the MMA runs (same swizzled positions)
+#pragma unroll
+        for (int it = 0; it < KB * 4; ++it) {
+            const int idx = tid + it * kTcThreads;           // 16-byte chunk of k
+            const int kb = idx >> 9, rem = idx & 511, row = rem >> 3, ch = rem & 7;
+            const uint32_t off = sw128(row, ch * 16);
+            const uint4 raw = ld_shared_v4(sm + Lay::kKQ + kb * 16384 + off);
+            const float s = eg_s[row];
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16(w4[e]);
+                o4[e] = pack_bf16(f.x * s, f.y * s);
+            }
+            st_shared_v4(sm + Lay::kWS + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
         }
         fail |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
         ph_mma ^= 1;
         if (__syncthreads_or(fail)) break;
         tc_fence_after_sync();
 
-        // ---- epilogue G: L (fp32) and P (bf16)
-        {
-            const int i = tid & 63;
-            const float gi = g_s[i];
-            const float bi = s2_s[i];
+        // ---- epilogue P (bf16, K-major rows)
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                uint32_t r[16];
-                tmem_ld16(tmem + kColG + lane_off + blk * 16, r);
-                tmem_wait_ld();
+        for (int blk = 0; blk < 4; ++blk) {
+            uint32_t r[16];
+            tmem_ld16(tmem + kColQK + lane_off + blk * 16, r);
+            tmem_wait_ld();
+            if (row64 >= 0) {
+                const float gi = g_s[row64];
                 float v[16];
-                if (tid < 64) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = blk * 16 + e;
-                        v[e] = (j < i) ? bi * __uint_as_float(r[e]) * __expf(gi - g_s[j]) : 0.f;
-                        L(i, j) = v[e];
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = blk * 16 + e;
-                        v[e] = (j <= i) ? scale * __uint_as_float(r[e]) * __expf(gi - g_s[j]) : 0.f;
-                    }
-                    st_bf16x8(sm + Lay::kPS + sw128(i, blk * 32), v);
-                    st_bf16x8(sm + Lay::kPS + sw128(i, blk * 32 + 16), v + 8);
+                for (int e = 0; e < 16; ++e) {
+                    const int j = blk * 16 + e;
+                    v[e] = (j <= row64) ? scale * __uint_as_float(r[e]) * __expf(gi - g_s[j]) : 0.f;
                 }
+                st_bf16x8(sm + Lay::kPS + sw128(row64, blk * 32), v);
+                st_bf16x8(sm + Lay::kPS + sw128(row64, blk * 32 + 16), v + 8);
             }
-            fence_proxy_async_smem();
         }
+        fence_proxy_async_smem();
         tc_fence_before_sync();
-        __syncthreads();
-
-        // ---- A = (I + L)^-1, then A' = A diag(beta exp(g)), A'' = A diag(beta)
-        invert_unit_lower64(L, reinterpret_cast<float *>(sm + Lay::kAP), tid);
-        {
-            const int i = tid >> 1, half = tid & 1;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const int j0 = half * 32 + ch * 8;
-                float a1[8], a2[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float a = L(i, j0 + e);
-                    a1[e] = a * s1_s[j0 + e];
-                    a2[e] = a * s2_s[j0 + e];
-                }
-                st_bf16x8(sm + Lay::kAP + sw128(i, j0 * 2), a1);
-                st_bf16x8(sm + Lay::kAU + sw128(i, j0 * 2), a2);
-            }
-            fence_proxy_async_smem();
-        }
         __syncthreads();
 
         // ---- MMA_W, MMA_U, MMA_QH
@@ -333,10 +207,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem + kColW, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
-                         smem_desc(s_kq + ks * 2048, 16384, 1024, kLayoutSw128), idW, ks > 0);
+                         smem_desc(s_ws + ks * 2048, 8192, 1024, kLayoutSw128), idW, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kColU, smem_desc(s_au + ks * 32, 16, 1024, kLayoutSw128),
+                mma_bf16(tmem + kColU, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
                          smem_desc(s_vt + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks)
@@ -454,7 +328,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         // ---- epilogue O: o = scale exp(g_t) q h + P v_new -> bf16 staging -> TMA store
         {
-            const float so = (row64 >= 0) ? scale * __expf(g_s[row64]) : 0.f;
+            const float so = (row64 >= 0) ? scale * eg_s[row64] : 0.f;
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t rq[16], rp[16];
@@ -493,51 +367,35 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// [B, T, H, inner] bf16 viewed as a 4-D tensor (inner, H, T, B); box 64 x 1 x 64 x 1,
-// 128-byte swizzle. Rows t >= T fall outside the tensor: loads read zeros and
-// stores skip them.
-bool make_map(CUtensorMap *m, const void *ptr, int inner, int H, int T, int B) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(H),
-                                static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(inner) * 2,
-                                   static_cast<cuuint64_t>(H) * inner * 2,
-                                   static_cast<cuuint64_t>(T) * H * inner * 2};
-    const cuuint32_t box[4] = {64, 1, 64, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// Stage export: A diag(beta) bf16 [B, T, H, 64] -> fp32 [B, T_pad, H, 64] (pad rows 0).
+__global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float *__restrict__ dst,
+                                    int B, int T, int T_pad, int H) {
+    const int64_t n = static_cast<int64_t>(B) * T_pad * H * 64;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / 64;   // (b, t, h) in the padded layout
+        const int hh = static_cast<int>(row % H);
+        const int64_t bt = row / H;
+        const int t = static_cast<int>(bt % T_pad), bb = static_cast<int>(bt / T_pad);
+        dst[i] = t < T ? __bfloat162float(src[((static_cast<int64_t>(bb) * T + t) * H + hh) * 64 + i % 64])
+                       : 0.f;
+    }
 }
 
 template <int K>
-cudaError_t launch_tc(const Args &a, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, a.q, K, a.H, a.T, a.B) || !make_map(&mk, a.k, K, a.H, a.T, a.B) ||
-        !make_map(&mv, a.v, a.V, a.H, a.T, a.B) || !make_map(&mo, a.o, a.V, a.H, a.T, a.B))
+cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
+    CUtensorMap mq, mk, mv, ma, mo;
+    if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&ma, abeta, 64, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&mo, a.o, a.V, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(TcLayout<K>::kBytes + 1024);
     cudaError_t e = cudaFuncSetAttribute(gdn_fused_tc_kernel<K>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     gdn_fused_tc_kernel<K><<<dim3(a.V / kTcBV, a.H, a.B), kTcThreads, smem, s>>>(
-        mq, mk, mv, mo, a.g, a.beta, a.h0, a.h_final, a.T, a.H, a.V, a.scale, a.status);
+        mq, mk, mv, ma, mo, a.g, a.h0, a.h_final, a.T, a.H, a.V, a.scale, a.status);
     return cudaGetLastError();
 }
 
@@ -547,20 +405,31 @@ bool tc_supported(int K, int V, gdn_dtype dtype) {
     return dtype == GDN_BF16 && (K == 64 || K == 128) && V % kTcBV == 0 && V >= kTcBV;
 }
 
-size_t tc_workspace_bytes(int, int, int, int, int) { return 0; }
-
-int tc_launches(const char **names, int max_names) {
-    if (names && max_names > 0) names[0] = "gdn_fused_tc_kernel";
-    return 1;
+size_t tc_workspace_bytes(int B, int T, int H, int, int) {
+    return align_up(static_cast<size_t>(B) * T * H * 64 * sizeof(__nv_bfloat16));
 }
 
-cudaError_t tc_forward(const Args &a, void *, cudaStream_t s, const Marks &m) {
+int tc_launches(const char **names, int max_names) {
+    static const char *const kNames[2] = {"gdn_wy_tc_kernel", "gdn_fused_tc_kernel"};
+    for (int i = 0; names && i < 2 && i < max_names; ++i) names[i] = kNames[i];
+    return 2;
+}
+
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     if ((e = m.mark(0, s)) != cudaSuccess) return e;
-    e = (a.K == 128) ? launch_tc<128>(a, s) : launch_tc<64>(a, s);
+    if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
+    if ((e = m.mark(1, s)) != cudaSuccess) return e;
+    e = (a.K == 128) ? launch_fused<128>(a, ws, s) : launch_fused<64>(a, ws, s);
     if (e != cudaSuccess) return e;
-    return m.mark(1, s);
+    return m.mark(2, s);
+}
+
+cudaError_t tc_export_abeta(const Args &a, const void *ws, float *dst, cudaStream_t s) {
+    export_abeta_kernel<<<304, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(ws), dst, a.B, a.T,
+                                           a.T_pad, a.H);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

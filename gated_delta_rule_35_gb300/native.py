@@ -40,7 +40,7 @@ class Problem(ctypes.Structure):
 
 class StageExports(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("w", ctypes.c_void_p), ("u", ctypes.c_void_p),
-                ("v_new", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+                ("v_new", ctypes.c_void_p), ("h", ctypes.c_void_p), ("A_beta", ctypes.c_void_p)]
 
 
 _lib = None
@@ -158,17 +158,23 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     return o, hf
 
 
-def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = "simt"):
-    """Forward plus the exported intermediates (A, w, u, v_new, h), all fp32."""
+STAGES = ("A", "w", "u", "v_new", "h", "A_beta")
+
+
+def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = "simt",
+                     stages=("A", "w", "u", "v_new", "h")):
+    """Forward plus the requested exported intermediates (fp32 tensors): A, w, u,
+    v_new, h (SIMT path) or A_beta = A diag(beta) (tensor-core path)."""
     B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
     p = problem(B, T, H, K, V, q.dtype, algo)
     NT = (T + CHUNK - 1) // CHUNK
     Tp = NT * CHUNK
     f32 = dict(dtype=torch.float32, device=q.device)
-    st_bufs = {"A": torch.empty((B, Tp, H, CHUNK), **f32), "w": torch.empty((B, Tp, H, K), **f32),
-               "u": torch.empty((B, Tp, H, V), **f32), "v_new": torch.empty((B, Tp, H, V), **f32),
-               "h": torch.empty((B, NT, H, K, V), **f32)}
-    ex = StageExports(*(ctypes.c_void_p(st_bufs[n].data_ptr()) for n in ("A", "w", "u", "v_new", "h")))
+    shapes = {"A": (B, Tp, H, CHUNK), "w": (B, Tp, H, K), "u": (B, Tp, H, V),
+              "v_new": (B, Tp, H, V), "h": (B, NT, H, K, V), "A_beta": (B, Tp, H, CHUNK)}
+    st_bufs = {n: torch.empty(shapes[n], **f32) for n in stages}
+    ex = StageExports(*(ctypes.c_void_p(st_bufs[n].data_ptr()) if n in st_bufs else None
+                        for n in STAGES))
     need = workspace_bytes(p)
     ws = torch.empty(need, dtype=torch.uint8, device=q.device)
     o = torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)

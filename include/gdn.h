@@ -95,16 +95,18 @@ GDN_API gdn_status gdn_chunk_fwd(const gdn_problem *p,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* Stage export for testing: same computation as gdn_chunk_fwd, then copies the
- * intermediates of the four-stage pipeline into the given device buffers
- * (each may be NULL = not exported), all fp32 and indexed with T_pad =
- * ceil(T/64)*64 rows per (b, h) (rows >= T are padding):
- *   A     [B,T_pad,H,64]  the chunk's WY matrix, row t, column = token index in its chunk
- *   w     [B,T_pad,H,K]   u [B,T_pad,H,V]   v_new [B,T_pad,H,V] (ungated)
- *   h     [B,NT,H,K,V]    the state entering each chunk, NT = ceil(T/64)
- * Returns GDN_ERR_UNSUPPORTED for an algorithm that never materialises the
- * requested stage. */
+ * intermediates of the pipeline into the given device buffers (each may be
+ * NULL = not exported), all fp32 and indexed with T_pad = ceil(T/64)*64 rows
+ * per (b, h) (rows >= T are padding):
+ *   A      [B,T_pad,H,64]  the chunk's WY matrix, row t, column = token index in its chunk
+ *   w      [B,T_pad,H,K]   u [B,T_pad,H,V]   v_new [B,T_pad,H,V] (ungated)
+ *   h      [B,NT,H,K,V]    the state entering each chunk, NT = ceil(T/64)
+ *   A_beta [B,T_pad,H,64]  A diag(beta), the WY stage the tensor-core path keeps (bf16 there)
+ * The SIMT path materialises A, w, u, v_new and h; the tensor-core path only
+ * A_beta. Requesting a stage the chosen path never materialises returns
+ * GDN_ERR_UNSUPPORTED before anything is enqueued. */
 typedef struct {
-    float *A, *w, *u, *v_new, *h;
+    float *A, *w, *u, *v_new, *h, *A_beta;
 } gdn_stage_exports;
 
 GDN_API gdn_status gdn_chunk_fwd_stages(const gdn_problem *p,

@@ -87,6 +87,33 @@ def test_simt_stages_against_chunked_form(dtype):
     assert rel(st["o"].float().cpu().numpy(), ref["o"]) < TOL[dtype]
 
 
+@pytest.mark.parametrize("K", [64, 128])
+def test_tc_wy_stage_against_chunked_form(K):
+    """The tensor-core WY stage, A diag(beta) per chunk (bf16 in the workspace),
+    against the fp64 chunked form's A with its columns scaled by beta."""
+    if not have_algo("tc", K, 128, "bf16"):
+        pytest.skip("not built")
+    T = 150
+    x = make_inputs(2, T, 2, K, 128, dtype="bf16", seed=6)
+    d = gpu(x)
+    st = chunk_fwd_stages(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None, algo="tc",
+                          stages=("A_beta",))
+    torch.cuda.synchronize()
+    ref = chunked.forward(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), to_f64(x["g"]),
+                          to_f64(x["beta"]), 1.0, None, stages=True)
+    beta = to_f64(x["beta"])
+    B, _, H = beta.shape
+    cols = np.zeros((B, T, H, 64))
+    for t in range(T):
+        s = (t // 64) * 64
+        e = min(T, s + 64)
+        cols[:, t, :, : e - s] = beta[:, s:e, :].transpose(0, 2, 1)
+    want = ref["A"] * cols
+    got = st["A_beta"][:, :T].cpu().numpy()
+    assert rel(got, want) < 1e-2, rel(got, want)
+    assert np.all(st["A_beta"][:, T:].cpu().numpy() == 0)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 def test_empty_sequence(algo):
     """T = 0: no output rows; h_final = h0, or zeros without h0."""
