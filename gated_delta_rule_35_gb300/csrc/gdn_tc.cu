@@ -32,29 +32,60 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTcThreads = 128;
+// 20 warps: 0 MMA issuer, 1 TMA producer, 2-3 scale group, 4-11 prep group, 12-19 chain group
+constexpr int kTcThreads = 640;
+constexpr int kScaleThreads = 64, kPrepThreads = 256, kChainThreads = 256;
 constexpr int kTcBV = 64;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 
-// Shared-memory map (bytes from a 1024-aligned base). Regions reused within a
-// chunk list every role they take, in order.
+// Shared-memory map (bytes from a 1024-aligned base).
 template <int K>
 struct TcLayout {
-    static constexpr int KB = K / 64;                        // 64-feature blocks
-    static constexpr uint32_t kKQ = 0;                       // per block: k rows 0-63 | q rows 0-63
-    static constexpr uint32_t kVT = kKQ + KB * 16384;        // v tile -> o staging
-    static constexpr uint32_t kAP = kVT + 8192;              // A diag(beta) -> v_new
-    static constexpr uint32_t kAU = kAP + 8192;              // v_gated
-    static constexpr uint32_t kPS = kAU + 8192;              // P
-    static constexpr uint32_t kWS = kPS + 8192;              // k_hat -> w (K/64 blocks of 8 KB)
-    static constexpr uint32_t kHS = kWS + KB * 8192;         // h bf16 [K rows x 64]
-    static constexpr uint32_t kMisc = kHS + K * 128;         // g, barriers
-    static constexpr uint32_t kBytes = kMisc + 1024;
+    static constexpr int KB = K / 64;                            // 64-feature blocks
+    // two input stages: per 64-feature block k rows | q rows, then v tile, then A diag(beta)
+    static constexpr uint32_t kStage = KB * 16384 + 16384;
+    static constexpr uint32_t kV = KB * 16384, kAb = kV + 8192;  // offsets inside a stage
+    static constexpr uint32_t kKH = 2 * kStage;                   // exp(g) k, KB x 8 KB
+    static constexpr uint32_t kW = kKH + KB * 8192;               // w, KB x 8 KB
+    static constexpr uint32_t kP = kW + KB * 8192;                // P, two buffers of 8 KB
+    static constexpr uint32_t kHS = kP + 16384;                   // h bf16 [K rows x 64]
+    static constexpr uint32_t kVN = kHS + K * 128;                // v_new
+    static constexpr uint32_t kVG = kVN + 8192;                   // v_new exp(g_last - g)
+    static constexpr uint32_t kOS = kVG + 8192;                   // o staging for the TMA store
+    static constexpr uint32_t kG = kOS + 8192;                    // g[2][64], exp(g)[2][64]
+    static constexpr uint32_t kBar = kG + 1024;                   // mbarriers, flags
+    static constexpr uint32_t kBytes = kBar + 256;
 };
 
-// TMEM columns (one 256-column allocation).
-constexpr uint32_t kColW = 0, kColPV = 0, kColH = 64, kColQK = 128, kColU = 128, kColQH = 192;
+// TMEM columns of the 512-column allocation.
+constexpr uint32_t kColQK = 0, kColW = 64, kColU0 = 192, kColQH = 320, kColPV = 384, kColH = 448;
+
+struct Bars {
+    uint64_t full[2], empty[2];      // TMA stage filled / released
+    uint64_t qk_done, w_done, x_done, h_done;   // MMA completions (tcgen05.commit)
+    uint64_t g_ready, kh_ready;                 // scale group: g in place, exp(g) k written
+    uint64_t p_ready, w_ready;                  // prep group: operands written
+    uint64_t hs_ready, vn_ready, o_free;        // chain group (128 arrivals)
+    uint32_t abort, tmem;
+};
+
+// Bounded wait: false if another role aborted or the limit passed (then aborts).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -65,26 +96,40 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float scale, uint32_t *status) {
     using Lay = TcLayout<K>;
     constexpr int KB = K / 64;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);   // g (0 past T)
-    float *eg_s = g_s + 64;                                      // exp(g)
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 768);
-    uint64_t *bar_mma = bar_tma + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned base, derived by offsetting the shared array itself so
+    // that every access through it stays a shared-memory access.
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float *g_s = reinterpret_cast<float *>(sm + Lay::kG);   // [2][64] g (0 past T)
+    float *eg_s = g_s + 128;                                 // [2][64] exp(g) (0 past T)
+    Bars *bs = reinterpret_cast<Bars *>(sm + Lay::kBar);
+    volatile uint32_t *abort = &bs->abort;
 
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (T + 63) / 64;
 
     if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(&bs->tmem, kTmemCols);
         tmem_relinquish();
     }
-    if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+    if (tid == 32) {
+        mbar_init(&bs->full[0], 1);
+        mbar_init(&bs->full[1], 1);
+        mbar_init(&bs->empty[0], 1);
+        mbar_init(&bs->empty[1], 1);
+        mbar_init(&bs->qk_done, 1);
+        mbar_init(&bs->w_done, 1);
+        mbar_init(&bs->x_done, 1);
+        mbar_init(&bs->h_done, 1);
+        mbar_init(&bs->g_ready, kScaleThreads);
+        mbar_init(&bs->kh_ready, kScaleThreads);
+        mbar_init(&bs->p_ready, kPrepThreads);
+        mbar_init(&bs->w_ready, kPrepThreads);
+        mbar_init(&bs->hs_ready, kChainThreads);
+        mbar_init(&bs->vn_ready, kChainThreads);
+        mbar_init(&bs->o_free, kChainThreads);
+        bs->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -95,180 +140,264 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tmem = bs->tmem;
+    const uint32_t s_base = smem_u32(sm);
 
-    const uint32_t s_kq = smem_u32(sm + Lay::kKQ), s_vt = smem_u32(sm + Lay::kVT);
-    const uint32_t s_ap = smem_u32(sm + Lay::kAP), s_au = smem_u32(sm + Lay::kAU);
-    const uint32_t s_ps = smem_u32(sm + Lay::kPS), s_ws = smem_u32(sm + Lay::kWS);
-    const uint32_t s_hs = smem_u32(sm + Lay::kHS);
-
-    // Row of the state this thread owns: the M = 128 accumulator puts row i in
-    // TMEM lane i; the M = 64 one puts row i in lane 32 (i / 16) + i % 16.
-    const int feat = (K == 128) ? tid : (lane < 16 ? warp * 16 + lane : -1);
-    const int row64 = lane < 16 ? warp * 16 + lane : -1;   // row of M = 64 accumulators
-    const int64_t state_off = (static_cast<int64_t>(b) * H + h) * K * V + vt * kTcBV;
-    float hreg[kTcBV];
-#pragma unroll
-    for (int j = 0; j < kTcBV; ++j)
-        hreg[j] = (feat >= 0 && h0) ? h0[state_off + static_cast<int64_t>(feat) * V + j] : 0.f;
-    if (feat >= 0) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_bf16x8(sm + Lay::kHS + sw128(feat, ch * 16), &hreg[ch * 8]);
-    }
-    fence_proxy_async_smem();
-
-    uint32_t ph_tma = 0, ph_mma = 0;
-    bool fail = false;
-    for (int c = 0; c < NT; ++c) {
-        const int t0 = c * 64, n = min(64, T - t0);
-        if (tid == 0) {
-            bulk_wait_group_read0();   // the previous o store has left the v-tile region
-            mbar_arrive_expect_tx(bar_tma, KB * 16384 + 8192 + 8192);
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb) {
-                tma_load_4d(sm + Lay::kKQ + kb * 16384, &tm_k, bar_tma, kb * 64, h, t0, b);
-                tma_load_4d(sm + Lay::kKQ + kb * 16384 + 8192, &tm_q, bar_tma, kb * 64, h, t0, b);
-            }
-            tma_load_4d(sm + Lay::kVT, &tm_v, bar_tma, vt * kTcBV, h, t0, b);
-            tma_load_4d(sm + Lay::kAP, &tm_a, bar_tma, 0, h, t0, b);
-        }
-        if (tid < 64) {
-            float gv = 0.f;
-            if (tid < n) gv = g[(static_cast<int64_t>(b) * T + t0 + tid) * H + h];
-            g_s[tid] = gv;
-            eg_s[tid] = tid < n ? __expf(gv) : 0.f;
-        }
-        fail |= !mbar_wait(bar_tma, ph_tma, kWaitNs);
-        ph_tma ^= 1;
-        if (__syncthreads_or(fail)) break;
-
-        // ---- MMA_QK: q k^T (M = 64)
-        if (tid == 0) {
-            tc_fence_after_sync();
-            constexpr uint32_t id = idesc_bf16(64, 64, false, false);
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem + kColQK, smem_desc(s_kq + off + 8192, 16, 1024, kLayoutSw128),
-                         smem_desc(s_kq + off, 16, 1024, kLayoutSw128), id, ks > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        // ---- k_hat = exp(g) k while the MMA runs (same swizzled positions)
-#pragma unroll
-        for (int it = 0; it < KB * 4; ++it) {
-            const int idx = tid + it * kTcThreads;           // 16-byte chunk of k
-            const int kb = idx >> 9, rem = idx & 511, row = rem >> 3, ch = rem & 7;
-            const uint32_t off = sw128(row, ch * 16);
-            const uint4 raw = ld_shared_v4(sm + Lay::kKQ + kb * 16384 + off);
-            const float s = eg_s[row];
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t o4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16(w4[e]);
-                o4[e] = pack_bf16(f.x * s, f.y * s);
-            }
-            st_shared_v4(sm + Lay::kWS + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
-        }
-        fail |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(fail)) break;
-        tc_fence_after_sync();
-
-        // ---- epilogue P (bf16, K-major rows)
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            uint32_t r[16];
-            tmem_ld16(tmem + kColQK + lane_off + blk * 16, r);
-            tmem_wait_ld();
-            if (row64 >= 0) {
-                const float gi = g_s[row64];
-                float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = blk * 16 + e;
-                    v[e] = (j <= row64) ? scale * __uint_as_float(r[e]) * __expf(gi - g_s[j]) : 0.f;
-                }
-                st_bf16x8(sm + Lay::kPS + sw128(row64, blk * 32), v);
-                st_bf16x8(sm + Lay::kPS + sw128(row64, blk * 32 + 16), v + 8);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // ---- MMA_W, MMA_U, MMA_QH
-        if (tid == 0) {
-            tc_fence_after_sync();
+    if (warp == 0) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idQK = idesc_bf16(64, 64, false, false);
             constexpr uint32_t idW = idesc_bf16(64, K, false, true);
             constexpr uint32_t id64 = idesc_bf16(64, 64, false, true);
+            constexpr uint32_t idX = idesc_bf16(64, 64, false, true, true);
+            constexpr uint32_t idH = idesc_bf16(K, 64, true, true);
+            const uint32_t s_kh = s_base + Lay::kKH, s_w = s_base + Lay::kW, s_p = s_base + Lay::kP;
+            const uint32_t s_hs = s_base + Lay::kHS, s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
+            auto issue_qk = [&](int s) {
+                const uint32_t kq = s_base + s * Lay::kStage;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kColW, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
-                         smem_desc(s_ws + ks * 2048, 8192, 1024, kLayoutSw128), idW, ks > 0);
+                for (int ks = 0; ks < K / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmem + kColQK, smem_desc(kq + off + 8192, 16, 1024, kLayoutSw128),
+                             smem_desc(kq + off, 16, 1024, kLayoutSw128), idQK, ks > 0);
+                }
+                mma_commit(&bs->qk_done);
+            };
+            auto issue_wu = [&](int s) {
+                const uint32_t ab = s_base + s * Lay::kStage + Lay::kAb;
+                const uint32_t vv = s_base + s * Lay::kStage + Lay::kV;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kColU, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
-                         smem_desc(s_vt + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColW, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(s_kh + ks * 2048, 8192, 1024, kLayoutSw128), idW, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks)
-                mma_bf16(tmem + kColQH,
-                         smem_desc(s_kq + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024,
-                                   kLayoutSw128),
-                         smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), id64, ks > 0);
-            mma_commit(bar_mma);
-        }
-        fail |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(fail)) break;
-        tc_fence_after_sync();
-
-        // ---- epilogue W: w -> bf16 operand (K-major, K/64 blocks of 8 KB)
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColU0 + 64 * s, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(vv + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
+                mma_commit(&bs->w_done);
+            };
+            bool ok = wait_bar(&bs->full[0], 0, abort);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_qk(0);
+                ok = wait_bar(&bs->kh_ready, 0, abort);
+            }
+            if (ok) {
+                tc_fence_after_sync();
+                issue_wu(0);
+            }
+            for (int c = 0; ok && c < NT; ++c) {
+                const int s = c & 1;
+                const uint32_t par = c & 1;
+                const uint32_t kq = s_base + s * Lay::kStage;
+                if (!(ok = wait_bar(&bs->hs_ready, par, abort) && wait_bar(&bs->w_ready, par, abort)))
+                    break;
+                tc_fence_after_sync();
+                // v_new = u - w h (accumulates onto u)
 #pragma unroll
-        for (int blk = 0; blk < K / 16; ++blk) {
-            uint32_t r[16];
-            tmem_ld16(tmem + kColW + lane_off + blk * 16, r);
-            tmem_wait_ld();
-            if (row64 >= 0) {
-                float v[16];
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_bf16(tmem + kColU0 + 64 * s,
+                             smem_desc(s_w + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), idX, 1);
+                mma_commit(&bs->x_done);
+                // next chunk's q k^T
+                if (!(ok = wait_bar(&bs->p_ready, par, abort))) break;
+                if (c + 1 < NT) {
+                    if (!(ok = wait_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort))) break;
+                    tc_fence_after_sync();
+                    issue_qk(s ^ 1);
+                }
+                // q h (its accumulator is free once the previous output is out)
+                if (c >= 1 && !(ok = wait_bar(&bs->o_free, (c - 1) & 1, abort))) break;
+                tc_fence_after_sync();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-                const int f0 = blk * 16;
-                unsigned char *base = sm + Lay::kWS + (f0 >> 6) * 8192;
-                st_bf16x8(base + sw128(row64, (f0 & 63) * 2), v);
-                st_bf16x8(base + sw128(row64, (f0 & 63) * 2 + 16), v + 8);
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_bf16(tmem + kColQH,
+                             smem_desc(kq + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024,
+                                       kLayoutSw128),
+                             smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), id64, ks > 0);
+                // P v_new, k^T v_gated
+                if (!(ok = wait_bar(&bs->vn_ready, par, abort))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColH, smem_desc(kq + ks * 2048, 16384, 1024, kLayoutSw128),
+                             smem_desc(s_vg + ks * 2048, 8192, 1024, kLayoutSw128), idH, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColPV, smem_desc(s_p + s * 8192 + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(s_vn + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
+                mma_commit(&bs->h_done);
+                mma_commit(&bs->empty[s]);
+                if (c + 1 < NT) {
+                    if (!(ok = wait_bar(&bs->kh_ready, (c + 1) & 1, abort))) break;
+                    tc_fence_after_sync();
+                    issue_wu(s ^ 1);
+                }
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // ---- MMA_X: D_U += (-w) h  ->  v_new
-        if (tid == 0) {
-            tc_fence_after_sync();
-            constexpr uint32_t idX = idesc_bf16(64, 64, false, true, true);
+    } else if (warp == 1) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            for (int c = 0; c < NT; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort)) break;
+                unsigned char *st = sm + s * Lay::kStage;
+                const int t0 = c * 64;
+                mbar_arrive_expect_tx(&bs->full[s], Lay::kStage);
 #pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks)
-                mma_bf16(tmem + kColU,
-                         smem_desc(s_ws + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kLayoutSw128),
-                         smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), idX, 1);
-            mma_commit(bar_mma);
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load_4d(st + kb * 16384, &tm_k, &bs->full[s], kb * 64, h, t0, b);
+                    tma_load_4d(st + kb * 16384 + 8192, &tm_q, &bs->full[s], kb * 64, h, t0, b);
+                }
+                tma_load_4d(st + Lay::kV, &tm_v, &bs->full[s], vt * kTcBV, h, t0, b);
+                tma_load_4d(st + Lay::kAb, &tm_a, &bs->full[s], 0, h, t0, b);
+            }
         }
-        fail |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(fail)) break;
-        tc_fence_after_sync();
-
-        // ---- epilogue X: v_new and v_gated -> bf16 operands (token rows, V contiguous)
-        const float g_last = g_s[n - 1];
-        {
-            const float gate = (row64 >= 0 && row64 < n) ? __expf(g_last - g_s[row64]) : 0.f;
+    } else if (warp < 4) {
+        // ================================================================ scale group
+        // g of each chunk (loaded one chunk ahead) and k_hat = exp(g) k.
+        const int stid = tid - 64;
+        auto load_g = [&](int c) {
+            const int t = c * 64 + stid;
+            return (c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
+        };
+        float g_next = load_g(0);
+        for (int c = 0; c < NT; ++c) {
+            const int s = c & 1;
+            const int n = min(64, T - c * 64);
+            const float g_cur = g_next;
+            g_next = load_g(c + 1);
+            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort)) break;
+            g_s[s * 64 + stid] = g_cur;
+            eg_s[s * 64 + stid] = stid < n ? __expf(g_cur) : 0.f;
+            named_sync(3, kScaleThreads);
+            mbar_arrive(&bs->g_ready);
+            // the previous k_hat must have been consumed by its MMA
+            if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
+            const unsigned char *kq = sm + s * Lay::kStage;
+#pragma unroll 4
+            for (int it = 0; it < KB * 8; ++it) {
+                const int idx = stid + it * kScaleThreads;   // 16-byte chunk of k
+                const int kb = idx >> 9, rem = idx & 511, row = rem >> 3, ch = rem & 7;
+                const uint32_t off = sw128(row, ch * 16);
+                const uint4 raw = ld_shared_v4(kq + kb * 16384 + off);
+                const float sc = eg_s[s * 64 + row];
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o4[4];
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16(w4[e]);
+                    o4[e] = pack_bf16(f.x * sc, f.y * sc);
+                }
+                st_shared_v4(sm + Lay::kKH + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bs->kh_ready);
+        }
+    } else if (warp < 12) {
+        // ================================================================ prep group
+        // Two warps per TMEM lane quarter, each owning half of the columns.
+        const int q4 = warp & 3, phalf = (warp - 4) >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
+        for (int c = 0; c < NT; ++c) {
+            const int s = c & 1;
+            const uint32_t par = c & 1;
+            // P = scale (q k^T) exp(g_i - g_j), i >= j. Column blocks right of this
+            // quarter's rows are all zero.
+            if (!wait_bar(&bs->g_ready, par, abort) || !wait_bar(&bs->qk_done, par, abort)) break;
+            tc_fence_after_sync();
+            {
+                const float gi = row64 >= 0 ? g_s[s * 64 + row64] : 0.f;
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int blk = phalf * 2 + bb;
+                    float v[16];
+                    if (blk <= q4) {
+                        uint32_t r[16];
+                        tmem_ld16(tmem + kColQK + lane_off + blk * 16, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = blk * 16 + e;
+                            const float d = (j <= row64) ? gi - g_s[s * 64 + j] : -INFINITY;
+                            v[e] = scale * __uint_as_float(r[e]) * __expf(d);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                    }
+                    if (row64 >= 0) {
+                        st_bf16x8(sm + Lay::kP + s * 8192 + sw128(row64, blk * 32), v);
+                        st_bf16x8(sm + Lay::kP + s * 8192 + sw128(row64, blk * 32 + 16), v + 8);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->p_ready);
+            // w -> bf16 operand
+            if (!wait_bar(&bs->w_done, par, abort)) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int bb = 0; bb < K / 32; ++bb) {
+                const int blk = phalf * (K / 32) + bb;
                 uint32_t r[16];
-                tmem_ld16(tmem + kColU + lane_off + blk * 16, r);
+                tmem_ld16(tmem + kColW + lane_off + blk * 16, r);
+                tmem_wait_ld();
+                if (row64 >= 0) {
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                    const int f0 = blk * 16;
+                    unsigned char *base = sm + Lay::kW + (f0 >> 6) * 8192;
+                    st_bf16x8(base + sw128(row64, (f0 & 63) * 2), v);
+                    st_bf16x8(base + sw128(row64, (f0 & 63) * 2 + 16), v + 8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->w_ready);
+        }
+    } else {
+        // ================================================================ chain group
+        // Two warps per TMEM lane quarter, each owning 32 of the tile's 64 columns.
+        const int ctid = tid - 384, q4 = warp & 3, half = (warp - 12) >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
+        const int col0 = half * 32;
+        // Row of the state this thread owns: the M = 128 accumulator puts row i in
+        // TMEM lane i; the M = 64 one puts row i in lane 32 (i / 16) + i % 16.
+        const int feat = (K == 128) ? q4 * 32 + lane : row64;
+        const int64_t state_off = (static_cast<int64_t>(b) * H + h) * K * V + vt * kTcBV + col0;
+        float hreg[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            hreg[j] = (feat >= 0 && h0) ? h0[state_off + static_cast<int64_t>(feat) * V + j] : 0.f;
+        if (feat >= 0) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                st_bf16x8(sm + Lay::kHS + sw128(feat, col0 * 2 + ch * 16), &hreg[ch * 8]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bs->hs_ready);
+        bool ok = true;
+        for (int c = 0; c < NT; ++c) {
+            const int s = c & 1;
+            const uint32_t par = c & 1;
+            const int t0 = c * 64, n = min(64, T - t0);
+            if (!(ok = wait_bar(&bs->x_done, par, abort))) break;
+            tc_fence_after_sync();
+            const float g_last = g_s[s * 64 + n - 1];
+            const float gate = (row64 >= 0 && row64 < n) ? __expf(g_last - g_s[s * 64 + row64]) : 0.f;
+            const float so = row64 >= 0 ? scale * eg_s[s * 64 + row64] : 0.f;
+            const float decay = __expf(g_last);
+            // v_new and v_gated -> bf16 operands (token rows, V contiguous)
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                uint32_t r[16];
+                tmem_ld16(tmem + kColU0 + 64 * s + col0 + lane_off + blk * 16, r);
                 tmem_wait_ld();
                 if (row64 >= 0) {
                     float v[16], vg[16];
@@ -277,44 +406,23 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         v[e] = __uint_as_float(r[e]);
                         vg[e] = v[e] * gate;
                     }
-                    st_bf16x8(sm + Lay::kAP + sw128(row64, blk * 32), v);
-                    st_bf16x8(sm + Lay::kAP + sw128(row64, blk * 32 + 16), v + 8);
-                    st_bf16x8(sm + Lay::kAU + sw128(row64, blk * 32), vg);
-                    st_bf16x8(sm + Lay::kAU + sw128(row64, blk * 32 + 16), vg + 8);
+                    const uint32_t byte = (col0 + blk * 16) * 2;
+                    st_bf16x8(sm + Lay::kVN + sw128(row64, byte), v);
+                    st_bf16x8(sm + Lay::kVN + sw128(row64, byte + 16), v + 8);
+                    st_bf16x8(sm + Lay::kVG + sw128(row64, byte), vg);
+                    st_bf16x8(sm + Lay::kVG + sw128(row64, byte + 16), vg + 8);
                 }
             }
             fence_proxy_async_smem();
-        }
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // ---- MMA_PV: P v_new ; MMA_H: k^T v_gated
-        if (tid == 0) {
+            tc_fence_before_sync();
+            mbar_arrive(&bs->vn_ready);
+            if (!(ok = wait_bar(&bs->h_done, par, abort))) break;
             tc_fence_after_sync();
-            constexpr uint32_t id64 = idesc_bf16(64, 64, false, true);
-            constexpr uint32_t idH = idesc_bf16(K, 64, true, true);
+            // h = h exp(g_last) + k^T v_gated; bf16 copy for the next chunk
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kColPV, smem_desc(s_ps + ks * 32, 16, 1024, kLayoutSw128),
-                         smem_desc(s_ap + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kColH, smem_desc(s_kq + ks * 2048, 16384, 1024, kLayoutSw128),
-                         smem_desc(s_au + ks * 2048, 8192, 1024, kLayoutSw128), idH, ks > 0);
-            mma_commit(bar_mma);
-        }
-        fail |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(fail)) break;
-        tc_fence_after_sync();
-
-        // ---- epilogue H: h = h exp(g_last) + k^T v_gated; bf16 copy for the next chunk
-        {
-            const float decay = __expf(g_last);
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
+            for (int blk = 0; blk < 2; ++blk) {
                 uint32_t r[16];
-                tmem_ld16(tmem + kColH + lane_off + blk * 16, r);
+                tmem_ld16(tmem + kColH + col0 + lane_off + blk * 16, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -322,48 +430,49 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             if (feat >= 0) {
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    st_bf16x8(sm + Lay::kHS + sw128(feat, ch * 16), &hreg[ch * 8]);
+                for (int ch = 0; ch < 4; ++ch)
+                    st_bf16x8(sm + Lay::kHS + sw128(feat, col0 * 2 + ch * 16), &hreg[ch * 8]);
             }
-        }
-        // ---- epilogue O: o = scale exp(g_t) q h + P v_new -> bf16 staging -> TMA store
-        {
-            const float so = (row64 >= 0) ? scale * eg_s[row64] : 0.f;
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->hs_ready);
+            // o = scale exp(g_t) q h + P v_new -> bf16 staging -> TMA store
+            if (ctid == 0) bulk_wait_group_read0();
+            named_sync(2, kChainThreads);
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
+            for (int blk = 0; blk < 2; ++blk) {
                 uint32_t rq[16], rp[16];
-                tmem_ld16(tmem + kColQH + lane_off + blk * 16, rq);
-                tmem_ld16(tmem + kColPV + lane_off + blk * 16, rp);
+                tmem_ld16(tmem + kColQH + col0 + lane_off + blk * 16, rq);
+                tmem_ld16(tmem + kColPV + col0 + lane_off + blk * 16, rp);
                 tmem_wait_ld();
                 if (row64 >= 0) {
                     float v[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        v[e] = fmaf(so, __uint_as_float(rq[e]), __uint_as_float(rp[e]));
-                    st_bf16x8(sm + Lay::kVT + sw128(row64, blk * 32), v);
-                    st_bf16x8(sm + Lay::kVT + sw128(row64, blk * 32 + 16), v + 8);
+                    for (int e = 0; e < 16; ++e) v[e] = fmaf(so, __uint_as_float(rq[e]), __uint_as_float(rp[e]));
+                    const uint32_t byte = (col0 + blk * 16) * 2;
+                    st_bf16x8(sm + Lay::kOS + sw128(row64, byte), v);
+                    st_bf16x8(sm + Lay::kOS + sw128(row64, byte + 16), v + 8);
                 }
             }
             fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->o_free);
+            named_sync(2, kChainThreads);
+            if (ctid == 0) {
+                tma_store_4d(&tm_o, sm + Lay::kOS, vt * kTcBV, h, t0, b);
+                bulk_commit_group();
+            }
         }
-        tc_fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tma_store_4d(&tm_o, sm + Lay::kVT, vt * kTcBV, h, t0, b);
-            bulk_commit_group();
+        if (ok && feat >= 0 && h_final) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h_final[state_off + static_cast<int64_t>(feat) * V + j] = hreg[j];
         }
+        if (ctid == 0) bulk_wait_group0();
     }
 
-    if (!fail && feat >= 0 && h_final) {
-#pragma unroll
-        for (int j = 0; j < kTcBV; ++j) h_final[state_off + static_cast<int64_t>(feat) * V + j] = hreg[j];
-    }
-    if (tid == 0) {
-        bulk_wait_group0();
-        if (fail) atomicOr(status, 1u);
-    }
     tc_fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *abort) atomicOr(status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 

@@ -4,18 +4,21 @@
 // A diag(beta) in bf16 [B, T, H, 64].
 //
 // One CTA per (chunk, h, b); the chunks are independent, so the grid is as
-// wide as the problem and several CTAs share an SM. Per chunk:
-//   TMA     k [64 x K]
-//   MMA     G = k k^T (M = 64)
-//   epi     L rows (fp32): the four 16x16 diagonal blocks to shared memory; the
-//           off-diagonal blocks as two bf16 operands N1 (blocks (1,0), (3,2))
-//           and N2 (rows 32-63, columns 0-31)
-//   SIMT    X = blockdiag of the inverted 16x16 diagonal blocks (forward
-//           substitution in fp32)
-//   MMA x4  level 1: Y1 = N1 X, Z1 = X Y1, A0 = X - Z1   (32x32 diagonal blocks)
-//           level 2: Y2 = N2 A0, Z2 = A0 Y2, A = A0 - Z2
-//           which is (I + L)^-1 because each off-diagonal part is nilpotent of
-//           order two against its block-diagonal: (D + N)^-1 = D^-1 - D^-1 N D^-1.
+// wide as the problem and several CTAs share an SM. With X the inverse of the
+// block diagonal of I + L (four 16x16 blocks), N1 its off-diagonal blocks
+// (1,0) and (3,2), N2 its bottom-left 32x32 block:
+//   A0 = (I + L_32x32 blocks)^-1 = X - X N1 X            (level 1)
+//   A  = A0 - A0 N2 A0                                    (level 2)
+// because each off-diagonal part squares to zero against its block diagonal:
+// (D + N)^-1 = D^-1 - D^-1 N D^-1. Expanding level 2 with Y1 = N1 X and
+// U = N2 X gives N2 A0 = U - U Y1, so after the Gram matrix only three tensor-
+// core round trips remain, each a stacked M = 128 product:
+//   MMA 1   G = k k^T                                     (M = 64)
+//   epi     L (fp32 16x16 diagonal blocks, bf16 N1 | N2 stacked)
+//   SIMT    X: forward substitution on the diagonal blocks (fp32)
+//   MMA 2   [Y1; U] = [N1; N2] X
+//   MMA 3   [X Y1; U Y1] = [X; U] Y1  ->  A0 = X - X Y1, Y2 = U - U Y1
+//   MMA 4   Z = A0 Y2                  ->  A  = A0 - Z
 //   epi     A diag(beta) -> bf16 -> TMA store
 // The correction products run with bf16 operands and fp32 accumulation; the
 // block-diagonal part and the subtractions stay fp32.
@@ -33,26 +36,28 @@ constexpr uint64_t kWyWaitNs = 1000000000ull;
 template <int K>
 struct WyLayout {
     static constexpr int KB = K / 64;
-    static constexpr uint32_t kK = 0;                                  // k tile -> N1 | N2 -> out
+    // k tile (K-major, KB blocks of 8 KB); after the Gram MMA the first 16 KB
+    // hold the stacked operand [N1; N2]
+    static constexpr uint32_t kK = 0;
     static constexpr uint32_t kKBytes = (KB * 8192 > 16384) ? KB * 8192 : 16384;
-    static constexpr uint32_t kN1 = 0, kN2 = 8192, kOut = 0;
-    static constexpr uint32_t kX = kKBytes;                            // X -> A0 (bf16)
-    static constexpr uint32_t kY = kX + 8192;                          // Y1 -> Y2 (bf16)
-    static constexpr uint32_t kLd = kY + 8192;                         // diag blocks fp32 [4][16][17]
-    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;           // g, beta, bars
+    static constexpr uint32_t kN = 0;
+    static constexpr uint32_t kXU = kKBytes;               // [X; U] stacked, then A0 (bf16)
+    static constexpr uint32_t kY = kXU + 16384;            // Y1, then Y2 (bf16, rows along N)
+    static constexpr uint32_t kOut = kY + 8192;            // A diag(beta) staging
+    static constexpr uint32_t kLd = kOut + 8192;           // diagonal blocks fp32 [4][16][17]
+    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;
     static constexpr uint32_t kBytes = kMisc + 768;
 };
 
 template <int K>
-__global__ void __launch_bounds__(kWyThreads, 3)
+__global__ void __launch_bounds__(kWyThreads, 4)
 gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_a,
                  const float *__restrict__ g, const float *__restrict__ beta, int T, int H,
                  uint32_t *status) {
     using Lay = WyLayout<K>;
     constexpr int KB = K / 64;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *Ld = reinterpret_cast<float *>(sm + Lay::kLd);
     float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);
     float *b_s = g_s + 64;
@@ -63,9 +68,6 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = c * 64, n = min(64, T - t0);
-    // Row of the M = 64 accumulator this thread reads (TMEM lane 32 (r/16) + r%16).
-    const int r = lane < 16 ? warp * 16 + lane : -1;
-    const int rb = r >> 4;   // 16-row block of r
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
 
     if (warp == 0) {
@@ -95,77 +97,73 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t s_k = smem_u32(sm + Lay::kK), s_x = smem_u32(sm + Lay::kX),
-                   s_y = smem_u32(sm + Lay::kY);
+    const uint32_t s_k = smem_u32(sm + Lay::kK), s_n = smem_u32(sm + Lay::kN);
+    const uint32_t s_xu = smem_u32(sm + Lay::kXU), s_y = smem_u32(sm + Lay::kY);
     uint32_t phase = 0;
     bool fail = !mbar_wait(bar_tma, 0, kWyWaitNs);
 
-    // D = A_op * B_op with M = N = 64, both operands 64x64 bf16 tiles (A K-major,
-    // B stored row-by-row along N), issued by one thread; everyone waits.
-    auto mma64 = [&](uint32_t a, uint32_t bop, bool b_mn, int ksteps, uint32_t b_kstep) {
+    // One MMA group issued by thread 0 (A K-major, B K-major or rows-along-N),
+    // then everyone waits for it.
+    auto mma = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
         if (tid == 0) {
             tc_fence_after_sync();
-            const uint32_t id = idesc_bf16(64, 64, false, b_mn);
+            const uint32_t id = idesc_bf16(M, 64, false, b_mn);
             for (int ks = 0; ks < ksteps; ++ks) {
                 const uint32_t a_off = (ks >> 2) * 8192 + (ks & 3) * 32;
                 mma_bf16(tmem, smem_desc(a + a_off, 16, 1024, kLayoutSw128),
                          smem_desc(bop + (b_mn ? ks * 2048 : a_off), 8192, 1024, kLayoutSw128), id,
                          ks > 0);
             }
-            (void)b_kstep;
             mma_commit(bar_mma);
         }
         fail |= !mbar_wait(bar_mma, phase, kWyWaitNs);
         phase ^= 1;
         tc_fence_after_sync();
     };
-    // Loads this thread's accumulator row (64 fp32; meaningful when r >= 0).
-    auto load_row = [&](float *v) {
+    // This thread's accumulator row, 16 columns at a time.
+    auto load16 = [&](int blk, float *v) {
+        uint32_t t[16];
+        tmem_ld16(tmem + lane_off + blk * 16, t);
+        tmem_wait_ld();
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            uint32_t t[16];
-            tmem_ld16(tmem + lane_off + blk * 16, t);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[blk * 16 + e] = __uint_as_float(t[e]);
-        }
-    };
-    auto store_row_bf16 = [&](uint32_t region, const float *v) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_bf16x8(sm + region + sw128(r, ch * 16), v + ch * 8);
+        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(t[e]);
     };
 
-    // ---- G = k k^T
+    // ---- G = k k^T (M = 64: row r in TMEM lane 32 (r / 16) + r % 16)
     if (__syncthreads_or(fail)) goto done;
-    mma64(s_k, s_k, false, K / 16, 0);
+    mma(64, s_k, s_k, false, K / 16);
     if (__syncthreads_or(fail)) goto done;
     {
-        float v[64];
-        load_row(v);
-        __syncthreads();   // every k-tile read done before N1 | N2 overwrite it
-        if (r >= 0) {
-            const float gr = g_s[r], br = b_s[r];
+        const int r = lane < 16 ? warp * 16 + lane : -1, rb = r >> 4;
+        const float gr = r >= 0 ? g_s[r] : 0.f, br = r >= 0 ? b_s[r] : 0.f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = (j < r) ? br * v[j] * __expf(gr - g_s[j]) : 0.f;
+        for (int blk = 0; blk < 4; ++blk) {
+            float v[16];
+            load16(blk, v);
+            if (r >= 0) {
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk)
+                for (int e = 0; e < 16; ++e) {
+                    const int j = blk * 16 + e;
+                    const float d = (j < r) ? gr - g_s[j] : -INFINITY;
+                    v[e] = br * v[e] * __expf(d);
+                }
                 if (blk == rb) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) Ld[(rb * 16 + (r & 15)) * 17 + e] = v[blk * 16 + e];
+                    for (int e = 0; e < 16; ++e) Ld[(rb * 16 + (r & 15)) * 17 + e] = v[e];
                 }
+                // N1: blocks (1,0) and (3,2); N2: rows 32-63 x columns 0-31
+                const bool in1 = (rb == 1 && blk == 0) || (rb == 3 && blk == 2);
+                const bool in2 = rb >= 2 && blk < 2;
+                float n1[16], n2[16];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int jb = ch >> 1;   // 16-column block of this 8-column chunk
-                const bool in1 = (rb == 1 && jb == 0) || (rb == 3 && jb == 2);
-                const bool in2 = rb >= 2 && jb < 2;
-                float n1[8], n2[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    n1[e] = in1 ? v[ch * 8 + e] : 0.f;
-                    n2[e] = in2 ? v[ch * 8 + e] : 0.f;
+                for (int e = 0; e < 16; ++e) {
+                    n1[e] = in1 ? v[e] : 0.f;
+                    n2[e] = in2 ? v[e] : 0.f;
                 }
-                st_bf16x8(sm + Lay::kN1 + sw128(r, ch * 16), n1);
-                st_bf16x8(sm + Lay::kN2 + sw128(r, ch * 16), n2);
+                st_bf16x8(sm + Lay::kN + sw128(r, blk * 32), n1);
+                st_bf16x8(sm + Lay::kN + sw128(r, blk * 32 + 16), n1 + 8);
+                st_bf16x8(sm + Lay::kN + 8192 + sw128(r, blk * 32), n2);
+                st_bf16x8(sm + Lay::kN + 8192 + sw128(r, blk * 32 + 16), n2 + 8);
             }
         }
         fence_proxy_async_smem();
@@ -191,59 +189,77 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         __syncthreads();
     }
-    float a0[64];   // this thread's row of X, then of A0 (fp32)
-    if (r >= 0) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) a0[j] = ((j >> 4) == rb) ? Ld[(rb * 16 + (r & 15)) * 17 + (j & 15)] : 0.f;
-        store_row_bf16(Lay::kX, a0);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    // ---- level 1: A0 = X - X (N1 X)
-    mma64(smem_u32(sm + Lay::kN1), s_x, true, 4, 0);
-    if (__syncthreads_or(fail)) goto done;
+    // From here on thread t owns row t of the M = 128 accumulators: rows 0-63
+    // belong to X / A0, rows 64-127 to U / Y2.
     {
-        float v[64];
-        load_row(v);
-        if (r >= 0) store_row_bf16(Lay::kY, v);
-        fence_proxy_async_smem();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    mma64(s_x, s_y, true, 4, 0);
-    if (__syncthreads_or(fail)) goto done;
-    {
-        float v[64];
-        load_row(v);
-        if (r >= 0) {
+        const int r = tid & 63, rb = r >> 4;
+        // keep: row r of X, then of A0 (threads < 64); row r of U (threads >= 64)
+        float keep[64];
+        if (tid < 64) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) a0[j] -= v[j];
-            store_row_bf16(Lay::kX, a0);
+            for (int j = 0; j < 64; ++j) keep[j] = ((j >> 4) == rb) ? Ld[(rb * 16 + (r & 15)) * 17 + (j & 15)] : 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) st_bf16x8(sm + Lay::kXU + sw128(r, ch * 16), keep + ch * 8);
         }
         fence_proxy_async_smem();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    // ---- level 2: A = A0 - A0 (N2 A0)
-    mma64(smem_u32(sm + Lay::kN2), s_x, true, 4, 0);
-    if (__syncthreads_or(fail)) goto done;
-    {
-        float v[64];
-        load_row(v);
-        if (r >= 0) store_row_bf16(Lay::kY, v);
-        fence_proxy_async_smem();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    mma64(s_x, s_y, true, 4, 0);
-    if (__syncthreads_or(fail)) goto done;
-    {
-        float v[64];
-        load_row(v);
-        if (r >= 0) {
+        __syncthreads();
+        // ---- [Y1; U] = [N1; N2] X
+        mma(128, s_n, s_xu, true, 4);
+        if (__syncthreads_or(fail)) goto done;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = (a0[j] - v[j]) * b_s[j];
-            store_row_bf16(Lay::kOut, v);
+        for (int blk = 0; blk < 4; ++blk) {
+            float v[16];
+            load16(blk, v);
+            // Y1 rows -> B operand (rows along N); U rows -> second half of [X; U]
+            unsigned char *dst = (tid < 64) ? sm + Lay::kY : sm + Lay::kXU + 8192;
+            st_bf16x8(dst + sw128(r, blk * 32), v);
+            st_bf16x8(dst + sw128(r, blk * 32 + 16), v + 8);
+            if (tid >= 64) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) keep[blk * 16 + e] = v[e];
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // ---- [X Y1; U Y1] = [X; U] Y1
+        mma(128, s_xu, s_y, true, 4);
+        if (__syncthreads_or(fail)) goto done;
+        tc_fence_before_sync();
+        __syncthreads();   // every MMA operand read before A0 / Y2 overwrite them
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+            float v[16];
+            load16(blk, v);
+            if (tid < 64) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) keep[blk * 16 + e] -= v[e];   // A0 = X - X Y1
+                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32), keep + blk * 16);
+                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32 + 16), keep + blk * 16 + 8);
+            } else {
+                float y2[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) y2[e] = keep[blk * 16 + e] - v[e];   // Y2 = U - U Y1
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32), y2);
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32 + 16), y2 + 8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // ---- Z = A0 Y2 (rows 64-127 of the operand are unused)
+        mma(128, s_xu, s_y, true, 4);
+        if (__syncthreads_or(fail)) goto done;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+            float v[16];
+            load16(blk, v);
+            if (tid < 64) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = (keep[blk * 16 + e] - v[e]) * b_s[blk * 16 + e];
+                st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32), v);
+                st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32 + 16), v + 8);
+            }
         }
         fence_proxy_async_smem();
     }
