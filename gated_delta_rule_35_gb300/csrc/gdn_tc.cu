@@ -43,14 +43,17 @@ constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate 
 template <int K>
 struct TcLayout {
     static constexpr int KB = K / 64;                            // 64-feature blocks
-    // two input stages: per 64-feature block k rows | q rows, then v tile, then A diag(beta)
-    static constexpr uint32_t kStage = KB * 16384 + 16384;
-    static constexpr uint32_t kV = KB * 16384, kAb = kV + 8192;  // offsets inside a stage
-    static constexpr uint32_t kKH = 2 * kStage;                   // exp(g) k, KB x 8 KB
-    static constexpr uint32_t kW = kKH + KB * 8192;               // w, KB x 8 KB
-    static constexpr uint32_t kP = kW + KB * 8192;                // P, two buffers of 8 KB
-    static constexpr uint32_t kHS = kP + 16384;                   // h bf16 [K rows x 64]
-    static constexpr uint32_t kVN = kHS + K * 128;                // v_new
+    // Two input stages. Per 64-feature block: k rows | h^T rows | q rows (8 KB
+    // each, K-major, 128-byte swizzle), then A diag(beta). k and h^T are
+    // adjacent so that together they form one 128-row operand.
+    static constexpr uint32_t kKb = 24576;                        // per-block stride
+    static constexpr uint32_t kHT = 8192, kQ = 16384;             // offsets in a block
+    static constexpr uint32_t kAb = KB * kKb;                     // offset in a stage
+    static constexpr uint32_t kStage = kAb + 8192;
+    static constexpr uint32_t kKHV = 2 * kStage;                  // exp(g) k (KB x 8 KB) | v tile
+    static constexpr uint32_t kW = kKHV + (KB + 1) * 8192;        // -w operand, KB x 8 KB
+    static constexpr uint32_t kP = kW + KB * 8192;                // P
+    static constexpr uint32_t kVN = kP + 8192;                    // v_new
     static constexpr uint32_t kVG = kVN + 8192;                   // v_new exp(g_last - g)
     static constexpr uint32_t kOS = kVG + 8192;                   // o staging for the TMA store
     static constexpr uint32_t kG = kOS + 8192;                    // g[2][64], exp(g)[2][64]
@@ -58,15 +61,16 @@ struct TcLayout {
     static constexpr uint32_t kBytes = kBar + 256;
 };
 
-// TMEM columns of the 512-column allocation.
-constexpr uint32_t kColQK = 0, kColW = 64, kColU0 = 192, kColQH = 320, kColPV = 384, kColH = 448;
+// TMEM columns of the 512-column allocation: [w | u] (K + 64), [q k^T | q h]
+// (128), (dh)^T (K), P v_new (64).
+constexpr uint32_t kColWU = 0, kColQKH = 192, kColHT = 320, kColPV = 448;
 
 struct Bars {
-    uint64_t full[2], empty[2];      // TMA stage filled / released
-    uint64_t qk_done, w_done, x_done, h_done;   // MMA completions (tcgen05.commit)
-    uint64_t g_ready, kh_ready;                 // scale group: g in place, exp(g) k written
-    uint64_t p_ready, w_ready;                  // prep group: operands written
-    uint64_t hs_ready, vn_ready, o_free;        // chain group (128 arrivals)
+    uint64_t full[2], empty[2], v_full;             // TMA: stage / v tile filled, stage released
+    uint64_t w_done, x_done, qkh_done, h_done, o_done;   // MMA completions (tcgen05.commit)
+    uint64_t g_ready;                               // scale group: g of the chunk in place
+    uint64_t kh_ready, p_ready, w_ready;            // prep group: operands written
+    uint64_t hs_ready, vn_ready, o_free;            // chain group
     uint32_t abort, tmem;
 };
 
@@ -82,6 +86,23 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
         }
     }
     return true;
+}
+// Polling variant for the latency-critical roles (MMA issuer, chain group): a
+// suspended waiter can take hundreds of cycles to resume after the phase
+// completes.
+__device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 255) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
 }
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -118,12 +139,14 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_init(&bs->full[1], 1);
         mbar_init(&bs->empty[0], 1);
         mbar_init(&bs->empty[1], 1);
-        mbar_init(&bs->qk_done, 1);
+        mbar_init(&bs->v_full, 1);
         mbar_init(&bs->w_done, 1);
         mbar_init(&bs->x_done, 1);
+        mbar_init(&bs->qkh_done, 1);
         mbar_init(&bs->h_done, 1);
+        mbar_init(&bs->o_done, 1);
         mbar_init(&bs->g_ready, kScaleThreads);
-        mbar_init(&bs->kh_ready, kScaleThreads);
+        mbar_init(&bs->kh_ready, kPrepThreads);
         mbar_init(&bs->p_ready, kPrepThreads);
         mbar_init(&bs->w_ready, kPrepThreads);
         mbar_init(&bs->hs_ready, kChainThreads);
@@ -146,42 +169,24 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idQK = idesc_bf16(64, 64, false, false);
-            constexpr uint32_t idW = idesc_bf16(64, K, false, true);
-            constexpr uint32_t id64 = idesc_bf16(64, 64, false, true);
-            constexpr uint32_t idX = idesc_bf16(64, 64, false, true, true);
-            constexpr uint32_t idH = idesc_bf16(K, 64, true, true);
-            const uint32_t s_kh = s_base + Lay::kKH, s_w = s_base + Lay::kW, s_p = s_base + Lay::kP;
-            const uint32_t s_hs = s_base + Lay::kHS, s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
-            auto issue_qk = [&](int s) {
-                const uint32_t kq = s_base + s * Lay::kStage;
-#pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem + kColQK, smem_desc(kq + off + 8192, 16, 1024, kLayoutSw128),
-                             smem_desc(kq + off, 16, 1024, kLayoutSw128), idQK, ks > 0);
-                }
-                mma_commit(&bs->qk_done);
-            };
+            constexpr uint32_t idWU = idesc_bf16(64, K + 64, false, true);
+            constexpr uint32_t idX = idesc_bf16(64, 64, false, false, true);
+            constexpr uint32_t idQKH = idesc_bf16(64, 128, false, false);
+            constexpr uint32_t idHT = idesc_bf16(64, K, true, true);
+            constexpr uint32_t idPV = idesc_bf16(64, 64, false, true);
+            const uint32_t s_khv = s_base + Lay::kKHV, s_w = s_base + Lay::kW, s_p = s_base + Lay::kP;
+            const uint32_t s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
+            // [w | u] = A diag(beta) [exp(g) k | v]
             auto issue_wu = [&](int s) {
                 const uint32_t ab = s_base + s * Lay::kStage + Lay::kAb;
-                const uint32_t vv = s_base + s * Lay::kStage + Lay::kV;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColW, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(s_kh + ks * 2048, 8192, 1024, kLayoutSw128), idW, ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColU0 + 64 * s, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(vv + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
+                    mma_bf16(tmem + kColWU, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(s_khv + ks * 2048, 8192, 1024, kLayoutSw128), idWU, ks > 0);
                 mma_commit(&bs->w_done);
             };
-            bool ok = wait_bar(&bs->full[0], 0, abort);
-            if (ok) {
-                tc_fence_after_sync();
-                issue_qk(0);
-                ok = wait_bar(&bs->kh_ready, 0, abort);
-            }
+            bool ok = spin_bar(&bs->full[0], 0, abort) && spin_bar(&bs->v_full, 0, abort) &&
+                      spin_bar(&bs->kh_ready, 0, abort);
             if (ok) {
                 tc_fence_after_sync();
                 issue_wu(0);
@@ -189,51 +194,55 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int c = 0; ok && c < NT; ++c) {
                 const int s = c & 1;
                 const uint32_t par = c & 1;
-                const uint32_t kq = s_base + s * Lay::kStage;
-                if (!(ok = wait_bar(&bs->hs_ready, par, abort) && wait_bar(&bs->w_ready, par, abort)))
+                const uint32_t st = s_base + s * Lay::kStage;
+                // v_new = u - w h (accumulates onto u)
+                if (!(ok = spin_bar(&bs->hs_ready, par, abort) && spin_bar(&bs->w_ready, par, abort)))
                     break;
                 tc_fence_after_sync();
-                // v_new = u - w h (accumulates onto u)
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
-                    mma_bf16(tmem + kColU0 + 64 * s,
+                    mma_bf16(tmem + kColWU + K,
                              smem_desc(s_w + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), idX, 1);
-                mma_commit(&bs->x_done);
-                // next chunk's q k^T
-                if (!(ok = wait_bar(&bs->p_ready, par, abort))) break;
-                if (c + 1 < NT) {
-                    if (!(ok = wait_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort))) break;
-                    tc_fence_after_sync();
-                    issue_qk(s ^ 1);
-                }
-                // q h (its accumulator is free once the previous output is out)
-                if (c >= 1 && !(ok = wait_bar(&bs->o_free, (c - 1) & 1, abort))) break;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks)
-                    mma_bf16(tmem + kColQH,
-                             smem_desc(kq + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024,
+                             smem_desc(st + (ks >> 2) * Lay::kKb + Lay::kHT + (ks & 3) * 32, 16, 1024,
                                        kLayoutSw128),
-                             smem_desc(s_hs + ks * 2048, K * 128, 1024, kLayoutSw128), id64, ks > 0);
-                // P v_new, k^T v_gated
-                if (!(ok = wait_bar(&bs->vn_ready, par, abort))) break;
+                             idX, 1);
+                mma_commit(&bs->x_done);
+                // [q k^T | q h]: k and h^T rows stacked as one operand
+                if (c >= 1 && !(ok = spin_bar(&bs->o_free, (c - 1) & 1, abort))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * Lay::kKb + (ks & 3) * 32;
+                    mma_bf16(tmem + kColQKH, smem_desc(st + off + Lay::kQ, 16, 1024, kLayoutSw128),
+                             smem_desc(st + off, 16, 1024, kLayoutSw128), idQKH, ks > 0);
+                }
+                mma_commit(&bs->qkh_done);
+                // (dh)^T = (v_new exp(g_last - g))^T k; the stage's last reader
+                if (!(ok = spin_bar(&bs->vn_ready, par, abort))) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColH, smem_desc(kq + ks * 2048, 16384, 1024, kLayoutSw128),
-                             smem_desc(s_vg + ks * 2048, 8192, 1024, kLayoutSw128), idH, ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColPV, smem_desc(s_p + s * 8192 + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(s_vn + ks * 2048, 8192, 1024, kLayoutSw128), id64, ks > 0);
+                    mma_bf16(tmem + kColHT, smem_desc(s_vg + ks * 2048, 8192, 1024, kLayoutSw128),
+                             smem_desc(st + ks * 2048, Lay::kKb, 1024, kLayoutSw128), idHT, ks > 0);
                 mma_commit(&bs->h_done);
                 mma_commit(&bs->empty[s]);
+                // next chunk's [w | u]
                 if (c + 1 < NT) {
-                    if (!(ok = wait_bar(&bs->kh_ready, (c + 1) & 1, abort))) break;
+                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort) &&
+                               spin_bar(&bs->v_full, (c + 1) & 1, abort) &&
+                               spin_bar(&bs->kh_ready, (c + 1) & 1, abort)))
+                        break;
                     tc_fence_after_sync();
                     issue_wu(s ^ 1);
                 }
+                // P v_new
+                if (!(ok = spin_bar(&bs->p_ready, par, abort))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColPV, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(s_vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, ks > 0);
+                mma_commit(&bs->o_done);
             }
         }
     } else if (warp == 1) {
@@ -244,19 +253,22 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort)) break;
                 unsigned char *st = sm + s * Lay::kStage;
                 const int t0 = c * 64;
-                mbar_arrive_expect_tx(&bs->full[s], Lay::kStage);
+                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 8192);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
-                    tma_load_4d(st + kb * 16384, &tm_k, &bs->full[s], kb * 64, h, t0, b);
-                    tma_load_4d(st + kb * 16384 + 8192, &tm_q, &bs->full[s], kb * 64, h, t0, b);
+                    tma_load_4d(st + kb * Lay::kKb, &tm_k, &bs->full[s], kb * 64, h, t0, b);
+                    tma_load_4d(st + kb * Lay::kKb + Lay::kQ, &tm_q, &bs->full[s], kb * 64, h, t0, b);
                 }
-                tma_load_4d(st + Lay::kV, &tm_v, &bs->full[s], vt * kTcBV, h, t0, b);
                 tma_load_4d(st + Lay::kAb, &tm_a, &bs->full[s], 0, h, t0, b);
+                // the single v slot is free once the previous [w | u] product is done
+                if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
+                mbar_arrive_expect_tx(&bs->v_full, 8192);
+                tma_load_4d(sm + Lay::kKHV + KB * 8192, &tm_v, &bs->v_full, vt * kTcBV, h, t0, b);
             }
         }
     } else if (warp < 4) {
         // ================================================================ scale group
-        // g of each chunk (loaded one chunk ahead) and k_hat = exp(g) k.
+        // g of each chunk, loaded one chunk ahead.
         const int stid = tid - 64;
         auto load_g = [&](int c) {
             const int t = c * 64 + stid;
@@ -273,15 +285,25 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             eg_s[s * 64 + stid] = stid < n ? __expf(g_cur) : 0.f;
             named_sync(3, kScaleThreads);
             mbar_arrive(&bs->g_ready);
-            // the previous k_hat must have been consumed by its MMA
-            if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
-            const unsigned char *kq = sm + s * Lay::kStage;
-#pragma unroll 4
-            for (int it = 0; it < KB * 8; ++it) {
-                const int idx = stid + it * kScaleThreads;   // 16-byte chunk of k
+        }
+    } else if (warp < 12) {
+        // ================================================================ prep group
+        // Two warps per TMEM lane quarter, each owning half of the columns.
+        const int ptid = tid - 128, q4 = warp & 3, phalf = (warp - 4) >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
+        // k_hat = exp(g) k for chunk c (same swizzled positions as k)
+        auto make_khat = [&](int c) -> bool {
+            const int s = c & 1;
+            if (!wait_bar(&bs->g_ready, c & 1, abort) || !wait_bar(&bs->full[s], (c >> 1) & 1, abort))
+                return false;
+            const unsigned char *st = sm + s * Lay::kStage;
+#pragma unroll
+            for (int it = 0; it < KB * 2; ++it) {
+                const int idx = ptid + it * kPrepThreads;   // 16-byte chunk of k
                 const int kb = idx >> 9, rem = idx & 511, row = rem >> 3, ch = rem & 7;
                 const uint32_t off = sw128(row, ch * 16);
-                const uint4 raw = ld_shared_v4(kq + kb * 16384 + off);
+                const uint4 raw = ld_shared_v4(st + kb * Lay::kKb + off);
                 const float sc = eg_s[s * 64 + row];
                 const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
                 uint32_t o4[4];
@@ -290,61 +312,21 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const float2 f = unpack_bf16(w4[e]);
                     o4[e] = pack_bf16(f.x * sc, f.y * sc);
                 }
-                st_shared_v4(sm + Lay::kKH + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
+                st_shared_v4(sm + Lay::kKHV + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(&bs->kh_ready);
-        }
-    } else if (warp < 12) {
-        // ================================================================ prep group
-        // Two warps per TMEM lane quarter, each owning half of the columns.
-        const int q4 = warp & 3, phalf = (warp - 4) >> 2;
-        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
-        for (int c = 0; c < NT; ++c) {
-            const int s = c & 1;
-            const uint32_t par = c & 1;
-            // P = scale (q k^T) exp(g_i - g_j), i >= j. Column blocks right of this
-            // quarter's rows are all zero.
-            if (!wait_bar(&bs->g_ready, par, abort) || !wait_bar(&bs->qk_done, par, abort)) break;
-            tc_fence_after_sync();
-            {
-                const float gi = row64 >= 0 ? g_s[s * 64 + row64] : 0.f;
-#pragma unroll
-                for (int bb = 0; bb < 2; ++bb) {
-                    const int blk = phalf * 2 + bb;
-                    float v[16];
-                    if (blk <= q4) {
-                        uint32_t r[16];
-                        tmem_ld16(tmem + kColQK + lane_off + blk * 16, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int j = blk * 16 + e;
-                            const float d = (j <= row64) ? gi - g_s[s * 64 + j] : -INFINITY;
-                            v[e] = scale * __uint_as_float(r[e]) * __expf(d);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                    }
-                    if (row64 >= 0) {
-                        st_bf16x8(sm + Lay::kP + s * 8192 + sw128(row64, blk * 32), v);
-                        st_bf16x8(sm + Lay::kP + s * 8192 + sw128(row64, blk * 32 + 16), v + 8);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            mbar_arrive(&bs->p_ready);
-            // w -> bf16 operand
-            if (!wait_bar(&bs->w_done, par, abort)) break;
+            return true;
+        };
+        // w (rows 0-63 of [w | u]) -> bf16 operand, negated by the MMA
+        auto epi_w = [&](int c) -> bool {
+            if (!wait_bar(&bs->w_done, c & 1, abort)) return false;
             tc_fence_after_sync();
 #pragma unroll
             for (int bb = 0; bb < K / 32; ++bb) {
                 const int blk = phalf * (K / 32) + bb;
                 uint32_t r[16];
-                tmem_ld16(tmem + kColW + lane_off + blk * 16, r);
+                tmem_ld16(tmem + kColWU + lane_off + blk * 16, r);
                 tmem_wait_ld();
                 if (row64 >= 0) {
                     float v[16];
@@ -359,26 +341,71 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->w_ready);
+            return true;
+        };
+        if (make_khat(0) && epi_w(0)) {
+            for (int c = 0; c < NT; ++c) {
+                const int s = c & 1;
+                // the exp(g) k slot is free: its product for chunk c finished (w_done(c))
+                if (c + 1 < NT && !make_khat(c + 1)) break;
+                // P = scale (q k^T) exp(g_i - g_j), i >= j. Column blocks right of this
+                // quarter's rows are all zero.
+                if (!wait_bar(&bs->qkh_done, c & 1, abort)) break;
+                tc_fence_after_sync();
+                {
+                    const float gi = row64 >= 0 ? g_s[s * 64 + row64] : 0.f;
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) {
+                        const int blk = phalf * 2 + bb;
+                        float v[16];
+                        if (blk <= q4) {
+                            uint32_t r[16];
+                            tmem_ld16(tmem + kColQKH + lane_off + blk * 16, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int j = blk * 16 + e;
+                                const float d = (j <= row64) ? gi - g_s[s * 64 + j] : -INFINITY;
+                                v[e] = scale * __uint_as_float(r[e]) * __expf(d);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                        }
+                        if (row64 >= 0) {
+                            st_bf16x8(sm + Lay::kP + sw128(row64, blk * 32), v);
+                            st_bf16x8(sm + Lay::kP + sw128(row64, blk * 32 + 16), v + 8);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bs->p_ready);
+                if (c + 1 < NT && !epi_w(c + 1)) break;
+            }
         }
     } else {
         // ================================================================ chain group
-        // Two warps per TMEM lane quarter, each owning 32 of the tile's 64 columns.
+        // Two warps per TMEM lane quarter, each owning half of the columns. The
+        // state is kept transposed: this thread owns row v = row64 of h^T (the
+        // v tile's column), features [half K/2, half K/2 + K/2).
+        constexpr int FH = K / 2;
         const int ctid = tid - 384, q4 = warp & 3, half = (warp - 12) >> 2;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int row64 = lane < 16 ? q4 * 16 + lane : -1;
-        const int col0 = half * 32;
-        // Row of the state this thread owns: the M = 128 accumulator puts row i in
-        // TMEM lane i; the M = 64 one puts row i in lane 32 (i / 16) + i % 16.
-        const int feat = (K == 128) ? q4 * 32 + lane : row64;
-        const int64_t state_off = (static_cast<int64_t>(b) * H + h) * K * V + vt * kTcBV + col0;
-        float hreg[32];
+        const int col0 = half * 32;   // v-columns of this warp in the v_new / o epilogues
+        const int f0 = half * FH;     // features of this warp in the state epilogue
+        const uint32_t ht_off = (f0 >> 6) * Lay::kKb + Lay::kHT;   // h^T block inside a stage
+        const uint32_t ht_byte = (f0 & 63) * 2;
+        const int64_t state_off = (static_cast<int64_t>(b) * H + h) * K * V + vt * kTcBV;
+        float hreg[FH];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            hreg[j] = (feat >= 0 && h0) ? h0[state_off + static_cast<int64_t>(feat) * V + j] : 0.f;
-        if (feat >= 0) {
+        for (int j = 0; j < FH; ++j)
+            hreg[j] = (row64 >= 0 && h0) ? h0[state_off + static_cast<int64_t>(f0 + j) * V + row64] : 0.f;
+        if (row64 >= 0) {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                st_bf16x8(sm + Lay::kHS + sw128(feat, col0 * 2 + ch * 16), &hreg[ch * 8]);
+            for (int ch = 0; ch < FH / 8; ++ch)
+                st_bf16x8(sm + ht_off + sw128(row64, ht_byte + ch * 16), &hreg[ch * 8]);
         }
         fence_proxy_async_smem();
         mbar_arrive(&bs->hs_ready);
@@ -387,7 +414,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int s = c & 1;
             const uint32_t par = c & 1;
             const int t0 = c * 64, n = min(64, T - t0);
-            if (!(ok = wait_bar(&bs->x_done, par, abort))) break;
+            if (!(ok = spin_bar(&bs->x_done, par, abort))) break;
             tc_fence_after_sync();
             const float g_last = g_s[s * 64 + n - 1];
             const float gate = (row64 >= 0 && row64 < n) ? __expf(g_last - g_s[s * 64 + row64]) : 0.f;
@@ -397,7 +424,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
                 uint32_t r[16];
-                tmem_ld16(tmem + kColU0 + 64 * s + col0 + lane_off + blk * 16, r);
+                tmem_ld16(tmem + kColWU + K + col0 + lane_off + blk * 16, r);
                 tmem_wait_ld();
                 if (row64 >= 0) {
                     float v[16], vg[16];
@@ -416,33 +443,35 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->vn_ready);
-            if (!(ok = wait_bar(&bs->h_done, par, abort))) break;
+            // h^T = h^T exp(g_last) + (dh)^T; bf16 copy into the next chunk's stage
+            if (!(ok = spin_bar(&bs->h_done, par, abort))) break;
             tc_fence_after_sync();
-            // h = h exp(g_last) + k^T v_gated; bf16 copy for the next chunk
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
+            for (int blk = 0; blk < FH / 16; ++blk) {
                 uint32_t r[16];
-                tmem_ld16(tmem + kColH + col0 + lane_off + blk * 16, r);
+                tmem_ld16(tmem + kColHT + f0 + lane_off + blk * 16, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     hreg[blk * 16 + e] = fmaf(hreg[blk * 16 + e], decay, __uint_as_float(r[e]));
             }
-            if (feat >= 0) {
+            if (row64 >= 0) {
+                unsigned char *dst = sm + (s ^ 1) * Lay::kStage + ht_off;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    st_bf16x8(sm + Lay::kHS + sw128(feat, col0 * 2 + ch * 16), &hreg[ch * 8]);
+                for (int ch = 0; ch < FH / 8; ++ch) st_bf16x8(dst + sw128(row64, ht_byte + ch * 16), &hreg[ch * 8]);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->hs_ready);
             // o = scale exp(g_t) q h + P v_new -> bf16 staging -> TMA store
+            if (!(ok = wait_bar(&bs->o_done, par, abort))) break;
+            tc_fence_after_sync();
             if (ctid == 0) bulk_wait_group_read0();
             named_sync(2, kChainThreads);
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
                 uint32_t rq[16], rp[16];
-                tmem_ld16(tmem + kColQH + col0 + lane_off + blk * 16, rq);
+                tmem_ld16(tmem + kColQKH + 64 + col0 + lane_off + blk * 16, rq);
                 tmem_ld16(tmem + kColPV + col0 + lane_off + blk * 16, rp);
                 tmem_wait_ld();
                 if (row64 >= 0) {
@@ -463,9 +492,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 bulk_commit_group();
             }
         }
-        if (ok && feat >= 0 && h_final) {
+        if (ok && row64 >= 0 && h_final) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) h_final[state_off + static_cast<int64_t>(feat) * V + j] = hreg[j];
+            for (int j = 0; j < FH; ++j) h_final[state_off + static_cast<int64_t>(f0 + j) * V + row64] = hreg[j];
         }
         if (ctid == 0) bulk_wait_group0();
     }
