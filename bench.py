@@ -118,49 +118,122 @@ def ncu_traffic(kernel, workload):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    """SM clock and clock-event reasons seen while the timed steps run.
 
-    def __init__(self, device):
-        ident = None
+    A host thread reads them through NVML (libnvidia-ml, read-only queries)
+    about every millisecond, so that even a timed region of a few milliseconds
+    gets samples; without NVML it polls nvidia-smi every 100 ms instead. Only
+    samples taken between mark_start() and mark_end() are reported; when the
+    region is shorter than the sampling period the nearest sample stands in and
+    "window" says so."""
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    # nvmlClocksEventReason* bit values from the public NVML header
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device, period_s=0.001):
+        import threading
+        self.samples = []          # (perf_counter, sm_mhz, set of reasons)
+        self.max_mhz = None
+        self.source = None
+        self.t0 = self.t1 = None
+        self._halt = threading.Event()
+        self._period = period_s
+        self._thread = None
+        uuid = None
         try:
-            ident = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
         except Exception:
-            ident = str(device.index or 0)
+            pass
+        if self._open_nvml(uuid):
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
+        else:
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._run_smi, args=(uuid,), daemon=True)
+        self._thread.start()
+
+    def _open_nvml(self, uuid):
+        import ctypes
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if uuid is None or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return False
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._lib, self._h = lib, h
+            return True
         except Exception:
-            self.proc = None
+            return False
+
+    def _run_nvml(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._halt.is_set():
+            if (self._lib.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0 and
+                    self._reasons_fn(self._h, ctypes.byref(rs)) == 0):
+                names = {n for n, bit in self.BITS.items() if rs.value & bit}
+                self.samples.append((time.perf_counter(), float(clk.value), names))
+            time.sleep(self._period)
+
+    def _run_smi(self, uuid):
+        try:
+            proc = subprocess.Popen(["nvidia-smi", f"--id={uuid}" if uuid else "--id=0",
+                                     f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                    text=True)
+        except Exception:
+            return
+        while not self._halt.is_set():
+            line = proc.stdout.readline()
+            if not line:
+                break
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            self.max_mhz = mx
+            names = {n for n, v in zip(self.NAMES, parts[2:6]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), sm, names))
+        proc.terminate()
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        for line in out.splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
-                continue
+        self._halt.set()
+        self._thread.join(timeout=5)
+        if self.source == "nvml":
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(self.NAMES, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                self._lib.nvmlShutdown()
+            except Exception:
+                pass
+        inside = [s for s in self.samples if self.t0 is not None and self.t0 <= s[0] <= self.t1]
+        window = "timed region"
+        if not inside and self.samples and self.t0 is not None:
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+            window = "nearest sample to a timed region shorter than the sampling period"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": self.source}
+        reasons = set().union(*(s[2] for s in inside))
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "sm_min_mhz": min(s[1] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "source": self.source, "window": window}
 
 
 # --------------------------------------------------------------------------- distributed
@@ -312,12 +385,15 @@ def bench_ours(args, w, world, rank, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(dev)
+    time.sleep(0.05)   # let the sampler take its first readings
+    clocks.mark_start()
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
         step(step_events[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    clocks.mark_end()
     clk = clocks.stop()
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -405,7 +481,7 @@ def bench_ours(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
