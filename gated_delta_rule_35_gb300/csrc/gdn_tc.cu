@@ -7,23 +7,28 @@
 //      parallel over all chunks, to a bf16 workspace [B, T, H, 64].
 //   2. gdn_fused_tc_kernel (this file): recompute_w_u, chunk_fwd_h and
 //      chunk_fwd_o fused. One CTA owns one (b, h, 64-wide V tile) and walks the
-//      chunks in order with its [K, 64] slice of the state in registers (fp32)
-//      and in shared memory (bf16, the MMA operand); h, w, u and v_new never
-//      reach HBM.
+//      chunks in order. The state lives in tensor memory in fp32, with a bf16
+//      copy in shared memory as an MMA operand; h, w, u and v_new never reach HBM.
 //
-// Per chunk (C = 64 tokens), D_* accumulators in tensor memory:
-//   TMA      q, k [64 x K], the v tile [64 x 64], A diag(beta) [64 x 64] (rows past T read 0)
-//   MMA_QK   D_QK = q k^T
-//   epi P    P_ij = scale (q_i.k_j) exp(g_i - g_j), i >= j  -> bf16 operand
-//            k_hat = exp(g) * k                             -> bf16 operand
-//   MMA_W    D_W = A diag(beta) k_hat   (= w)    MMA_U  D_U = A diag(beta) v (= u)
-//   MMA_QH   D_QH = q h
-//   epi W    w -> bf16 operand
-//   MMA_X    D_U += (-w) h            (= v_new, negated-A MMA)
-//   epi X    v_new and v_new * exp(g_last - g_t) -> bf16 operands
-//   MMA_PV   D_PV = P v_new           MMA_H  D_H = k^T (v_new * exp(g_last - g_t))
-//   epi H    h = h * exp(g_last) + D_H (fp32 registers), bf16 copy for the next chunk
-//   epi O    o = scale exp(g_t) D_QH + D_PV -> bf16 -> TMA store
+// Per chunk (C = 64 tokens), with A' = A diag(beta exp(g)) so that
+// w = A diag(beta) (exp(g) k) = A' k. Accumulators live in tensor memory, one
+// row per TMEM lane; "." marks operand rows whose products are never read:
+//   W    [A'; .] k                      W rows 0-63 = w
+//   U    [0; A diag(beta)] v            X rows 64-127 = u, X rows 0-63 = 0
+//   BIG  [q; -w] [h^T | k]              X += [q h; -w h]  (rows 64-127: v_new)
+//                                       QK rows 0-63 += q k^T (cleared after each read)
+//   HT   [v_g; v_g]^T k                 h^T += v_g^T k, v_g = v_new exp(g_last - g)
+//   PV   [P; .] v_new                   O += P v_new
+// TMA writes q and k straight into the stacked operands' halves; the prep group
+// builds A' and the per-chunk decay tables; the w epilogue writes -w under q.
+// The chain group turns QK into P = scale (q k^T) exp(g_i - g_j) (i >= j),
+// normally as QK times a row and a column factor of exp(g_i - g_j) taken about
+// g_last / 2 (per-element exponentials only for chunks whose decay could
+// overflow those factors). It seeds O with scale exp(g) (q h), writes v_new and
+// v_g, keeps the state (pre-decayed by the next chunk's exp(g_last), so that
+// HT completes the update) and sends o to HBM. From one chunk to the next the
+// dependency chain is BIG -> v_new -> HT -> bf16 h^T -> BIG; W, U and PV fill
+// the tensor pipe around it.
 #include "gdn_internal.h"
 #include "tc_common.cuh"
 
@@ -32,45 +37,46 @@ namespace {
 
 using namespace ptx;
 
-// 20 warps: 0 MMA issuer, 1 TMA producer, 2-3 scale group, 4-11 prep group, 12-19 chain group
-constexpr int kTcThreads = 640;
-constexpr int kScaleThreads = 64, kPrepThreads = 256, kChainThreads = 256;
+// 16 warps: 0 MMA issuer, 1 TMA producer, 2-3 and 6-7 prep group, 4-5 w
+// epilogue, 8-15 chain group. A warp reaches the TMEM lanes of quarter warp % 4.
+constexpr int kTcThreads = 512;
+constexpr int kPrepThreads = 128, kWThreads = 64, kChainThreads = 256;
 constexpr int kTcBV = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
 
-// Shared-memory map (bytes from a 1024-aligned base).
+// Shared-memory map (bytes from a 1024-aligned base). Every tile is 64 rows of
+// 128 bytes with the 128-byte swizzle, as TMA writes it.
 template <int K>
 struct TcLayout {
     static constexpr int KB = K / 64;                            // 64-feature blocks
-    // Two input stages. Per 64-feature block: k rows | h^T rows | q rows (8 KB
-    // each, K-major, 128-byte swizzle), then A diag(beta). k and h^T are
-    // adjacent so that together they form one 128-row operand.
-    static constexpr uint32_t kKb = 24576;                        // per-block stride
-    static constexpr uint32_t kHT = 8192, kQ = 16384;             // offsets in a block
-    static constexpr uint32_t kAb = KB * kKb;                     // offset in a stage
-    static constexpr uint32_t kStage = kAb + 8192;
-    static constexpr uint32_t kKHV = 2 * kStage;                  // exp(g) k (KB x 8 KB) | v tile
-    static constexpr uint32_t kW = kKHV + (KB + 1) * 8192;        // -w operand, KB x 8 KB
-    static constexpr uint32_t kP = kW + KB * 8192;                // P
-    static constexpr uint32_t kVN = kP + 8192;                    // v_new
-    static constexpr uint32_t kVG = kVN + 8192;                   // v_new exp(g_last - g)
-    static constexpr uint32_t kOS = kVG + 8192;                   // o staging for the TMA store
-    static constexpr uint32_t kG = kOS + 8192;                    // g[2][64], exp(g)[2][64]
-    static constexpr uint32_t kBar = kG + 1024;                   // mbarriers, flags
+    // Two stages, one per chunk parity. Per 64-feature block the stacked
+    // operands [q; -w] and [h^T; k] (16 KB each: TMA writes q and k straight
+    // into their halves), then v | zero tile | A diag(beta), [0; A diag(beta)]
+    // being U's A operand. W and HT read k N-major out of [h^T; k] (atoms 16 KB
+    // apart); HT reads the one v_g tile as both halves of its A operand.
+    static constexpr uint32_t kStAbig = 0, kStBbig = KB * 16384;
+    static constexpr uint32_t kStV = 2 * KB * 16384, kStZ = kStV + 8192, kStA = kStZ + 8192;
+    static constexpr uint32_t kStage = kStA + 8192;
+    static constexpr uint32_t kP = 2 * kStage;                   // P
+    static constexpr uint32_t kAp = kP + 8192;                   // A'
+    static constexpr uint32_t kVN = kAp + 8192;                  // v_new
+    static constexpr uint32_t kVG = kVN + 8192;                  // v_g
+    static constexpr uint32_t kG = kVG + 8192;                   // decay tables, 4 chunk slots
+    static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
     static constexpr uint32_t kBytes = kBar + 256;
 };
 
-// TMEM columns of the 512-column allocation: [w | u] (K + 64), [q k^T | q h]
-// (128), (dh)^T (K), P v_new (64).
-constexpr uint32_t kColWU = 0, kColQKH = 192, kColHT = 320, kColPV = 448;
+// TMEM columns: X-region [X (64) | QK (64)], O (64), W (K), HT (K).
+constexpr uint32_t kColX = 0, kColQK = 64, kColO = 128, kColW = 192, kColHT = 320;
 
 struct Bars {
-    uint64_t full[2], empty[2], v_full;             // TMA: stage / v tile filled, stage released
-    uint64_t w_done, x_done, qkh_done, h_done, o_done;   // MMA completions (tcgen05.commit)
-    uint64_t g_ready;                               // scale group: g of the chunk in place
-    uint64_t kh_ready, p_ready, w_ready;            // prep group: operands written
-    uint64_t hs_ready, vn_ready, o_free;            // chain group
+    uint64_t full[2], empty[2];                     // TMA stages
+    uint64_t big_done, w_done, h_done, o_done;      // MMA completions (tcgen05.commit)
+    uint64_t g_ready[4], ap_ready;                  // prep group (g_ready per table slot)
+    uint64_t w_ready;                               // w epilogue
+    uint64_t xo_ready, vn_ready, hs_ready;          // chain group
+    uint64_t drain;                                 // every MMA issued is done
     uint32_t abort, tmem;
 };
 
@@ -87,9 +93,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
     return true;
 }
-// Polling variant for the latency-critical roles (MMA issuer, chain group): a
-// suspended waiter can take hundreds of cycles to resume after the phase
-// completes.
+// Polling variant for the latency-critical roles: a suspended waiter can take
+// hundreds of cycles to resume after the phase completes.
 __device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -104,25 +109,45 @@ __device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatil
         }
     }
 }
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// A warp leaves its loop together: the tcgen05 loads that follow a wait are
+// warp-collective.
+__device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
+__device__ __forceinline__ void store_bf16x8_global(void *dst, const float *v) {
+    uint4 u = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                         pack_bf16(v[6], v[7]));
+    *reinterpret_cast<uint4 *>(dst) = u;
+}
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
 }
 
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
-                    const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ g,
-                    const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V,
-                    float scale, uint32_t *status) {
+                    const float *__restrict__ g, const float *__restrict__ h0,
+                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
+                    float scale, int l2_prefetch, uint32_t *status) {
     using Lay = TcLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so
     // that every access through it stays a shared-memory access.
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float *g_s = reinterpret_cast<float *>(sm + Lay::kG);   // [2][64] g (0 past T)
-    float *eg_s = g_s + 128;                                 // [2][64] exp(g) (0 past T)
+    // Per chunk slot (c & 3), 0 past T where marked: g; exp(g) (0); exp(g_last - g)
+    // (0); and the two factors of exp(g_i - g_j) about g_ref = g_last / 2,
+    // scale exp(g_i - g_ref) (0) and exp(g_ref - g_j) (0), usable while |g_last|
+    // stays small enough for both to be finite fp32 numbers (flag fz_s).
+    float *g_s = reinterpret_cast<float *>(sm + Lay::kG);
+    float *eg_s = g_s + 256;
+    float *gate_s = g_s + 512;
+    float *rf_s = g_s + 768;
+    float *cf_s = g_s + 1024;
+    int *fz_s = reinterpret_cast<int *>(g_s + 1280);
     Bars *bs = reinterpret_cast<Bars *>(sm + Lay::kBar);
     volatile uint32_t *abort = &bs->abort;
 
@@ -130,35 +155,36 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (T + 63) / 64;
 
+    // the zero tiles of both stages, read by U as the zero halves of its operands
+    for (int i = tid; i < 1024; i += kTcThreads)
+        st_shared_v4(sm + (i >> 9) * Lay::kStage + Lay::kStZ + (i & 511) * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(&bs->tmem, kTmemCols);
         tmem_relinquish();
     }
     if (tid == 32) {
-        mbar_init(&bs->full[0], 1);
-        mbar_init(&bs->full[1], 1);
-        mbar_init(&bs->empty[0], 1);
-        mbar_init(&bs->empty[1], 1);
-        mbar_init(&bs->v_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bs->full[s], 1);
+            mbar_init(&bs->empty[s], 1);
+        }
+        mbar_init(&bs->big_done, 1);
         mbar_init(&bs->w_done, 1);
-        mbar_init(&bs->x_done, 1);
-        mbar_init(&bs->qkh_done, 1);
         mbar_init(&bs->h_done, 1);
         mbar_init(&bs->o_done, 1);
-        mbar_init(&bs->g_ready, kScaleThreads);
-        mbar_init(&bs->kh_ready, kPrepThreads);
-        mbar_init(&bs->p_ready, kPrepThreads);
-        mbar_init(&bs->w_ready, kPrepThreads);
+        for (int i = 0; i < 4; ++i) mbar_init(&bs->g_ready[i], kPrepThreads);
+        mbar_init(&bs->ap_ready, kPrepThreads);
+        mbar_init(&bs->w_ready, kWThreads);
+        mbar_init(&bs->xo_ready, kChainThreads / 2);
+        mbar_init(&bs->vn_ready, kChainThreads / 2);
         mbar_init(&bs->hs_ready, kChainThreads);
-        mbar_init(&bs->vn_ready, kChainThreads);
-        mbar_init(&bs->o_free, kChainThreads);
+        mbar_init(&bs->drain, 1);
         bs->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_a);
-        prefetch_tmap(&tm_o);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -169,334 +195,420 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idWU = idesc_bf16(64, K + 64, false, true);
-            constexpr uint32_t idX = idesc_bf16(64, 64, false, false, true);
-            constexpr uint32_t idQKH = idesc_bf16(64, 128, false, false);
-            constexpr uint32_t idHT = idesc_bf16(64, K, true, true);
-            constexpr uint32_t idPV = idesc_bf16(64, 64, false, true);
-            const uint32_t s_khv = s_base + Lay::kKHV, s_w = s_base + Lay::kW, s_p = s_base + Lay::kP;
+            constexpr uint32_t idW = idesc_bf16(128, K, false, true);
+            constexpr uint32_t idU = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t idBIG = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idHT = idesc_bf16(128, K, true, true);
+            constexpr uint32_t idPV = idesc_bf16(128, 64, false, true);
+            const uint32_t s_p = s_base + Lay::kP, s_ap = s_base + Lay::kAp;
             const uint32_t s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
-            // [w | u] = A diag(beta) [exp(g) k | v]
-            auto issue_wu = [&](int s) {
-                const uint32_t ab = s_base + s * Lay::kStage + Lay::kAb;
+            // W = [A'; .] k, k read N-major from the stage's [h^T; k]
+            auto issue_w = [&](int s) {
+                const uint32_t kt = s_base + s * Lay::kStage + Lay::kStBbig + 8192;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColWU, smem_desc(ab + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(s_khv + ks * 2048, 8192, 1024, kLayoutSw128), idWU, ks > 0);
+                    mma_bf16(tmem + kColW, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(kt + ks * 2048, 16384, 1024, kLayoutSw128), idW, ks > 0);
                 mma_commit(&bs->w_done);
             };
-            bool ok = spin_bar(&bs->full[0], 0, abort) && spin_bar(&bs->v_full, 0, abort) &&
-                      spin_bar(&bs->kh_ready, 0, abort);
+            // X = [0; A diag(beta)] v
+            auto issue_u = [&](int s) {
+                const uint32_t st = s_base + s * Lay::kStage;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColX, smem_desc(st + Lay::kStZ + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(st + Lay::kStV + ks * 2048, 8192, 1024, kLayoutSw128), idU,
+                             ks > 0);
+            };
+            // O += [P; .] v_new of chunk cp
+            auto issue_pv = [&](int cp) {
+                const uint32_t vn = s_vn;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColO, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
+                             smem_desc(vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, 1);
+                mma_commit(&bs->o_done);
+            };
+            bool ok = spin_bar(&bs->full[0], 0, abort) && spin_bar(&bs->ap_ready, 0, abort);
             if (ok) {
                 tc_fence_after_sync();
-                issue_wu(0);
+                issue_w(0);
+                issue_u(0);
             }
             for (int c = 0; ok && c < NT; ++c) {
                 const int s = c & 1;
                 const uint32_t par = c & 1;
-                const uint32_t st = s_base + s * Lay::kStage;
-                // v_new = u - w h (accumulates onto u)
+                // X += [q; -w] [h^T | k] (q and k landed before W(c) was issued)
                 if (!(ok = spin_bar(&bs->hs_ready, par, abort) && spin_bar(&bs->w_ready, par, abort)))
                     break;
                 tc_fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks)
-                    mma_bf16(tmem + kColWU + K,
-                             smem_desc(s_w + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(st + (ks >> 2) * Lay::kKb + Lay::kHT + (ks & 3) * 32, 16, 1024,
-                                       kLayoutSw128),
-                             idX, 1);
-                mma_commit(&bs->x_done);
-                // [q k^T | q h]: k and h^T rows stacked as one operand
-                if (c >= 1 && !(ok = spin_bar(&bs->o_free, (c - 1) & 1, abort))) break;
-                tc_fence_after_sync();
+                const uint32_t st = s_base + s * Lay::kStage;
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * Lay::kKb + (ks & 3) * 32;
-                    mma_bf16(tmem + kColQKH, smem_desc(st + off + Lay::kQ, 16, 1024, kLayoutSw128),
-                             smem_desc(st + off, 16, 1024, kLayoutSw128), idQKH, ks > 0);
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmem + kColX, smem_desc(st + Lay::kStAbig + off, 16, 1024, kLayoutSw128),
+                             smem_desc(st + Lay::kStBbig + off, 16, 1024, kLayoutSw128), idBIG, 1);
                 }
-                mma_commit(&bs->qkh_done);
-                // (dh)^T = (v_new exp(g_last - g))^T k; the stage's last reader
+                mma_commit(&bs->big_done);
+                // next chunk's w, in the gap before v_new is ready, if its inputs
+                // are already there; otherwise after HT(c), which must not queue
+                // behind it in the in-order tensor pipe
+                bool w_next = c + 1 < NT;
+                if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1) &&
+                    mbar_test_wait(&bs->ap_ready, (c + 1) & 1)) {
+                    tc_fence_after_sync();
+                    issue_w(s ^ 1);
+                    w_next = false;
+                }
+                // h^T += v_g^T k
                 if (!(ok = spin_bar(&bs->vn_ready, par, abort))) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColHT, smem_desc(s_vg + ks * 2048, 8192, 1024, kLayoutSw128),
-                             smem_desc(st + ks * 2048, Lay::kKb, 1024, kLayoutSw128), idHT, ks > 0);
+                    mma_bf16(tmem + kColHT, smem_desc(s_vg + ks * 2048, 0, 1024, kLayoutSw128),
+                             smem_desc(st + Lay::kStBbig + 8192 + ks * 2048, 16384, 1024, kLayoutSw128),
+                             idHT, 1);
                 mma_commit(&bs->h_done);
-                mma_commit(&bs->empty[s]);
-                // next chunk's [w | u]
-                if (c + 1 < NT) {
+                mma_commit(&bs->empty[s]);   // HT(c) is the stage's last reader
+                if (w_next) {
                     if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort) &&
-                               spin_bar(&bs->v_full, (c + 1) & 1, abort) &&
-                               spin_bar(&bs->kh_ready, (c + 1) & 1, abort)))
+                               spin_bar(&bs->ap_ready, (c + 1) & 1, abort)))
                         break;
                     tc_fence_after_sync();
-                    issue_wu(s ^ 1);
+                    issue_w(s ^ 1);
                 }
-                // P v_new
-                if (!(ok = spin_bar(&bs->p_ready, par, abort))) break;
+                // once P, q h and v_new are out of the X-region: next chunk's u, then o
+                if (!(ok = spin_bar(&bs->xo_ready, par, abort))) break;
                 tc_fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColPV, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(s_vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, ks > 0);
-                mma_commit(&bs->o_done);
+                if (c + 1 < NT) issue_u(s ^ 1);
+                issue_pv(c);
             }
+            // nothing of ours may still run when the accumulators are released
+            mma_commit(&bs->drain);
+            mbar_wait(&bs->drain, 0, kWaitNs);
         }
     } else if (warp == 1) {
         // ================================================================ TMA producer
         if (lane == 0) {
+            int issued = 0;   // chunks whose loads were issued
             for (int c = 0; c < NT; ++c) {
-                const int s = c & 1;
+                const int s = c & 1, t0 = c * 64;
                 if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort)) break;
                 unsigned char *st = sm + s * Lay::kStage;
-                const int t0 = c * 64;
-                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 8192);
+                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 16384);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
-                    tma_load_4d(st + kb * Lay::kKb, &tm_k, &bs->full[s], kb * 64, h, t0, b);
-                    tma_load_4d(st + kb * Lay::kKb + Lay::kQ, &tm_q, &bs->full[s], kb * 64, h, t0, b);
+                    tma_load_4d(st + Lay::kStAbig + kb * 16384, &tm_q, &bs->full[s], kb * 64, h, t0, b);
+                    tma_load_4d(st + Lay::kStBbig + kb * 16384 + 8192, &tm_k, &bs->full[s], kb * 64, h,
+                                t0, b);
                 }
-                tma_load_4d(st + Lay::kAb, &tm_a, &bs->full[s], 0, h, t0, b);
-                // the single v slot is free once the previous [w | u] product is done
-                if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
-                mbar_arrive_expect_tx(&bs->v_full, 8192);
-                tma_load_4d(sm + Lay::kKHV + KB * 8192, &tm_v, &bs->v_full, vt * kTcBV, h, t0, b);
-            }
-        }
-    } else if (warp < 4) {
-        // ================================================================ scale group
-        // g of each chunk, loaded one chunk ahead.
-        const int stid = tid - 64;
-        auto load_g = [&](int c) {
-            const int t = c * 64 + stid;
-            return (c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
-        };
-        float g_next = load_g(0);
-        for (int c = 0; c < NT; ++c) {
-            const int s = c & 1;
-            const int n = min(64, T - c * 64);
-            const float g_cur = g_next;
-            g_next = load_g(c + 1);
-            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort)) break;
-            g_s[s * 64 + stid] = g_cur;
-            eg_s[s * 64 + stid] = stid < n ? __expf(g_cur) : 0.f;
-            named_sync(3, kScaleThreads);
-            mbar_arrive(&bs->g_ready);
-        }
-    } else if (warp < 12) {
-        // ================================================================ prep group
-        // Two warps per TMEM lane quarter, each owning half of the columns.
-        const int ptid = tid - 128, q4 = warp & 3, phalf = (warp - 4) >> 2;
-        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
-        // k_hat = exp(g) k for chunk c (same swizzled positions as k)
-        auto make_khat = [&](int c) -> bool {
-            const int s = c & 1;
-            if (!wait_bar(&bs->g_ready, c & 1, abort) || !wait_bar(&bs->full[s], (c >> 1) & 1, abort))
-                return false;
-            const unsigned char *st = sm + s * Lay::kStage;
+                tma_load_4d(st + Lay::kStV, &tm_v, &bs->full[s], vt * kTcBV, h, t0, b);
+                tma_load_4d(st + Lay::kStA, &tm_a, &bs->full[s], 0, h, t0, b);
+                issued = c + 1;
+                // chunk c + 2 into L2 now, so that its stage load, two chunks from
+                // now, is served from L2 rather than HBM. Only when the grid leaves
+                // SMs idle: with every SM busy it costs more than the latency it hides.
+                if (l2_prefetch && c + 2 < NT) {
+                    const int tp = t0 + 128;
 #pragma unroll
-            for (int it = 0; it < KB * 2; ++it) {
-                const int idx = ptid + it * kPrepThreads;   // 16-byte chunk of k
-                const int kb = idx >> 9, rem = idx & 511, row = rem >> 3, ch = rem & 7;
-                const uint32_t off = sw128(row, ch * 16);
-                const uint4 raw = ld_shared_v4(st + kb * Lay::kKb + off);
-                const float sc = eg_s[s * 64 + row];
+                    for (int kb = 0; kb < KB; ++kb) {
+                        tma_prefetch_4d(&tm_q, kb * 64, h, tp, b);
+                        tma_prefetch_4d(&tm_k, kb * 64, h, tp, b);
+                    }
+                    tma_prefetch_4d(&tm_v, vt * kTcBV, h, tp, b);
+                    tma_prefetch_4d(&tm_a, 0, h, tp, b);
+                }
+            }
+            // no copy may still be landing in shared memory when the CTA exits
+            // (after an abort the last loads may have no consumer)
+            for (int c = max(0, issued - 2); c < issued; ++c)
+                mbar_wait(&bs->full[c & 1], (c >> 1) & 1, kWaitNs);
+        }
+    } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
+        // ================================================================ prep group
+        const int ptid = warp < 4 ? tid - 64 : tid - 128;
+        // g of chunk c and of its last valid token, loaded one chunk ahead
+        auto load_g = [&](int c) {
+            const int t = c * 64 + ptid;
+            return (ptid < 64 && c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
+        };
+        auto load_gl = [&](int c) {
+            return (ptid < 64 && c < NT) ? g[(static_cast<int64_t>(b) * T + min(T, c * 64 + 64) - 1) * H + h]
+                                         : 0.f;
+        };
+        // this thread's 16-byte chunks of A diag(beta) all cover columns
+        // [8 (ptid % 8), + 8): their g, one chunk ahead (1 past T: those columns
+        // of A diag(beta) are zero)
+        const int cj = (ptid & 7) * 8;
+        auto load_gj = [&](int c, float (&x)[8]) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int t = c * 64 + cj + m;
+                x[m] = (c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
+            }
+        };
+        float g_next = load_g(0), gl_next = load_gl(0);
+        float gj_next[8];
+        load_gj(0, gj_next);
+        for (int c = 0; c < NT; ++c) {
+            const int s = c & 1, gs = c & 3;
+            const int n = min(64, T - c * 64);
+            const float g_cur = g_next, gl = gl_next;
+            float ej[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) ej[m] = __expf(gj_next[m]);
+            g_next = load_g(c + 1);
+            gl_next = load_gl(c + 1);
+            load_gj(c + 1, gj_next);
+            // Decay tables of chunk c in slot c % 4. Their previous reader, chunk
+            // c - 4, finished before U(c - 3) was issued, and stage s landing for
+            // chunk c needs HT(c - 2). For the same reason the next phase of
+            // g_ready[c % 4] (chunk c + 4) cannot complete before every waiter of
+            // this one has passed.
+            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort)) break;
+            if (ptid < 64) {
+                const float gref = 0.5f * gl;
+                g_s[gs * 64 + ptid] = g_cur;
+                eg_s[gs * 64 + ptid] = ptid < n ? __expf(g_cur) : 0.f;
+                gate_s[gs * 64 + ptid] = ptid < n ? __expf(gl - g_cur) : 0.f;
+                rf_s[gs * 64 + ptid] = ptid < n ? scale * __expf(g_cur - gref) : 0.f;
+                cf_s[gs * 64 + ptid] = ptid < n ? __expf(gref - g_cur) : 0.f;
+                // |g_i - g_ref| <= |g_last| / 2 for cumulative log decays in [g_last, 0]
+                if (ptid == 0) fz_s[gs] = fabsf(gl) <= 160.f;
+            }
+            mbar_arrive(&bs->g_ready[gs]);
+            // A' = A diag(beta) diag(exp(g)); its tile is free once W(c - 1) is done
+            if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
+#pragma unroll 1
+            for (int it = 0; it < 4; ++it) {
+                const int idx = ptid + it * kPrepThreads;   // 16-byte chunk of the tile
+                const int r = idx >> 3, ch = idx & 7;
+                const uint32_t off = sw128(r, ch * 16);
+                const uint4 raw = ld_shared_v4(sm + s * Lay::kStage + Lay::kStA + off);
                 const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
                 uint32_t o4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = unpack_bf16(w4[e]);
-                    o4[e] = pack_bf16(f.x * sc, f.y * sc);
+                    o4[e] = pack_bf16(f.x * ej[2 * e], f.y * ej[2 * e + 1]);
                 }
-                st_shared_v4(sm + Lay::kKHV + kb * 8192 + off, o4[0], o4[1], o4[2], o4[3]);
+                st_shared_v4(sm + Lay::kAp + off, o4[0], o4[1], o4[2], o4[3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bs->kh_ready);
-            return true;
-        };
-        // w (rows 0-63 of [w | u]) -> bf16 operand, negated by the MMA
-        auto epi_w = [&](int c) -> bool {
-            if (!wait_bar(&bs->w_done, c & 1, abort)) return false;
+            mbar_arrive(&bs->ap_ready);
+        }
+    } else if (warp < 6) {
+        // ================================================================ w epilogue
+        // Rows 0-63 of W (lane quarters 0-1) -> -w, bf16, under q in the stage's
+        // stacked operand (that half was last read by BIG(c - 2)).
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int row = (warp & 3) * 32 + lane;
+        for (int c = 0; c < NT; ++c) {
+            if (!warp_all(wait_bar(&bs->w_done, c & 1, abort))) break;
             tc_fence_after_sync();
-#pragma unroll
+#pragma unroll 1
             for (int bb = 0; bb < K / 32; ++bb) {
-                const int blk = phalf * (K / 32) + bb;
-                uint32_t r[16];
-                tmem_ld16(tmem + kColWU + lane_off + blk * 16, r);
+                const int f0 = bb * 32;
+                uint32_t r[32];
+                tmem_ld32(tmem + kColW + lane_off + f0, r);
                 tmem_wait_ld();
-                if (row64 >= 0) {
-                    float v[16];
+                float v[32];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-                    const int f0 = blk * 16;
-                    unsigned char *base = sm + Lay::kW + (f0 >> 6) * 8192;
-                    st_bf16x8(base + sw128(row64, (f0 & 63) * 2), v);
-                    st_bf16x8(base + sw128(row64, (f0 & 63) * 2 + 16), v + 8);
-                }
+                for (int e = 0; e < 32; ++e) v[e] = -__uint_as_float(r[e]);
+                unsigned char *base = sm + (c & 1) * Lay::kStage + Lay::kStAbig + (f0 >> 6) * 16384;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_bf16x8(base + sw128(64 + row, (f0 & 63) * 2 + q * 16), v + q * 8);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->w_ready);
-            return true;
-        };
-        if (make_khat(0) && epi_w(0)) {
-            for (int c = 0; c < NT; ++c) {
-                const int s = c & 1;
-                // the exp(g) k slot is free: its product for chunk c finished (w_done(c))
-                if (c + 1 < NT && !make_khat(c + 1)) break;
-                // P = scale (q k^T) exp(g_i - g_j), i >= j. Column blocks right of this
-                // quarter's rows are all zero.
-                if (!wait_bar(&bs->qkh_done, c & 1, abort)) break;
-                tc_fence_after_sync();
-                {
-                    const float gi = row64 >= 0 ? g_s[s * 64 + row64] : 0.f;
-#pragma unroll
-                    for (int bb = 0; bb < 2; ++bb) {
-                        const int blk = phalf * 2 + bb;
-                        float v[16];
-                        if (blk <= q4) {
-                            uint32_t r[16];
-                            tmem_ld16(tmem + kColQKH + lane_off + blk * 16, r);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int j = blk * 16 + e;
-                                const float d = (j <= row64) ? gi - g_s[s * 64 + j] : -INFINITY;
-                                v[e] = scale * __uint_as_float(r[e]) * __expf(d);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                        }
-                        if (row64 >= 0) {
-                            st_bf16x8(sm + Lay::kP + sw128(row64, blk * 32), v);
-                            st_bf16x8(sm + Lay::kP + sw128(row64, blk * 32 + 16), v + 8);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                mbar_arrive(&bs->p_ready);
-                if (c + 1 < NT && !epi_w(c + 1)) break;
-            }
         }
     } else {
         // ================================================================ chain group
-        // Two warps per TMEM lane quarter, each owning half of the columns. The
-        // state is kept transposed: this thread owns row v = row64 of h^T (the
-        // v tile's column), features [half K/2, half K/2 + K/2).
-        constexpr int FH = K / 2;
-        const int ctid = tid - 384, q4 = warp & 3, half = (warp - 12) >> 2;
+        // Warps on lane quarters 0-1 own token rows 0-63 (P, the O seed, o);
+        // warps on quarters 2-3 own rows 64-127 (v_new). Each handles 32 of the
+        // 64 columns. The state h^T (rows v) sits twice in HT, lanes 0-63 and
+        // 64-127; copy q4 / 2 keeps features [q4 / 2 * K / 2, + K / 2) current,
+        // and each warp owns K / 4 of them.
+        constexpr int NF = K / 4;
+        const int q4 = warp & 3, hf = (warp - 8) >> 2;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-        const int row64 = lane < 16 ? q4 * 16 + lane : -1;
-        const int col0 = half * 32;   // v-columns of this warp in the v_new / o epilogues
-        const int f0 = half * FH;     // features of this warp in the state epilogue
-        const uint32_t ht_off = (f0 >> 6) * Lay::kKb + Lay::kHT;   // h^T block inside a stage
-        const uint32_t ht_byte = (f0 & 63) * 2;
+        const bool upper = q4 < 2;
+        const int row = (q4 & 1) * 32 + lane;
+        const int col0 = hf * 32;
+        const int f0 = (q4 >> 1) * (K / 2) + hf * NF;
         const int64_t state_off = (static_cast<int64_t>(b) * H + h) * K * V + vt * kTcBV;
-        float hreg[FH];
+        auto g_last_of = [&](int c) {
+            return g[(static_cast<int64_t>(b) * T + min(T, c * 64 + 64) - 1) * H + h];
+        };
+        // initial state: bf16 h^T under k in the stacked operand; fp32 in TMEM,
+        // pre-decayed by exp(g_last) of chunk 0
+        {
+            const float d0 = __expf(g_last_of(0));
+#pragma unroll 1
+            for (int blk = 0; blk < NF / 16; ++blk) {
+                const int f = f0 + blk * 16;
+                float v[16];
+                uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < FH; ++j)
-            hreg[j] = (row64 >= 0 && h0) ? h0[state_off + static_cast<int64_t>(f0 + j) * V + row64] : 0.f;
-        if (row64 >= 0) {
-#pragma unroll
-            for (int ch = 0; ch < FH / 8; ++ch)
-                st_bf16x8(sm + ht_off + sw128(row64, ht_byte + ch * 16), &hreg[ch * 8]);
+                for (int e = 0; e < 16; ++e) {
+                    v[e] = h0 ? h0[state_off + static_cast<int64_t>(f + e) * V + row] : 0.f;
+                    r[e] = __float_as_uint(v[e] * d0);
+                }
+                tmem_st16(tmem + kColHT + lane_off + f, r);
+                unsigned char *dst = sm + Lay::kStBbig + (f >> 6) * 16384;
+                st_bf16x8(dst + sw128(row, (f & 63) * 2), v);
+                st_bf16x8(dst + sw128(row, (f & 63) * 2 + 16), v + 8);
+            }
+            if (upper) {   // QK starts at zero (U writes X only)
+                const uint32_t z[16] = {};
+                tmem_st16(tmem + kColQK + lane_off + col0, z);
+                tmem_st16(tmem + kColQK + lane_off + col0 + 16, z);
+            }
+            tmem_wait_st();
         }
         fence_proxy_async_smem();
+        tc_fence_before_sync();
         mbar_arrive(&bs->hs_ready);
         bool ok = true;
+        float g_last_next = NT > 1 ? g_last_of(1) : 0.f;
         for (int c = 0; c < NT; ++c) {
-            const int s = c & 1;
-            const uint32_t par = c & 1;
-            const int t0 = c * 64, n = min(64, T - t0);
-            if (!(ok = spin_bar(&bs->x_done, par, abort))) break;
+            const int t0 = c * 64, n = min(64, T - t0), gs = c & 3;
+            const float d_next = (c + 1 < NT) ? __expf(g_last_next) : 1.f;
+            if (c + 2 < NT) g_last_next = g_last_of(c + 2);   // one chunk ahead
+            if (!(ok = warp_all(wait_bar(&bs->g_ready[gs], (c >> 2) & 1, abort) &&
+                                spin_bar(&bs->big_done, c & 1, abort))))
+                break;
             tc_fence_after_sync();
-            const float g_last = g_s[s * 64 + n - 1];
-            const float gate = (row64 >= 0 && row64 < n) ? __expf(g_last - g_s[s * 64 + row64]) : 0.f;
-            const float so = row64 >= 0 ? scale * eg_s[s * 64 + row64] : 0.f;
-            const float decay = __expf(g_last);
-            // v_new and v_gated -> bf16 operands (token rows, V contiguous)
+            const float *gc = g_s + gs * 64;
+            if (upper) {
+                const bool fz = fz_s[gs];
+                const float gi = gc[row], ri = rf_s[gs * 64 + row];
+                const float *cfc = cf_s + gs * 64;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int j0 = col0 + half * 16;
+                    float v[16];
+                    if (j0 <= (q4 & 1) * 32 + 31) {
+                        float fj[16];
+                        const float *src = fz ? cfc : gc;
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                uint32_t r[16];
-                tmem_ld16(tmem + kColWU + K + col0 + lane_off + blk * 16, r);
-                tmem_wait_ld();
-                if (row64 >= 0) {
+                        for (int m = 0; m < 4; ++m) {
+                            const float4 f4 = *reinterpret_cast<const float4 *>(src + j0 + 4 * m);
+                            fj[4 * m] = f4.x;
+                            fj[4 * m + 1] = f4.y;
+                            fj[4 * m + 2] = f4.z;
+                            fj[4 * m + 3] = f4.w;
+                        }
+                        tmem_ld16f(tmem + kColQK + lane_off + j0, v);
+                        if (fz) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = (j0 + e <= row) ? v[e] * ri * fj[e] : 0.f;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float d = (j0 + e <= row) ? gi - fj[e] : -INFINITY;
+                                v[e] = scale * v[e] * __expf(d);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                    }
+                    st_bf16x8(sm + Lay::kP + sw128(row, j0 * 2), v);
+                    st_bf16x8(sm + Lay::kP + sw128(row, j0 * 2 + 16), v + 8);
+                }
+                {
+                    const uint32_t z[16] = {};
+                    tmem_st16(tmem + kColQK + lane_off + col0, z);
+                    tmem_st16(tmem + kColQK + lane_off + col0 + 16, z);
+                }
+                const float so = scale * eg_s[gs * 64 + row];
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + kColX + lane_off + col0 + half * 16, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(so * __uint_as_float(r[e]));
+                    tmem_st16(tmem + kColO + lane_off + col0 + half * 16, r);
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bs->xo_ready);
+            } else {
+                if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort)))) break;
+                const float gate = gate_s[gs * 64 + row];
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int cc = col0 + half * 16;
                     float v[16], vg[16];
+                    tmem_ld16f(tmem + kColX + lane_off + cc, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) vg[e] = v[e] * gate;
+                    st_bf16x8(sm + Lay::kVN + sw128(row, cc * 2), v);
+                    st_bf16x8(sm + Lay::kVN + sw128(row, cc * 2 + 16), v + 8);
+                    st_bf16x8(sm + Lay::kVG + sw128(row, cc * 2), vg);
+                    st_bf16x8(sm + Lay::kVG + sw128(row, cc * 2 + 16), vg + 8);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bs->vn_ready);
+            }
+            if (!(ok = warp_all(spin_bar(&bs->h_done, c & 1, abort)))) break;
+            tc_fence_after_sync();
+            if (c + 1 < NT) {
+#pragma unroll 1
+                for (int blk = 0; blk < NF / 16; ++blk) {
+                    const int f = f0 + blk * 16;
+                    uint32_t r[16];
+                    tmem_ld16(tmem + kColHT + lane_off + f, r);
+                    tmem_wait_ld();
+                    float v[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         v[e] = __uint_as_float(r[e]);
-                        vg[e] = v[e] * gate;
+                        r[e] = __float_as_uint(v[e] * d_next);
                     }
-                    const uint32_t byte = (col0 + blk * 16) * 2;
-                    st_bf16x8(sm + Lay::kVN + sw128(row64, byte), v);
-                    st_bf16x8(sm + Lay::kVN + sw128(row64, byte + 16), v + 8);
-                    st_bf16x8(sm + Lay::kVG + sw128(row64, byte), vg);
-                    st_bf16x8(sm + Lay::kVG + sw128(row64, byte + 16), vg + 8);
+                    tmem_st16(tmem + kColHT + lane_off + f, r);
+                    unsigned char *dst = sm + ((c + 1) & 1) * Lay::kStage + Lay::kStBbig + (f >> 6) * 16384;
+                    st_bf16x8(dst + sw128(row, (f & 63) * 2), v);
+                    st_bf16x8(dst + sw128(row, (f & 63) * 2 + 16), v + 8);
                 }
+                tmem_wait_st();
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            mbar_arrive(&bs->vn_ready);
-            // h^T = h^T exp(g_last) + (dh)^T; bf16 copy into the next chunk's stage
-            if (!(ok = spin_bar(&bs->h_done, par, abort))) break;
-            tc_fence_after_sync();
-#pragma unroll
-            for (int blk = 0; blk < FH / 16; ++blk) {
-                uint32_t r[16];
-                tmem_ld16(tmem + kColHT + f0 + lane_off + blk * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    hreg[blk * 16 + e] = fmaf(hreg[blk * 16 + e], decay, __uint_as_float(r[e]));
-            }
-            if (row64 >= 0) {
-                unsigned char *dst = sm + (s ^ 1) * Lay::kStage + ht_off;
-#pragma unroll
-                for (int ch = 0; ch < FH / 8; ++ch) st_bf16x8(dst + sw128(row64, ht_byte + ch * 16), &hreg[ch * 8]);
-            }
-            fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->hs_ready);
-            // o = scale exp(g_t) q h + P v_new -> bf16 staging -> TMA store
-            if (!(ok = wait_bar(&bs->o_done, par, abort))) break;
-            tc_fence_after_sync();
-            if (ctid == 0) bulk_wait_group_read0();
-            named_sync(2, kChainThreads);
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                uint32_t rq[16], rp[16];
-                tmem_ld16(tmem + kColQKH + 64 + col0 + lane_off + blk * 16, rq);
-                tmem_ld16(tmem + kColPV + col0 + lane_off + blk * 16, rp);
-                tmem_wait_ld();
-                if (row64 >= 0) {
+            if (upper) {
+                if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort)))) break;
+                tc_fence_after_sync();
+                __nv_bfloat16 *dst = o + ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V +
+                                     vt * kTcBV + col0;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
                     float v[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = fmaf(so, __uint_as_float(rq[e]), __uint_as_float(rp[e]));
-                    const uint32_t byte = (col0 + blk * 16) * 2;
-                    st_bf16x8(sm + Lay::kOS + sw128(row64, byte), v);
-                    st_bf16x8(sm + Lay::kOS + sw128(row64, byte + 16), v + 8);
+                    tmem_ld16f(tmem + kColO + lane_off + col0 + half * 16, v);
+                    if (row < n) {
+                        store_bf16x8_global(dst + half * 16, v);
+                        store_bf16x8_global(dst + half * 16 + 8, v + 8);
+                    }
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            mbar_arrive(&bs->o_free);
-            named_sync(2, kChainThreads);
-            if (ctid == 0) {
-                tma_store_4d(&tm_o, sm + Lay::kOS, vt * kTcBV, h, t0, b);
-                bulk_commit_group();
+        }
+        // final state straight from tensor memory
+        if (warp_all(ok) && h_final) {
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int blk = 0; blk < NF / 16; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + kColHT + lane_off + f0 + blk * 16, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    h_final[state_off + static_cast<int64_t>(f0 + blk * 16 + e) * V + row] = v[e];
             }
         }
-        if (ok && row64 >= 0 && h_final) {
-#pragma unroll
-            for (int j = 0; j < FH; ++j) h_final[state_off + static_cast<int64_t>(f0 + j) * V + row64] = hreg[j];
-        }
-        if (ctid == 0) bulk_wait_group0();
     }
 
     tc_fence_before_sync();
@@ -522,18 +634,22 @@ __global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float
 
 template <int K>
 cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, ma, mo;
+    CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&ma, abeta, 64, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&mo, a.o, a.V, a.H, a.T, a.B))
+        !make_tmap_bthx(&ma, abeta, 64, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(TcLayout<K>::kBytes + 1024);
     cudaError_t e = cudaFuncSetAttribute(gdn_fused_tc_kernel<K>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long ctas = static_cast<long long>(a.V / kTcBV) * a.H * a.B;
     gdn_fused_tc_kernel<K><<<dim3(a.V / kTcBV, a.H, a.B), kTcThreads, smem, s>>>(
-        mq, mk, mv, ma, mo, a.g, a.h0, a.h_final, a.T, a.H, a.V, a.scale, a.status);
+        mq, mk, mv, ma, a.g, a.h0, a.h_final, static_cast<__nv_bfloat16 *>(a.o), a.T, a.H, a.V,
+        a.scale, ctas <= sms ? 1 : 0, a.status);
     return cudaGetLastError();
 }
 

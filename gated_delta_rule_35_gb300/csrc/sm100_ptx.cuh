@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, ui
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
+// Prefetch of a tensor tile into L2 (no shared memory, no completion signal);
+// tiles outside the tensor are skipped.
+__device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int32_t x, int32_t y, int32_t z,
+                                                int32_t w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
 // Tensor store from shared memory; elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const void *tmap, const void *smem_src, int32_t x,
                                              int32_t y, int32_t z, int32_t w) {

@@ -69,6 +69,23 @@ def test_scale_and_zero_state(algo):
     assert rel(o, o_ref) < TOL["bf16"] and rel(hf, hf_ref) < TOL["bf16"]
 
 
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("g_div", [1.0, 0.25])
+def test_strong_decay(algo, g_div):
+    """Forget gates far below 1: a chunk's cumulative log decay reaches about -45
+    (g_div = 1) or about -180 (g_div = 0.25), where the inverse decay factors
+    leave the fp32 range and the exact exp(g_i - g_j) form must be used."""
+    if not have_algo(algo, 128, 128, "bf16"):
+        pytest.skip("not built")
+    x = make_inputs(2, 200, 2, 128, 128, dtype="bf16", seed=21, h0_std=0.1, g_div=g_div)
+    assert float(x["g"].min()) < (-30 if g_div == 1.0 else -150)
+    o, hf = run_gpu(x, algo)
+    o_ref, hf_ref = run_oracle(x)
+    assert np.isfinite(o).all() and np.isfinite(hf).all()
+    assert rel(o, o_ref) < TOL["bf16"], rel(o, o_ref)
+    assert rel(hf, hf_ref) < TOL["bf16"], rel(hf, hf_ref)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_simt_stages_against_chunked_form(dtype):
     """Every SIMT intermediate (A, w, u, v_new, h) against the fp64 chunked form.
