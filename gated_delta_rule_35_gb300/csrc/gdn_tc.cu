@@ -250,18 +250,28 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                              smem_desc(st + Lay::kStBbig + off, 16, 1024, kLayoutSw128), idBIG, 1);
                 }
                 mma_commit(&bs->big_done);
-                // next chunk's w, in the gap before v_new is ready, if its inputs
-                // are already there; otherwise after HT(c), which must not queue
-                // behind it in the in-order tensor pipe
+                // Next chunk's w as soon as its inputs land, if that happens before
+                // v_new is ready; otherwise after HT(c), which must not queue behind
+                // it in the in-order tensor pipe. One loop polls both.
                 bool w_next = c + 1 < NT;
-                if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1) &&
-                    mbar_test_wait(&bs->ap_ready, (c + 1) & 1)) {
-                    tc_fence_after_sync();
-                    issue_w(s ^ 1);
-                    w_next = false;
+                {
+                    const uint64_t t0 = globaltimer_ns();
+                    for (uint32_t i = 1;; ++i) {
+                        if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1) &&
+                            mbar_test_wait(&bs->ap_ready, (c + 1) & 1)) {
+                            tc_fence_after_sync();
+                            issue_w(s ^ 1);
+                            w_next = false;
+                        }
+                        if (mbar_test_wait(&bs->vn_ready, par)) break;
+                        if ((i & 255) == 0) {
+                            if (*abort) { ok = false; break; }
+                            if (globaltimer_ns() - t0 > kWaitNs) { *abort = 1; ok = false; break; }
+                        }
+                    }
+                    if (!ok) break;
                 }
                 // h^T += v_g^T k
-                if (!(ok = spin_bar(&bs->vn_ready, par, abort))) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
