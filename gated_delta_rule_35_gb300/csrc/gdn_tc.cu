@@ -3,8 +3,8 @@
 // Two kernels, following the "WarpDrive" page's pipeline (kernel 5
 // recompute_w_u takes the chunk's WY matrix A as given; kernels 3 chunk_fwd_h
 // and 4 chunk_fwd_o follow it):
-//   1. gdn_wy_tc_kernel (gdn_tc_wy.cu): A diag(beta) for every chunk, in
-//      parallel over all chunks, to a bf16 workspace [B, T, H, 64].
+//   1. gdn_wy_tc_kernel (gdn_tc_wy.cu): A diag(beta) and A diag(beta exp(g)) for
+//      every chunk, in parallel over all chunks, to a bf16 workspace [B, T, H, 128].
 //   2. gdn_fused_tc_kernel (this file): recompute_w_u, chunk_fwd_h and
 //      chunk_fwd_o fused. One CTA owns one (b, h, 64-wide V tile) and walks the
 //      chunks in order. The state lives in tensor memory in fp32, with a bf16
@@ -20,7 +20,7 @@
 //   HT   [v_g; v_g]^T k                 h^T += v_g^T k, v_g = v_new exp(g_last - g)
 //   PV   [P; .] v_new                   O += P v_new
 // TMA writes q and k straight into the stacked operands' halves; the prep group
-// builds A' and the per-chunk decay tables; the w epilogue writes -w under q.
+// builds the per-chunk decay tables; the w epilogue writes -w under q.
 // The chain group turns QK into P = scale (q k^T) exp(g_i - g_j) (i >= j),
 // normally as QK times a row and a column factor of exp(g_i - g_j) taken about
 // g_last / 2 (per-element exponentials only for chunks whose decay could
@@ -52,15 +52,15 @@ struct TcLayout {
     static constexpr int KB = K / 64;                            // 64-feature blocks
     // Two stages, one per chunk parity. Per 64-feature block the stacked
     // operands [q; -w] and [h^T; k] (16 KB each: TMA writes q and k straight
-    // into their halves), then v | zero tile | A diag(beta), [0; A diag(beta)]
+    // into their halves), then v | zero tile | A diag(beta) | A', [0; A diag(beta)]
     // being U's A operand. W and HT read k N-major out of [h^T; k] (atoms 16 KB
     // apart); HT reads the one v_g tile as both halves of its A operand.
     static constexpr uint32_t kStAbig = 0, kStBbig = KB * 16384;
     static constexpr uint32_t kStV = 2 * KB * 16384, kStZ = kStV + 8192, kStA = kStZ + 8192;
-    static constexpr uint32_t kStage = kStA + 8192;
+    static constexpr uint32_t kStAp = kStA + 8192;               // A' (W's A operand rows 0-63)
+    static constexpr uint32_t kStage = kStAp + 8192;
     static constexpr uint32_t kP = 2 * kStage;                   // P
-    static constexpr uint32_t kAp = kP + 8192;                   // A'
-    static constexpr uint32_t kVN = kAp + 8192;                  // v_new
+    static constexpr uint32_t kVN = kP + 8192;                   // v_new
     static constexpr uint32_t kVG = kVN + 8192;                  // v_g
     static constexpr uint32_t kG = kVG + 8192;                   // decay tables, 4 chunk slots
     static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
@@ -73,7 +73,7 @@ constexpr uint32_t kColX = 0, kColQK = 64, kColO = 128, kColW = 192, kColHT = 32
 struct Bars {
     uint64_t full[2], empty[2];                     // TMA stages
     uint64_t big_done, w_done, h_done, o_done;      // MMA completions (tcgen05.commit)
-    uint64_t g_ready[4], ap_ready;                  // prep group (g_ready per table slot)
+    uint64_t g_ready[4];                            // prep group (one per table slot)
     uint64_t w_ready;                               // w epilogue
     uint64_t xo_ready, vn_ready, hs_ready;          // chain group
     uint64_t drain;                                 // every MMA issued is done
@@ -173,7 +173,6 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_init(&bs->h_done, 1);
         mbar_init(&bs->o_done, 1);
         for (int i = 0; i < 4; ++i) mbar_init(&bs->g_ready[i], kPrepThreads);
-        mbar_init(&bs->ap_ready, kPrepThreads);
         mbar_init(&bs->w_ready, kWThreads);
         mbar_init(&bs->xo_ready, kChainThreads / 2);
         mbar_init(&bs->vn_ready, kChainThreads / 2);
@@ -200,14 +199,16 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t idBIG = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idHT = idesc_bf16(128, K, true, true);
             constexpr uint32_t idPV = idesc_bf16(128, 64, false, true);
-            const uint32_t s_p = s_base + Lay::kP, s_ap = s_base + Lay::kAp;
+            const uint32_t s_p = s_base + Lay::kP;
             const uint32_t s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
-            // W = [A'; .] k, k read N-major from the stage's [h^T; k]
+            // W = [A'; .] k, k read N-major from the stage's [h^T; k]; the rows under A'
+            // are whatever follows it (the next stage or P): their products are unused
             auto issue_w = [&](int s) {
                 const uint32_t kt = s_base + s * Lay::kStage + Lay::kStBbig + 8192;
+                const uint32_t ap = s_base + s * Lay::kStage + Lay::kStAp;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColW, smem_desc(s_ap + ks * 32, 16, 1024, kLayoutSw128),
+                    mma_bf16(tmem + kColW, smem_desc(ap + ks * 32, 16, 1024, kLayoutSw128),
                              smem_desc(kt + ks * 2048, 16384, 1024, kLayoutSw128), idW, ks > 0);
                 mma_commit(&bs->w_done);
             };
@@ -229,7 +230,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                              smem_desc(vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, 1);
                 mma_commit(&bs->o_done);
             };
-            bool ok = spin_bar(&bs->full[0], 0, abort) && spin_bar(&bs->ap_ready, 0, abort);
+            bool ok = spin_bar(&bs->full[0], 0, abort);
             if (ok) {
                 tc_fence_after_sync();
                 issue_w(0);
@@ -257,8 +258,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 {
                     const uint64_t t0 = globaltimer_ns();
                     for (uint32_t i = 1;; ++i) {
-                        if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1) &&
-                            mbar_test_wait(&bs->ap_ready, (c + 1) & 1)) {
+                        if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1)) {
                             tc_fence_after_sync();
                             issue_w(s ^ 1);
                             w_next = false;
@@ -281,9 +281,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mma_commit(&bs->h_done);
                 mma_commit(&bs->empty[s]);   // HT(c) is the stage's last reader
                 if (w_next) {
-                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort) &&
-                               spin_bar(&bs->ap_ready, (c + 1) & 1, abort)))
-                        break;
+                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort))) break;
                     tc_fence_after_sync();
                     issue_w(s ^ 1);
                 }
@@ -305,7 +303,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int s = c & 1, t0 = c * 64;
                 if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort)) break;
                 unsigned char *st = sm + s * Lay::kStage;
-                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 16384);
+                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 24576);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_4d(st + Lay::kStAbig + kb * 16384, &tm_q, &bs->full[s], kb * 64, h, t0, b);
@@ -314,6 +312,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
                 tma_load_4d(st + Lay::kStV, &tm_v, &bs->full[s], vt * kTcBV, h, t0, b);
                 tma_load_4d(st + Lay::kStA, &tm_a, &bs->full[s], 0, h, t0, b);
+                tma_load_4d(st + Lay::kStAp, &tm_a, &bs->full[s], 64, h, t0, b);
                 issued = c + 1;
                 // chunk c + 2 into L2 now, so that its stage load, two chunks from
                 // now, is served from L2 rather than HBM. Only when the grid leaves
@@ -327,6 +326,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     }
                     tma_prefetch_4d(&tm_v, vt * kTcBV, h, tp, b);
                     tma_prefetch_4d(&tm_a, 0, h, tp, b);
+                    tma_prefetch_4d(&tm_a, 64, h, tp, b);
                 }
             }
             // no copy may still be landing in shared memory when the CTA exits
@@ -336,6 +336,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         // ================================================================ prep group
+        // Per-chunk decay tables (A' = A diag(beta exp(g)) comes with A diag(beta)
+        // from the WY kernel).
         const int ptid = warp < 4 ? tid - 64 : tid - 128;
         // g of chunk c and of its last valid token, loaded one chunk ahead
         auto load_g = [&](int c) {
@@ -346,30 +348,13 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             return (ptid < 64 && c < NT) ? g[(static_cast<int64_t>(b) * T + min(T, c * 64 + 64) - 1) * H + h]
                                          : 0.f;
         };
-        // this thread's 16-byte chunks of A diag(beta) all cover columns
-        // [8 (ptid % 8), + 8): their g, one chunk ahead (1 past T: those columns
-        // of A diag(beta) are zero)
-        const int cj = (ptid & 7) * 8;
-        auto load_gj = [&](int c, float (&x)[8]) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int t = c * 64 + cj + m;
-                x[m] = (c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
-            }
-        };
         float g_next = load_g(0), gl_next = load_gl(0);
-        float gj_next[8];
-        load_gj(0, gj_next);
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1, gs = c & 3;
             const int n = min(64, T - c * 64);
             const float g_cur = g_next, gl = gl_next;
-            float ej[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) ej[m] = __expf(gj_next[m]);
             g_next = load_g(c + 1);
             gl_next = load_gl(c + 1);
-            load_gj(c + 1, gj_next);
             // Decay tables of chunk c in slot c % 4. Their previous reader, chunk
             // c - 4, finished before U(c - 3) was issued, and stage s landing for
             // chunk c needs HT(c - 2). For the same reason the next phase of
@@ -387,25 +372,6 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (ptid == 0) fz_s[gs] = fabsf(gl) <= 160.f;
             }
             mbar_arrive(&bs->g_ready[gs]);
-            // A' = A diag(beta) diag(exp(g)); its tile is free once W(c - 1) is done
-            if (c >= 1 && !wait_bar(&bs->w_done, (c - 1) & 1, abort)) break;
-#pragma unroll 1
-            for (int it = 0; it < 4; ++it) {
-                const int idx = ptid + it * kPrepThreads;   // 16-byte chunk of the tile
-                const int r = idx >> 3, ch = idx & 7;
-                const uint32_t off = sw128(r, ch * 16);
-                const uint4 raw = ld_shared_v4(sm + s * Lay::kStage + Lay::kStA + off);
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t o4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack_bf16(w4[e]);
-                    o4[e] = pack_bf16(f.x * ej[2 * e], f.y * ej[2 * e + 1]);
-                }
-                st_shared_v4(sm + Lay::kAp + off, o4[0], o4[1], o4[2], o4[3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bs->ap_ready);
         }
     } else if (warp < 6) {
         // ================================================================ w epilogue
@@ -627,7 +593,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Stage export: A diag(beta) bf16 [B, T, H, 64] -> fp32 [B, T_pad, H, 64] (pad rows 0).
+// Stage export: A diag(beta), columns 0-63 of the bf16 workspace [B, T, H, 128],
+// -> fp32 [B, T_pad, H, 64] (pad rows 0).
 __global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float *__restrict__ dst,
                                     int B, int T, int T_pad, int H) {
     const int64_t n = static_cast<int64_t>(B) * T_pad * H * 64;
@@ -637,7 +604,7 @@ __global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float
         const int hh = static_cast<int>(row % H);
         const int64_t bt = row / H;
         const int t = static_cast<int>(bt % T_pad), bb = static_cast<int>(bt / T_pad);
-        dst[i] = t < T ? __bfloat162float(src[((static_cast<int64_t>(bb) * T + t) * H + hh) * 64 + i % 64])
+        dst[i] = t < T ? __bfloat162float(src[((static_cast<int64_t>(bb) * T + t) * H + hh) * 128 + i % 64])
                        : 0.f;
     }
 }
@@ -647,7 +614,7 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&ma, abeta, 64, a.H, a.T, a.B))
+        !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(TcLayout<K>::kBytes + 1024);
     cudaError_t e = cudaFuncSetAttribute(gdn_fused_tc_kernel<K>,
@@ -670,7 +637,7 @@ bool tc_supported(int K, int V, gdn_dtype dtype) {
 }
 
 size_t tc_workspace_bytes(int B, int T, int H, int, int) {
-    return align_up(static_cast<size_t>(B) * T * H * 64 * sizeof(__nv_bfloat16));
+    return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
 }
 
 int tc_launches(const char **names, int max_names) {

@@ -1,7 +1,8 @@
 // WY build on the tensor cores: for every 64-token chunk, the matrix
 // A = (I + L)^-1 of the "WarpDrive" page's recompute_w_u (kernel 5 takes it as
 // given), with L_ij = beta_i (k_i . k_j) exp(g_i - g_j) for i > j, written out as
-// A diag(beta) in bf16 [B, T, H, 64].
+// A diag(beta) and A diag(beta exp(g)) in bf16 [B, T, H, 128] (columns 0-63
+// and 64-127).
 //
 // One CTA per (chunk, h, b); the chunks are independent, so the grid is as
 // wide as the problem and several CTAs share an SM. With X the inverse of the
@@ -19,7 +20,7 @@
 //   MMA 2   [Y1; U] = [N1; N2] X
 //   MMA 3   [X Y1; U Y1] = [X; U] Y1  ->  A0 = X - X Y1, Y2 = U - U Y1
 //   MMA 4   Z = A0 Y2                  ->  A  = A0 - Z
-//   epi     A diag(beta) -> bf16 -> TMA store
+//   epi     A diag(beta), A diag(beta exp(g)) -> bf16 -> TMA store
 // The correction products run with bf16 operands and fp32 accumulation; the
 // block-diagonal part and the subtractions stay fp32.
 #include "gdn_internal.h"
@@ -45,8 +46,8 @@ struct WyLayout {
     static constexpr uint32_t kY = kXU + 16384;            // Y1, then Y2 (bf16, rows along N)
     static constexpr uint32_t kOut = kY + 8192;            // A diag(beta) staging
     static constexpr uint32_t kLd = kOut + 8192;           // diagonal blocks fp32 [4][16][17]
-    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;
-    static constexpr uint32_t kBytes = kMisc + 768;
+    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;   // g, beta, beta exp(g); barriers
+    static constexpr uint32_t kBytes = kMisc + 1024;
 };
 
 template <int K>
@@ -61,7 +62,8 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     float *Ld = reinterpret_cast<float *>(sm + Lay::kLd);
     float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);
     float *b_s = g_s + 64;
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 512);
+    float *eb_s = g_s + 128;   // beta exp(g): the column scale of A diag(beta exp(g))
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 768);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
 
@@ -92,6 +94,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         g_s[tid] = gv;
         b_s[tid] = bv;
+        eb_s[tid] = bv * __expf(gv);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -255,10 +258,19 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             float v[16];
             load16(blk, v);
             if (tid < 64) {
+                // A diag(beta) and A diag(beta exp(g)); the second goes to the
+                // [N1; N2] tile, free since the first merge product
+                float v2[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = (keep[blk * 16 + e] - v[e]) * b_s[blk * 16 + e];
+                for (int e = 0; e < 16; ++e) {
+                    const float a = keep[blk * 16 + e] - v[e];
+                    v[e] = a * b_s[blk * 16 + e];
+                    v2[e] = a * eb_s[blk * 16 + e];
+                }
                 st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32), v);
                 st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32 + 16), v + 8);
+                st_bf16x8(sm + Lay::kN + sw128(r, blk * 32), v2);
+                st_bf16x8(sm + Lay::kN + sw128(r, blk * 32 + 16), v2 + 8);
             }
         }
         fence_proxy_async_smem();
@@ -266,6 +278,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     __syncthreads();
     if (tid == 0) {
         tma_store_4d(&tm_a, sm + Lay::kOut, 0, h, t0, b);
+        tma_store_4d(&tm_a, sm + Lay::kN, 64, h, t0, b);
         bulk_commit_group();
         bulk_wait_group0();
     }
@@ -279,7 +292,7 @@ done:
 template <int K>
 cudaError_t launch_wy(const Args &a, void *abeta, cudaStream_t s) {
     CUtensorMap mk, ma;
-    if (!make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 64, a.H, a.T, a.B))
+    if (!make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(WyLayout<K>::kBytes + 1024);
     cudaError_t e = cudaFuncSetAttribute(gdn_wy_tc_kernel<K>,
