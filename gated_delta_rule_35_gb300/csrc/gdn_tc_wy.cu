@@ -46,8 +46,8 @@ struct WyLayout {
     static constexpr uint32_t kY = kXU + 16384;            // Y1, then Y2 (bf16, rows along N)
     static constexpr uint32_t kOut = kY + 8192;            // A diag(beta) staging
     static constexpr uint32_t kLd = kOut + 8192;           // diagonal blocks fp32 [4][16][17]
-    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;   // g, beta, beta exp(g); barriers
-    static constexpr uint32_t kBytes = kMisc + 1024;
+    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;   // g, beta, beta exp(g), cf; barriers
+    static constexpr uint32_t kBytes = kMisc + 1280;
 };
 
 template <int K>
@@ -63,7 +63,11 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     float *g_s = reinterpret_cast<float *>(sm + Lay::kMisc);
     float *b_s = g_s + 64;
     float *eb_s = g_s + 128;   // beta exp(g): the column scale of A diag(beta exp(g))
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 768);
+    // exp(g_ref - g_j) with g_ref = g_last / 2: with the row factor
+    // beta_i exp(g_i - g_ref) it gives beta_i exp(g_i - g_j) without an
+    // exponential per element, while |g_last| keeps both factors finite
+    float *cf_s = g_s + 192;
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 1024);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
 
@@ -85,6 +89,9 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int kb = 0; kb < KB; ++kb)
             tma_load_4d(sm + Lay::kK + kb * 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
     }
+    const float g_last = g[(static_cast<int64_t>(b) * T + t0 + n - 1) * H + h];
+    const float g_ref = 0.5f * g_last;
+    const bool fz = fabsf(g_last) <= 160.f;   // |g_i - g_ref| <= |g_last| / 2 for decays <= 0
     if (tid < 64) {
         float gv = 0.f, bv = 0.f;
         if (tid < n) {
@@ -95,6 +102,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         g_s[tid] = gv;
         b_s[tid] = bv;
         eb_s[tid] = bv * __expf(gv);
+        cf_s[tid] = tid < n ? __expf(g_ref - gv) : 0.f;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -139,16 +147,30 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     {
         const int r = lane < 16 ? warp * 16 + lane : -1, rb = r >> 4;
         const float gr = r >= 0 ? g_s[r] : 0.f, br = r >= 0 ? b_s[r] : 0.f;
+        const float rf = br * __expf(gr - g_ref);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
             float v[16];
             load16(blk, v);
             if (r >= 0) {
+                if (fz) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = blk * 16 + e;
-                    const float d = (j < r) ? gr - g_s[j] : -INFINITY;
-                    v[e] = br * v[e] * __expf(d);
+                    for (int m = 0; m < 4; ++m) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(cf_s + blk * 16 + 4 * m);
+                        const float cf[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const int e = 4 * m + e4;
+                            v[e] = (blk * 16 + e < r) ? v[e] * rf * cf[e4] : 0.f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = blk * 16 + e;
+                        const float d = (j < r) ? gr - g_s[j] : -INFINITY;
+                        v[e] = br * v[e] * __expf(d);
+                    }
                 }
                 if (blk == rb) {
 #pragma unroll
