@@ -140,12 +140,14 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(t[e]);
     };
 
-    // ---- G = k k^T (M = 64: row r in TMEM lane 32 (r / 16) + r % 16)
+    // ---- G = k k^T, issued as M = 128 so that row r lands in TMEM lane r: the A
+    // rows past the k tile are whatever follows it (their products are unused),
+    // and two full warps form L instead of four half-empty ones
     if (__syncthreads_or(fail)) goto done;
-    mma(64, s_k, s_k, false, K / 16);
+    mma(128, s_k, s_k, false, K / 16);
     if (__syncthreads_or(fail)) goto done;
-    {
-        const int r = lane < 16 ? warp * 16 + lane : -1, rb = r >> 4;
+    if (warp < 2) {
+        const int r = warp * 32 + lane, rb = r >> 4;
         const float gr = r >= 0 ? g_s[r] : 0.f, br = r >= 0 ? b_s[r] : 0.f;
         const float rf = br * __expf(gr - g_ref);
 #pragma unroll
