@@ -13,6 +13,10 @@ data path); the time is the max over ranks. Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (rank 0
 only), each step a bounded sample of the workload's (b, h) sequences.
+
+The line also carries "decode": the recurrent decode step timed on its own
+workload (256 sequences x 16 heads, one token, K = V = 128, bf16) against the
+HBM roofline of reading and writing the fp32 state once (--no-decode skips it).
 """
 from __future__ import annotations
 
@@ -31,7 +35,10 @@ sys.path.insert(0, str(ROOT))
 
 import torch  # noqa: E402
 
-from gated_delta_rule_35_gb300.inputs import BENCH_WORKLOAD, WORKLOADS, make_workload, to_f64  # noqa: E402
+from gated_delta_rule_35_gb300.inputs import (BENCH_WORKLOAD, DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
+                                              make_workload, to_f64)
+
+DECODE_WORKLOAD = "bf16_b256_h16_t1_k128_v128_decode"
 
 METRIC = "GDN chunked-fwd tokens/s on 1 GB300; % of roofline; vs CPU oracle"
 CHUNK = 64
@@ -80,6 +87,8 @@ KERNEL_MODEL = {
 }
 KERNEL_SOURCE = {
     "gdn_fused_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc.cu",
+    "gdn_wy_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc_wy.cu",
+    "gdn_decode_step_kernel": "gated_delta_rule_35_gb300/csrc/gdn_decode.cu",
     "wy_prepare_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
     "chunk_h_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
     "chunk_o_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",
@@ -348,6 +357,50 @@ def config_of(w, args):
             "parallelism": f"replica x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
+def bench_decode(args, world, dev):
+    """The decode step on its own workload: one token for each of B*H heads, the
+    state [B,H,K,V] fp32 read and written in place once per call. The state
+    (537 MB) is larger than L2, so no flush is needed between calls."""
+    from gated_delta_rule_35_gb300 import decode_step, native
+
+    w = DECODE_WORKLOADS[DECODE_WORKLOAD]
+    x = make_workload(w.name)
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    state = d.pop("h0")
+    o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kernels = native.decode_launches(native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype))
+    n = max(10, min(args.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+
+    def call():
+        decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, 1.0, out=o, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    for a, b in evs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n / 1e3, world, dev)
+    es = DSIZE[w.dtype]
+    heads = w.B * w.H
+    nbytes = heads * w.K * w.V * 4 * 2 + heads * w.T * ((2 * w.K + 2 * w.V) * es + 8)
+    peaks = load_peaks()
+    achieved = nbytes / t / 1e9
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
+            "calls_timed": n, "ms_per_call": 1e3 * t, "tokens_per_s": w.B * w.T * world / t,
+            "kernels": kernels, "gpu_launches": len(kernels) * n,
+            "l2": "not flushed: the 537 MB state exceeds L2",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": ncu_traffic(kernels[0], w.name) if kernels else None,
+                         "algorithmic_bytes_per_call": nbytes, "peak_source": peaks["_source"]}}
+
+
 def bench_ours(args, w, world, rank, local):
     from gated_delta_rule_35_gb300 import chunk_fwd, chunk_fwd_host, native
 
@@ -457,6 +510,8 @@ def bench_ours(args, w, world, rank, local):
     e2e = {"value": tokens_step * e2e_steps * world / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    dec = None if args.no_decode else bench_decode(args, world, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, w, args.cpu_seconds)
@@ -473,7 +528,7 @@ def bench_ours(args, w, world, rank, local):
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
             "kernels": kernels,
             "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
-            "clocks": clk, "wall_timed_s": wall,
+            "clocks": clk, "wall_timed_s": wall, "decode": dec,
         }
         print(json.dumps(line), flush=True)
 
@@ -487,6 +542,7 @@ def main():
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="target CPU time of the oracle baseline sample")
     args = ap.parse_args()

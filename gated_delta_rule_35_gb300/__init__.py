@@ -7,7 +7,7 @@ The compute runs in ``lib/libgdn.so`` (hand-written sm_103a kernels behind the
 C ABI of ``include/gdn.h``); this package only marshals arguments.
 """
 from .native import (GdnError, chunk_fwd, chunk_fwd_host, chunk_fwd_stages, check_device_status,
-                     problem, workspace_bytes)
+                     decode_step, problem, workspace_bytes)
 
 __all__ = ["GdnError", "chunk_fwd", "chunk_fwd_host", "chunk_fwd_stages", "check_device_status",
-           "problem", "workspace_bytes"]
+           "decode_step", "problem", "workspace_bytes"]

@@ -1,0 +1,260 @@
+// Recurrent (decode) step of the gated delta rule: gdn_decode_step of include/gdn.h.
+//
+// Per token (the row update of the "KdaSplit" decode kernel page, `update`,
+// with Gated DeltaNet's scalar decay alpha = exp(gamma)):
+//   S <- alpha S;  delta = beta (v - S^T k);  S += k delta^T;  o = scale S^T q.
+// Column j of S [K, V] evolves on its own: delta[j] needs only column j of S
+// (through (S^T k)[j]) and v[j]. So the work splits over (b, h, slice of VS
+// columns) with no exchange between CTAs (the page instead splits the state's
+// rows over a cluster and reduces across it). A CTA holds its [K, VS] slice in
+// registers for all of the call's tokens: the state is read once and written
+// once per call, which is the whole HBM cost at decode batch sizes.
+//
+// o is formed from the pre-update reads: S'^T q = alpha S^T q + delta (k . q),
+// so one pass over the state per token gives both S^T k and S^T q.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kRows = 8;   // state rows per thread
+constexpr int kCols = 4;   // state columns per thread (one float4)
+constexpr const char *kDecodeName = "gdn_decode_step_kernel";
+
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0];
+    const float4 b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32.
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float load1(const float *p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store1(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Thread (cg, rg) owns rows rg*8 .. rg*8+7 and columns cg*4 .. cg*4+3 of the
+// CTA's slice; cg = tid % (VS/4), so a warp's load of one of its rows covers
+// 32/(VS/4) whole rows of the slice (VS*4 contiguous bytes each).
+template <typename E, int K, int VS>
+__global__ void __launch_bounds__(K * VS / (kRows * kCols))
+gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E *__restrict__ v,
+                       const float *__restrict__ gamma, const float *__restrict__ beta,
+                       float scale, const float *state_in, float *state_out, E *__restrict__ o,
+                       int T, int H, int V) {
+    constexpr int CG = VS / kCols;            // column groups
+    constexpr int NT = CG * (K / kRows);      // threads
+    constexpr int NW = NT / 32;               // warps
+    static_assert(NT % 32 == 0 && NT <= 1024, "thread layout");
+    __shared__ float red_k[NW][VS], red_q[NW][VS], red_kq[NW];
+    __shared__ __align__(16) float delta_s[VS];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % CG, rg = tid / CG;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int col0 = blockIdx.x * VS;
+    const size_t bh = static_cast<size_t>(b) * H + h;
+    const size_t s_off = (bh * K + rg * kRows) * V + col0 + cg * kCols;
+
+    float S[kRows][kCols];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+        const float4 x = *reinterpret_cast<const float4 *>(state_in + s_off + size_t(i) * V);
+        S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+    }
+
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+        const size_t row = (static_cast<size_t>(b) * T + t) * H + h;   // token-head row
+        float kk[kRows], qq[kRows];
+        load8(k + row * K + rg * kRows, kk);
+        load8(q + row * K + rg * kRows, qq);
+        const float alpha = expf(gamma[row]);
+
+        // Partial S^T k, S^T q over this thread's rows, and k . q.
+        float pk[kCols], pq[kCols], kq = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) pk[c] = pq[c] = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            kq = fmaf(kk[i], qq[i], kq);
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                pk[c] = fmaf(S[i][c], kk[i], pk[c]);
+                pq[c] = fmaf(S[i][c], qq[i], pq[c]);
+            }
+        }
+        // Sum over the row groups of the warp (lanes that share cg).
+#pragma unroll
+        for (int off = CG; off < 32; off <<= 1) {
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], off);
+                pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], off);
+            }
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        }
+        if (lane < CG) {
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                red_k[warp][cg * kCols + c] = pk[c];
+                red_q[warp][cg * kCols + c] = pq[c];
+            }
+        }
+        if (lane == 0) red_kq[warp] = kq;
+        __syncthreads();
+
+        // One thread per column: delta and o.
+        if (tid < VS) {
+            float dk = 0.f, dq = 0.f, kqs = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                dk += red_k[w][tid];
+                dq += red_q[w][tid];
+                kqs += red_kq[w];
+            }
+            const size_t vo = row * V + col0 + tid;
+            const float d = beta[row] * (load1(v + vo) - alpha * dk);
+            delta_s[tid] = d;
+            store1(o + vo, scale * fmaf(d, kqs, alpha * dq));
+        }
+        __syncthreads();
+
+        // S = alpha S + k delta^T on this thread's block.
+        const float4 d4 = *reinterpret_cast<const float4 *>(&delta_s[cg * kCols]);
+        const float dd[kCols] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) S[i][c] = fmaf(kk[i], dd[c], alpha * S[i][c]);
+        // The next token's writes to red_* and delta_s follow this token's
+        // second barrier and its own first barrier, after every read above.
+    }
+
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+        *reinterpret_cast<float4 *>(state_out + s_off + size_t(i) * V) =
+            make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_decode(const gdn_problem *p) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->K <= 0 || p->V <= 0) return GDN_ERR_INVALID_ARG;
+    if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
+        return GDN_ERR_INVALID_ARG;
+    if (p->algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
+    if (p->K % 64 != 0 || p->K > 256) return GDN_ERR_UNSUPPORTED;
+    if (p->V % 16 != 0 || p->V > 4096) return GDN_ERR_UNSUPPORTED;
+    if (p->H > 65535 || p->B > 65535) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+// Columns per CTA: the widest slice (fewest, largest loads per row) that
+// still gives at least two CTAs per SM; narrower slices only add CTAs.
+int pick_vs(const gdn_problem *p, int sms) {
+    const long long heads = static_cast<long long>(p->B) * p->H;
+    for (int vs : {64, 32}) {
+        if (p->V % vs == 0 && heads * (p->V / vs) >= 2LL * sms) return vs;
+    }
+    return 16;
+}
+
+template <typename E, int K, int VS>
+cudaError_t launch(const gdn_problem *p, const void *q, const void *k, const void *v,
+                   const float *gamma, const float *beta, float scale, const float *state_in,
+                   float *state_out, void *o, cudaStream_t s) {
+    constexpr int threads = K * VS / (kRows * kCols);
+    const dim3 grid(p->V / VS, p->H, p->B);
+    gdn_decode_step_kernel<E, K, VS><<<grid, threads, 0, s>>>(
+        static_cast<const E *>(q), static_cast<const E *>(k), static_cast<const E *>(v), gamma,
+        beta, scale, state_in, state_out, static_cast<E *>(o), p->T, p->H, p->V);
+    return cudaGetLastError();
+}
+
+template <typename E, int K>
+cudaError_t dispatch_vs(int vs, const gdn_problem *p, const void *q, const void *k, const void *v,
+                        const float *gamma, const float *beta, float scale,
+                        const float *state_in, float *state_out, void *o, cudaStream_t s) {
+    if (vs == 64) return launch<E, K, 64>(p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    if (vs == 32) return launch<E, K, 32>(p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    return launch<E, K, 16>(p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+}
+
+template <typename E>
+cudaError_t dispatch_k(int vs, const gdn_problem *p, const void *q, const void *k, const void *v,
+                       const float *gamma, const float *beta, float scale,
+                       const float *state_in, float *state_out, void *o, cudaStream_t s) {
+    if (p->K == 64)
+        return dispatch_vs<E, 64>(vs, p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    if (p->K == 128)
+        return dispatch_vs<E, 128>(vs, p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    if (p->K == 192)
+        return dispatch_vs<E, 192>(vs, p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    return dispatch_vs<E, 256>(vs, p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+GDN_API gdn_status gdn_decode_step(const gdn_problem *p, const void *q, const void *k,
+                                   const void *v, const float *gamma, const float *beta,
+                                   float scale, const float *state_in, float *state_out, void *o,
+                                   void *stream) {
+    const gdn_status st = gdn::check_decode(p);
+    if (st != GDN_OK) return st;
+    if (!state_in || !state_out) return GDN_ERR_INVALID_ARG;
+    const bool empty = p->T == 0;
+    if (!empty && (!q || !k || !v || !gamma || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, gamma, beta, state_in, state_out, o};
+    for (const void *ptr : ptrs)
+        if (ptr && !gdn::aligned16(ptr)) return GDN_ERR_ALIGNMENT;
+    const size_t state_bytes =
+        static_cast<size_t>(p->B) * p->H * p->K * p->V * sizeof(float);
+    const char *si = reinterpret_cast<const char *>(state_in);
+    const char *so = reinterpret_cast<const char *>(state_out);
+    if (si != so && si < so + state_bytes && so < si + state_bytes) return GDN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (empty) {
+        if (si != so)
+            e = cudaMemcpyAsync(state_out, state_in, state_bytes, cudaMemcpyDeviceToDevice, s);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int vs = gdn::pick_vs(p, sms);
+    if (p->dtype == GDN_BF16)
+        e = gdn::dispatch_k<__nv_bfloat16>(vs, p, q, k, v, gamma, beta, scale, state_in,
+                                           state_out, o, s);
+    else
+        e = gdn::dispatch_k<float>(vs, p, q, k, v, gamma, beta, scale, state_in, state_out, o, s);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+GDN_API int32_t gdn_decode_step_launches(const gdn_problem *p, const char **names,
+                                         int32_t max_names) {
+    if (gdn::check_decode(p) != GDN_OK || p->T == 0) return 0;
+    if (names && max_names > 0) names[0] = gdn::kDecodeName;
+    return 1;
+}
+
+}  // extern "C"

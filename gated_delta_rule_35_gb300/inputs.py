@@ -10,7 +10,8 @@ Recipe (one ``torch.Generator('cpu')`` per workload, drawn in this order):
   q, k are L2-normalised over K per (b,t,h) in fp32 (no epsilon); q is then
   multiplied by K**-0.5; beta = sigmoid(beta_raw + beta_mean);
   per-token log-decay = logsigmoid(g_raw + g_mean) / g_div;
-  g = cumulative sum of the per-token log-decay *within each 64-token chunk*;
+  g = cumulative sum of the per-token log-decay *within each 64-token chunk*
+  (``chunk=1`` leaves the per-token log-decay itself, the decode step's gamma);
   h0 = h0_std * h0_raw. q, k, v are then cast to the compute dtype; g, beta and
   h0 stay fp32.
 
@@ -18,6 +19,10 @@ Five named workloads: a small fp32 case (one 256-token head, K=V=64), and
 four bf16 cases with K=128: a short batch, a long prefill with a non-zero
 initial state, a wide batch, and a V=256 case with near-zero decay and large
 beta. The chunk size is C=64 throughout ("WarpDrive" page, section "Pipeline").
+
+One decode workload (``DECODE_WORKLOADS``): 256 sequences x 16 heads advanced by
+one token each, K = V = 128, bf16, from a state of std 0.1 (a prefill's h_final
+stands there in use); its gamma is the per-token log-decay (``chunk=1``).
 """
 from __future__ import annotations
 
@@ -65,6 +70,13 @@ WORKLOADS = {
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)
+DECODE_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("bf16_b256_h16_t1_k128_v128_decode", 256, 1, 16, 128, 128, "bf16", seed=11,
+                 h0_std=0.1),
+    ]
+}
 BENCH_WORKLOAD = "bf16_b4_h16_t2048_k128_v128"
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -81,8 +93,9 @@ def chunk_local_cumsum(x: torch.Tensor, chunk: int = CHUNK) -> torch.Tensor:
 
 def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", seed: int = 0,
                 h0_std: float = 0.0, g_mean: float = 0.0, g_div: float = 16.0,
-                beta_mean: float = 0.0) -> dict:
-    """Return CPU tensors q,k,v (dtype), g, beta (fp32) and h0 (fp32 or None)."""
+                beta_mean: float = 0.0, chunk: int = CHUNK) -> dict:
+    """Return CPU tensors q,k,v (dtype), g, beta (fp32) and h0 (fp32 or None).
+    g is the per-token log-decay summed within chunks of ``chunk`` tokens."""
     gen = torch.Generator("cpu").manual_seed(seed)
     q = torch.randn(B, T, H, K, generator=gen)
     k = torch.randn(B, T, H, K, generator=gen)
@@ -95,7 +108,7 @@ def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", 
     q = q / q.norm(dim=-1, keepdim=True) * (K ** -0.5)
     k = k / k.norm(dim=-1, keepdim=True)
     beta = torch.sigmoid(beta_raw + beta_mean)
-    g = chunk_local_cumsum(F.logsigmoid(g_raw + g_mean) / g_div)
+    g = chunk_local_cumsum(F.logsigmoid(g_raw + g_mean) / g_div, chunk)
     td = TORCH_DTYPE[dtype]
     return {
         "q": q.to(td).contiguous(),
@@ -110,12 +123,12 @@ def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", 
 
 def make_workload(name: str, **overrides) -> dict:
     """Inputs of a named workload; ``overrides`` may change B/T/H (e.g. a sample)."""
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if name in WORKLOADS else DECODE_WORKLOADS[name]
     p = w.as_dict()
     p.update(overrides)
     return make_inputs(p["B"], p["T"], p["H"], p["K"], p["V"], dtype=p["dtype"], seed=p["seed"],
                        h0_std=p["h0_std"], g_mean=p["g_mean"], g_div=p["g_div"],
-                       beta_mean=p["beta_mean"])
+                       beta_mean=p["beta_mean"], chunk=1 if name in DECODE_WORKLOADS else CHUNK)
 
 
 def to_f64(t):

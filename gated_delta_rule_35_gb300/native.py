@@ -23,7 +23,8 @@ CHUNK = 64
 # Every function include/gdn.h declares.
 EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stages",
            "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
-           "gdn_chunk_fwd_noalloc", "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_noalloc", "gdn_decode_step", "gdn_decode_step_launches",
+           "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -70,6 +71,11 @@ def lib():
                                                         ctypes.c_int32, vp]
         L.gdn_check_device_status.restype = ctypes.c_int
         L.gdn_check_device_status.argtypes = [vp, vp]
+        L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+        L.gdn_decode_step_launches.restype = ctypes.c_int32
+        L.gdn_decode_step_launches.argtypes = [pp, ctypes.POINTER(ctypes.c_char_p),
+                                               ctypes.c_int32]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_version.restype = ctypes.c_uint32
@@ -188,6 +194,53 @@ def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = 
         raise GdnError(st, "gdn_chunk_fwd_stages")
     st_bufs.update(o=o, h_final=hf)
     return st_bufs
+
+
+def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None, out=None,
+                stream=None):
+    """Recurrent step(s) of the rule on CUDA tensors: advances every sequence by
+    its T tokens and returns (o, state_out).
+
+    q, k [B,T,H,K] and v [B,T,H,V] (float32 or bfloat16); gamma, beta [B,T,H]
+    float32, gamma the per-token log decay itself (not a cumulative sum);
+    state [B,H,K,V] float32 (an h_final of chunk_fwd). ``state_out=None``
+    updates ``state`` in place; pass ``state_out=state`` for the same, or
+    another buffer to keep ``state``."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
+    if gamma.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("gamma and beta must be float32")
+    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or gamma.shape != (B, T, H) \
+            or beta.shape != (B, T, H):
+        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], gamma, beta [B,T,H]")
+    so = state if state_out is None else state_out
+    for st in (state, so):
+        if st.shape != (B, H, K, V) or st.dtype != torch.float32:
+            raise ValueError("state must be float32 [B,H,K,V]")
+    for t in (q, k, v, gamma, beta, state, so):
+        if not t.is_contiguous() or t.device != dev:
+            raise ValueError("all tensors must be contiguous and on the same device")
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
+    p = problem(B, T, H, K, V, q.dtype, "auto")
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = lib().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                               _ptr(beta), float(scale), _ptr(state), _ptr(so), _ptr(o),
+                               ctypes.c_void_p(s.cuda_stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode_step")
+    return o, so
+
+
+def decode_launches(p: Problem) -> list[str]:
+    """Names of the kernels one decode_step call launches."""
+    names = (ctypes.c_char_p * 1)()
+    n = int(lib().gdn_decode_step_launches(ctypes.byref(p), names, 1))
+    return [names[i].decode() for i in range(n)]
 
 
 def check_device_status(workspace, stream=None) -> int:

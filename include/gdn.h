@@ -167,6 +167,46 @@ GDN_API gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p,
                                          const float *h0, void *o, float *h_final,
                                          void *stream);
 
+/* One or a few tokens of the recurrent (decode) form of the same rule, for
+ * generation after a prefill: for every batch b and head h, token by token,
+ *
+ *   S <- exp(gamma_t) S;   delta_t = beta_t (v_t - S^T k_t);   S += k_t delta_t^T;
+ *   o_t = scale S^T q_t
+ *
+ * i.e. the state is decayed first, then read at k_t, written, and read at q_t
+ * (the order of the delta-rule row update of the "KdaSplit" decode kernel page,
+ * its `update` step, with the scalar per-head decay of Gated DeltaNet). Tokens
+ * after the first of a call see the state left by the one before.
+ *
+ *  - p->T >= 0 tokens per sequence (1 for plain decode; a few for multi-token
+ *    verification); every sequence of the batch advances by the same T.
+ *    T = 0 copies state_in to state_out (nothing when they are the same).
+ *  - q, k [B,T,H,K] and v, o [B,T,H,V] in p->dtype; gamma, beta [B,T,H] fp32.
+ *    gamma is the per-token log decay log(alpha_t) <= 0 itself, NOT the
+ *    chunk-local cumulative sum gdn_chunk_fwd takes (for T = 1 the two agree).
+ *  - state_in, state_out [B,H,K,V] fp32, in the layout of h0 / h_final, so a
+ *    prefill's h_final is a decode's state_in. They may be the same pointer
+ *    (update in place) or non-overlapping buffers; partial overlap is
+ *    undefined. state_in is required (a zero state is a zeroed buffer).
+ *  - Limits: K a multiple of 64 up to 256; V a multiple of 16 up to 4096;
+ *    p->algo GDN_ALGO_AUTO or GDN_ALGO_SIMT (the step is a matrix-vector
+ *    product with no tensor-core form; GDN_ALGO_TC gives GDN_ERR_UNSUPPORTED).
+ *  - No workspace; nothing is allocated. For long T the chunked forward is
+ *    the faster route to the same result.
+ * Pointer, alignment, stream and error conventions are those above. */
+GDN_API gdn_status gdn_decode_step(const gdn_problem *p,
+                                   const void *q, const void *k, const void *v,
+                                   const float *gamma, const float *beta, float scale,
+                                   const float *state_in, float *state_out, void *o,
+                                   void *stream);
+
+/* Number of kernels one gdn_decode_step call on this problem launches: 1 for
+ * T >= 1, 0 for T = 0 (the state copy is a cudaMemcpyAsync) or an invalid
+ * problem. names[0] receives the kernel's static name when names != NULL,
+ * max_names > 0 and the count is 1. */
+GDN_API int32_t gdn_decode_step_launches(const gdn_problem *p, const char **names,
+                                         int32_t max_names);
+
 /* Static description of a status code. Never NULL. */
 GDN_API const char *gdn_status_string(gdn_status s);
 

@@ -129,6 +129,24 @@ def pin_product_form(fwd):
     assert rel(hf, hf_x) < 1e-12, f"product form h_final: {rel(hf, hf_x)}"
 
 
+def pin_product_form_per_token(fwd):
+    """Chunks of one token: g is then each token's own log-decay (the form the
+    decode step takes). Random fp64 inputs against the product form, T=5."""
+    rng = np.random.default_rng(13)
+    B, T, H, K, V = 2, 5, 3, 4, 3
+    q = rng.standard_normal((B, T, H, K))
+    k = rng.standard_normal((B, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, V))
+    h0 = rng.standard_normal((B, H, K, V))
+    log_alpha = -rng.uniform(0.0, 2.0, (B, T, H))
+    beta = rng.uniform(0.1, 1.0, (B, T, H))
+    o_x, hf_x = product_form(q, k, v, np.exp(log_alpha), beta, 1.3, h0)
+    o, hf = fwd(q, k, v, log_alpha, beta, 1.3, h0, 1)
+    assert rel(o, o_x) < 1e-12, f"per-token product form o: {rel(o, o_x)}"
+    assert rel(hf, hf_x) < 1e-12, f"per-token product form h_final: {rel(hf, hf_x)}"
+
+
 # ---------------------------------------------------------------- closed forms
 def pin_beta_zero(fwd):
     """beta = 0: no writes, so S_t = exp(G_t) h0 with G_t the running sum of the
@@ -250,5 +268,5 @@ def pin_causal_and_independent(fwd):
     assert np.array_equal(hf3, hf[:, perm]), "head independence h_final"
 
 
-ALL_PINS = [pin_rational, pin_product_form, pin_beta_zero, pin_orthonormal_retrieval,
+ALL_PINS = [pin_rational, pin_product_form, pin_product_form_per_token, pin_beta_zero, pin_orthonormal_retrieval,
             pin_overwrite, pin_forget_reset, pin_split_resume, pin_causal_and_independent]

@@ -97,3 +97,41 @@ def test_stage_export_needs_exports():
                                            None, None)
     assert st == native.GDN_ERR_INVALID_ARG
     assert native.lib().gdn_check_device_status(None, None) == native.GDN_ERR_INVALID_ARG
+
+
+def _decode(p, q=FAKE, k=FAKE, v=FAKE, gamma=FAKE, beta=FAKE, s_in=FAKE, s_out=FAKE, o=FAKE):
+    vp = ctypes.c_void_p
+    return native.lib().gdn_decode_step(ctypes.byref(p) if p is not None else None, vp(q),
+                                        vp(k), vp(v), vp(gamma), vp(beta), 1.0, vp(s_in),
+                                        vp(s_out), vp(o), None)
+
+
+@pytest.mark.parametrize("shape,algo,status", [
+    ((0, 1, 1, 64, 64), "auto", native.GDN_ERR_INVALID_ARG),
+    ((1, -1, 1, 64, 64), "auto", native.GDN_ERR_INVALID_ARG),
+    ((1, 1, 1, 96, 64), "auto", native.GDN_ERR_UNSUPPORTED),    # K not a multiple of 64
+    ((1, 1, 1, 320, 64), "auto", native.GDN_ERR_UNSUPPORTED),   # K > 256
+    ((1, 1, 1, 64, 24), "auto", native.GDN_ERR_UNSUPPORTED),    # V not a multiple of 16
+    ((1, 1, 1, 64, 8192), "auto", native.GDN_ERR_UNSUPPORTED),  # V > 4096
+    ((1, 1, 1, 64, 64), "tc", native.GDN_ERR_UNSUPPORTED),      # no tensor-core decode
+])
+def test_decode_rejects_bad_problems(shape, algo, status):
+    assert _decode(native.problem(*shape, native.GDN_BF16, algo)) == status
+
+
+def test_decode_rejects_null_misaligned_and_overlapping():
+    p = native.problem(2, 1, 3, 128, 128, native.GDN_BF16, "auto")
+    assert _decode(None) == native.GDN_ERR_INVALID_ARG
+    for field in ("q", "k", "v", "gamma", "beta", "s_in", "s_out", "o"):
+        assert _decode(p, **{field: None}) == native.GDN_ERR_INVALID_ARG, field
+        assert _decode(p, **{field: FAKE + 4}) == native.GDN_ERR_ALIGNMENT, field
+    # the state is 2*3*128*128*4 bytes; an output starting inside it overlaps
+    assert _decode(p, s_out=FAKE + 4096) == native.GDN_ERR_INVALID_ARG
+    assert _decode(p, s_in=FAKE + 4096) == native.GDN_ERR_INVALID_ARG
+
+
+def test_decode_launches():
+    assert native.decode_launches(native.problem(4, 1, 16, 128, 128, native.GDN_BF16)) == \
+        ["gdn_decode_step_kernel"]
+    assert native.decode_launches(native.problem(4, 0, 16, 128, 128, native.GDN_BF16)) == []
+    assert native.decode_launches(native.problem(4, 1, 16, 96, 128, native.GDN_BF16)) == []

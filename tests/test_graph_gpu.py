@@ -1,0 +1,72 @@
+"""Both product calls are capturable in a CUDA graph: neither allocates, syncs
+or reads device memory on the host, so a serving loop can replay them without
+launch overhead. The replayed graph must give exactly what eager calls give."""
+import pytest
+import torch
+
+from gated_delta_rule_35_gb300 import chunk_fwd, decode_step, native
+from gated_delta_rule_35_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu(x):
+    return {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+
+
+def test_decode_steps_replay_from_a_graph():
+    B, T, H, K, V = 8, 4, 16, 128, 128
+    x = gpu(make_inputs(B, T, H, K, V, dtype="bf16", seed=51, h0_std=0.1, chunk=1))
+    tok = [{n: x[n][:, t:t + 1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+           for t in range(T)]
+    outs = [torch.empty(B, 1, H, V, dtype=torch.bfloat16, device="cuda") for _ in range(T)]
+
+    eager_state = x["h0"].clone()
+    eager = []
+    for t in range(T):
+        o, _ = decode_step(tok[t]["q"], tok[t]["k"], tok[t]["v"], tok[t]["g"], tok[t]["beta"],
+                           eager_state)
+        eager.append(o)
+
+    state = x["h0"].clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up outside capture
+        decode_step(tok[0]["q"], tok[0]["k"], tok[0]["v"], tok[0]["g"], tok[0]["beta"],
+                    state.clone(), out=outs[0])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(T):
+            decode_step(tok[t]["q"], tok[t]["k"], tok[t]["v"], tok[t]["g"], tok[t]["beta"],
+                        state, out=outs[t])
+    g.replay()
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert torch.equal(outs[t], eager[t]), t
+    assert torch.equal(state, eager_state)
+
+
+@pytest.mark.parametrize("algo", ["simt", "tc"])
+def test_chunk_fwd_replays_from_a_graph(algo):
+    B, T, H, K, V = 2, 200, 4, 128, 128
+    p = native.problem(B, T, H, K, V, torch.bfloat16, algo)
+    if native.workspace_bytes(p) == 0:
+        pytest.skip(f"{algo} not built")
+    x = gpu(make_inputs(B, T, H, K, V, dtype="bf16", seed=52, h0_std=0.1))
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, x["h0"])
+    o_e, hf_e = chunk_fwd(*args, algo=algo)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(o_e)
+    hf = torch.empty_like(hf_e)
+    chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf)   # warm-up
+    torch.cuda.synchronize()
+    o.fill_(float("nan"))
+    hf.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(hf, hf_e)
