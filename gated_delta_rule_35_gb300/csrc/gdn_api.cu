@@ -15,6 +15,8 @@ gdn_status check_problem(const gdn_problem *p) {
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
+    if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+    if (p->flags != 0) return GDN_ERR_UNSUPPORTED;   // front-end not built yet
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
     if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
     // Every index is computed in 64 bits; B*T*H rows must still fit a grid.

@@ -158,6 +158,8 @@ gdn_status check_decode(const gdn_problem *p) {
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
+    if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+    if (p->flags & GDN_FLAG_QK_L2NORM) return GDN_ERR_UNSUPPORTED;   // not built yet
     if (p->algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
     if (p->K % 64 != 0 || p->K > 256) return GDN_ERR_UNSUPPORTED;
     if (p->V % 16 != 0 || p->V > 4096) return GDN_ERR_UNSUPPORTED;

@@ -12,6 +12,8 @@ Recipe (one ``torch.Generator('cpu')`` per workload, drawn in this order):
   per-token log-decay = logsigmoid(g_raw + g_mean) / g_div;
   g = cumulative sum of the per-token log-decay *within each 64-token chunk*
   (``chunk=1`` leaves the per-token log-decay itself, the decode step's gamma);
+  with ``raw=True`` q and k are left unnormalised (and q unscaled) and g is
+  the per-token log-decay itself: the inputs of the in-kernel front-end;
   h0 = h0_std * h0_raw. q, k, v are then cast to the compute dtype; g, beta and
   h0 stay fp32.
 
@@ -93,9 +95,10 @@ def chunk_local_cumsum(x: torch.Tensor, chunk: int = CHUNK) -> torch.Tensor:
 
 def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", seed: int = 0,
                 h0_std: float = 0.0, g_mean: float = 0.0, g_div: float = 16.0,
-                beta_mean: float = 0.0, chunk: int = CHUNK) -> dict:
+                beta_mean: float = 0.0, chunk: int = CHUNK, raw: bool = False) -> dict:
     """Return CPU tensors q,k,v (dtype), g, beta (fp32) and h0 (fp32 or None).
-    g is the per-token log-decay summed within chunks of ``chunk`` tokens."""
+    g is the per-token log-decay summed within chunks of ``chunk`` tokens;
+    ``raw`` skips the q/k normalisation and the sum (same draws)."""
     gen = torch.Generator("cpu").manual_seed(seed)
     q = torch.randn(B, T, H, K, generator=gen)
     k = torch.randn(B, T, H, K, generator=gen)
@@ -105,10 +108,13 @@ def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", 
     h0 = None
     if h0_std > 0:
         h0 = torch.randn(B, H, K, V, generator=gen) * h0_std
-    q = q / q.norm(dim=-1, keepdim=True) * (K ** -0.5)
-    k = k / k.norm(dim=-1, keepdim=True)
+    if not raw:
+        q = q / q.norm(dim=-1, keepdim=True) * (K ** -0.5)
+        k = k / k.norm(dim=-1, keepdim=True)
     beta = torch.sigmoid(beta_raw + beta_mean)
-    g = chunk_local_cumsum(F.logsigmoid(g_raw + g_mean) / g_div, chunk)
+    g = F.logsigmoid(g_raw + g_mean) / g_div
+    if not raw:
+        g = chunk_local_cumsum(g, chunk)
     td = TORCH_DTYPE[dtype]
     return {
         "q": q.to(td).contiguous(),

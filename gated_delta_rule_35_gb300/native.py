@@ -16,6 +16,7 @@ LIB_PATH = Path(__file__).resolve().parent / "lib" / "libgdn.so"
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGNMENT = 0, 1, 2, 3
 GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 GDN_F32, GDN_BF16 = 0, 1
+GDN_FLAG_RAW_G, GDN_FLAG_QK_L2NORM = 1, 2
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
 CHUNK = 64
@@ -36,7 +37,7 @@ class GdnError(RuntimeError):
 class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("algo", ctypes.c_int32)]
+                ("algo", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class StageExports(ctypes.Structure):
@@ -88,9 +89,14 @@ def status_string(s: int) -> str:
     return lib().gdn_status_string(int(s)).decode()
 
 
-def problem(B, T, H, K, V, dtype, algo="auto") -> Problem:
+def flags_of(raw_g: bool = False, qk_l2norm: bool = False) -> int:
+    return (GDN_FLAG_RAW_G if raw_g else 0) | (GDN_FLAG_QK_L2NORM if qk_l2norm else 0)
+
+
+def problem(B, T, H, K, V, dtype, algo="auto", flags: int = 0) -> Problem:
     d = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return Problem(int(B), int(T), int(H), int(K), int(V), d, ALGOS[algo] if isinstance(algo, str) else int(algo))
+    return Problem(int(B), int(T), int(H), int(K), int(V), d,
+                   ALGOS[algo] if isinstance(algo, str) else int(algo), int(flags))
 
 
 def workspace_bytes(p: Problem) -> int:

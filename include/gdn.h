@@ -28,8 +28,9 @@
  *  - Layouts: q, k [B,T,H,K]; v, o [B,T,H,V]; g, beta [B,T,H] fp32;
  *    h0, h_final [B,H,K,V] fp32.
  *  - g is the per-token log-decay summed cumulatively *within each 64-token
- *    chunk* (restarting at t = 0, 64, 128, ...). Values should be <= 0 and
- *    non-increasing inside a chunk; exp(g_i - g_j) is only evaluated for i >= j.
+ *    chunk* (restarting at t = 0, 64, 128, ...), unless the problem's flags
+ *    hold GDN_FLAG_RAW_G (below). Values should be <= 0 and non-increasing
+ *    inside a chunk; exp(g_i - g_j) is only evaluated for i >= j.
  *  - T need not be a multiple of 64: the last chunk is partial and g_last is
  *    the g of its last valid token. T = 0 is valid: h_final = h0 (or zeros).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -71,12 +72,33 @@ typedef enum {
     GDN_ALGO_TC = 2      /* tensor-core (tcgen05/TMEM, TMA) path, bf16 only */
 } gdn_algo;
 
+/* Input front-end options (gdn_problem.flags), a bit set; 0 = inputs as
+ * described above. Both steps sit before the WY build: they are the
+ * normalisation and gate steps that a Gated DeltaNet layer applies to its
+ * projections ("KdaSplit" decode kernel page, its q/k normalisation), done
+ * inside the kernels so that no separate pass over q, k or g is needed.
+ *  - GDN_FLAG_RAW_G: g holds the per-token log decays gamma_t themselves;
+ *    the chunk-local cumulative sum is taken in the kernels (restarting at
+ *    t = 0, 64, 128, ...). Without it g is that cumulative sum already.
+ *  - GDN_FLAG_QK_L2NORM: every q and k row (one token of one head, K values)
+ *    is replaced by x / sqrt(sum_i x_i^2 + 1e-6) before use; scale still
+ *    multiplies o, i.e. it scales the normalised q. The normalised rows are
+ *    never rounded back to the input dtype.
+ * gdn_decode_step always takes raw gamma and accepts either g flag; it
+ * honours GDN_FLAG_QK_L2NORM. */
+enum {
+    GDN_FLAG_RAW_G = 1,
+    GDN_FLAG_QK_L2NORM = 2
+};
+
 /* Problem description. K in {64, 128}; V a multiple of 64 in [64, 256];
- * dtype is the element type of q, k, v and o. */
+ * dtype is the element type of q, k, v and o; flags a set of GDN_FLAG_*
+ * (unknown bits give GDN_ERR_INVALID_ARG). */
 typedef struct {
     int32_t B, T, H, K, V;
     int32_t dtype;   /* gdn_dtype */
     int32_t algo;    /* gdn_algo */
+    int32_t flags;   /* GDN_FLAG_* bits */
 } gdn_problem;
 
 /* Bytes of device workspace gdn_chunk_fwd needs for this problem (0 if the
