@@ -16,7 +16,9 @@ only), each step a bounded sample of the workload's (b, h) sequences.
 
 The line also carries "decode": the recurrent decode step timed on its own
 workload (256 sequences x 16 heads, one token, K = V = 128, bf16) against the
-HBM roofline of reading and writing the fp32 state once (--no-decode skips it).
+HBM roofline of reading and writing the fp32 state once (--no-decode skips it);
+and "frontend": the same step on raw inputs with the chunk-local cumsum of g
+and the q/k L2 norm done in the kernels (--no-frontend skips it).
 """
 from __future__ import annotations
 
@@ -36,7 +38,7 @@ sys.path.insert(0, str(ROOT))
 import torch  # noqa: E402
 
 from gated_delta_rule_35_gb300.inputs import (BENCH_WORKLOAD, DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
-                                              make_workload, to_f64)
+                                              make_inputs, make_workload, to_f64)
 
 DECODE_WORKLOAD = "bf16_b256_h16_t1_k128_v128_decode"
 
@@ -357,6 +359,47 @@ def config_of(w, args):
             "parallelism": f"replica x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
+def bench_frontend(args, w, world, dev, flush):
+    """The same workload with the input front-end in the kernels: q and k as
+    drawn (unnormalised), g the raw per-token log decays, flags RAW_G and
+    QK_L2NORM, scale K^-0.5. Timed like the main step (L2 flushed before each
+    step, CUDA events on the launching stream)."""
+    from gated_delta_rule_35_gb300 import chunk_fwd, native
+
+    x = make_inputs(w.B, w.T, w.H, w.K, w.V, dtype=w.dtype, seed=w.seed, h0_std=w.h0_std,
+                    g_mean=w.g_mean, g_div=w.g_div, beta_mean=w.beta_mean, raw=True)
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    flags = native.flags_of(True, True)
+    p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, args.algo, flags)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
+    hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(10, min(args.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+
+    def step():
+        chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], w.K ** -0.5, d["h0"], algo=args.algo,
+                  workspace=ws, out=o, final_state=hf, stream=stream, raw_g=True, qk_l2norm=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n / 1e3, world, dev)
+    return {"workload": w.name + "_raw", "flags": ["RAW_G", "QK_L2NORM"], "steps_timed": n,
+            "ms_per_step": 1e3 * t, "tokens_per_s": w.B * w.T * world / t,
+            "kernels": native.launches(p), "gpu_launches": len(native.launches(p)) * n,
+            "inputs": "q, k unnormalised N(0,1); g per-token log decays; scale K^-0.5"}
+
+
 def bench_decode(args, world, dev):
     """The decode step on its own workload: one token for each of B*H heads, the
     state [B,H,K,V] fp32 read and written in place once per call. The state
@@ -511,6 +554,7 @@ def bench_ours(args, w, world, rank, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     dec = None if args.no_decode else bench_decode(args, world, dev)
+    fe = None if args.no_frontend else bench_frontend(args, w, world, dev, flush)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -528,7 +572,7 @@ def bench_ours(args, w, world, rank, local):
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
             "kernels": kernels,
             "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
-            "clocks": clk, "wall_timed_s": wall, "decode": dec,
+            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe,
         }
         print(json.dumps(line), flush=True)
 
@@ -543,6 +587,8 @@ def main():
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-frontend", action="store_true",
+                    help="skip the in-kernel front-end measurement")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="target CPU time of the oracle baseline sample")
     args = ap.parse_args()

@@ -16,7 +16,6 @@ gdn_status check_problem(const gdn_problem *p) {
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
-    if (p->flags != 0) return GDN_ERR_UNSUPPORTED;   // front-end not built yet
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
     if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
     // Every index is computed in 64 bits; B*T*H rows must still fit a grid.
@@ -33,10 +32,16 @@ gdn_algo resolve_algo(const gdn_problem *p) {
                                                                        : GDN_ALGO_SIMT;
 }
 
+// Front-end region: g_cum and rk, one fp32 per token-head each.
+size_t front_bytes(const gdn_problem *p) {
+    return 2 * align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
+}
+
 size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
     if (p->T == 0) return 0;
-    if (algo == GDN_ALGO_TC) return tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
-    return simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+    const size_t front = front_bytes(p);
+    if (algo == GDN_ALGO_TC) return front + tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+    return front + simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
 }
 
 gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
@@ -65,7 +70,12 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale; a.h0 = h0;
     a.o = o; a.h_final = h_final;
     a.status = static_cast<uint32_t *>(workspace);
-    void *body = static_cast<char *>(workspace) + kStatusBytes;
+    a.flags = p->flags;
+    char *front = static_cast<char *>(workspace) + kStatusBytes;
+    const size_t plane = align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
+    a.g_cum = reinterpret_cast<float *>(front);
+    a.rk = reinterpret_cast<float *>(front + plane);
+    void *body = empty ? front : front + front_bytes(p);
 
     cudaError_t e;
     if (empty) {

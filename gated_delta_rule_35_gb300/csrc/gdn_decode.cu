@@ -12,6 +12,11 @@
 //
 // o is formed from the pre-update reads: S'^T q = alpha S^T q + delta (k . q),
 // so one pass over the state per token gives both S^T k and S^T q.
+//
+// With the front-end norm (GDN_FLAG_QK_L2NORM) the same pass also sums |k|^2
+// and |q|^2; with rk, rq their factors 1 / sqrt(sum + eps), the normalised
+// rows enter as S^T k^ = rk S^T k, k^ . q^ = rk rq (k . q) and
+// S += k (rk delta)^T, so the rows themselves are never rescaled.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -49,7 +54,7 @@ __device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float
 // Thread (cg, rg) owns rows rg*8 .. rg*8+7 and columns cg*4 .. cg*4+3 of the
 // CTA's slice; cg = tid % (VS/4), so a warp's load of one of its rows covers
 // 32/(VS/4) whole rows of the slice (VS*4 contiguous bytes each).
-template <typename E, int K, int VS>
+template <typename E, int K, int VS, bool NORM>
 __global__ void __launch_bounds__(K * VS / (kRows * kCols))
 gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E *__restrict__ v,
                        const float *__restrict__ gamma, const float *__restrict__ beta,
@@ -59,7 +64,7 @@ gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E
     constexpr int NT = CG * (K / kRows);      // threads
     constexpr int NW = NT / 32;               // warps
     static_assert(NT % 32 == 0 && NT <= 1024, "thread layout");
-    __shared__ float red_k[NW][VS], red_q[NW][VS], red_kq[NW];
+    __shared__ float red_k[NW][VS], red_q[NW][VS], red_kq[NW], red_kk[NW], red_qq[NW];
     __shared__ __align__(16) float delta_s[VS];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -85,12 +90,16 @@ gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E
         const float alpha = expf(gamma[row]);
 
         // Partial S^T k, S^T q over this thread's rows, and k . q.
-        float pk[kCols], pq[kCols], kq = 0.f;
+        float pk[kCols], pq[kCols], kq = 0.f, k2 = 0.f, q2 = 0.f;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) pk[c] = pq[c] = 0.f;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             kq = fmaf(kk[i], qq[i], kq);
+            if (NORM) {
+                k2 = fmaf(kk[i], kk[i], k2);
+                q2 = fmaf(qq[i], qq[i], q2);
+            }
 #pragma unroll
             for (int c = 0; c < kCols; ++c) {
                 pk[c] = fmaf(S[i][c], kk[i], pk[c]);
@@ -106,6 +115,10 @@ gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E
                 pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], off);
             }
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if (NORM) {
+                k2 += __shfl_xor_sync(0xffffffffu, k2, off);
+                q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+            }
         }
         if (lane < CG) {
 #pragma unroll
@@ -114,22 +127,39 @@ gdn_decode_step_kernel(const E *__restrict__ q, const E *__restrict__ k, const E
                 red_q[warp][cg * kCols + c] = pq[c];
             }
         }
-        if (lane == 0) red_kq[warp] = kq;
+        if (lane == 0) {
+            red_kq[warp] = kq;
+            if (NORM) {
+                red_kk[warp] = k2;
+                red_qq[warp] = q2;
+            }
+        }
         __syncthreads();
 
         // One thread per column: delta and o.
         if (tid < VS) {
-            float dk = 0.f, dq = 0.f, kqs = 0.f;
+            float dk = 0.f, dq = 0.f, kqs = 0.f, kks = 0.f, qqs = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
                 dk += red_k[w][tid];
                 dq += red_q[w][tid];
                 kqs += red_kq[w];
+                if (NORM) {
+                    kks += red_kk[w];
+                    qqs += red_qq[w];
+                }
             }
             const size_t vo = row * V + col0 + tid;
-            const float d = beta[row] * (load1(v + vo) - alpha * dk);
-            delta_s[tid] = d;
-            store1(o + vo, scale * fmaf(d, kqs, alpha * dq));
+            if (NORM) {
+                const float rk = rsqrtf(kks + kL2NormEps), rq = rsqrtf(qqs + kL2NormEps);
+                const float d = beta[row] * (load1(v + vo) - alpha * rk * dk);
+                delta_s[tid] = rk * d;
+                store1(o + vo, scale * rq * fmaf(d, rk * kqs, alpha * dq));
+            } else {
+                const float d = beta[row] * (load1(v + vo) - alpha * dk);
+                delta_s[tid] = d;
+                store1(o + vo, scale * fmaf(d, kqs, alpha * dq));
+            }
         }
         __syncthreads();
 
@@ -159,7 +189,6 @@ gdn_status check_decode(const gdn_problem *p) {
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
-    if (p->flags & GDN_FLAG_QK_L2NORM) return GDN_ERR_UNSUPPORTED;   // not built yet
     if (p->algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
     if (p->K % 64 != 0 || p->K > 256) return GDN_ERR_UNSUPPORTED;
     if (p->V % 16 != 0 || p->V > 4096) return GDN_ERR_UNSUPPORTED;
@@ -183,9 +212,11 @@ cudaError_t launch(const gdn_problem *p, const void *q, const void *k, const voi
                    float *state_out, void *o, cudaStream_t s) {
     constexpr int threads = K * VS / (kRows * kCols);
     const dim3 grid(p->V / VS, p->H, p->B);
-    gdn_decode_step_kernel<E, K, VS><<<grid, threads, 0, s>>>(
-        static_cast<const E *>(q), static_cast<const E *>(k), static_cast<const E *>(v), gamma,
-        beta, scale, state_in, state_out, static_cast<E *>(o), p->T, p->H, p->V);
+    const auto kernel = (p->flags & GDN_FLAG_QK_L2NORM) ? gdn_decode_step_kernel<E, K, VS, true>
+                                                        : gdn_decode_step_kernel<E, K, VS, false>;
+    kernel<<<grid, threads, 0, s>>>(static_cast<const E *>(q), static_cast<const E *>(k),
+                                    static_cast<const E *>(v), gamma, beta, scale, state_in,
+                                    state_out, static_cast<E *>(o), p->T, p->H, p->V);
     return cudaGetLastError();
 }
 

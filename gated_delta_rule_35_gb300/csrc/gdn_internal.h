@@ -26,7 +26,18 @@ struct Args {
     void *o;
     float *h_final;
     uint32_t *status;   // device status word (first bytes of the workspace)
+    // Input front-end (GDN_FLAG_*). With GDN_FLAG_RAW_G, g holds raw per-token
+    // log decays and the first kernel writes their chunk-local cumulative sum
+    // to g_cum, which the later kernels read; with GDN_FLAG_QK_L2NORM the first
+    // kernel writes each k row's factor 1 / sqrt(|k|^2 + eps) to rk.
+    int flags;
+    float *g_cum;   // [B, T, H] fp32 workspace
+    float *rk;      // [B, T, H] fp32 workspace
+    // g as the kernels after the first one read it: g_cum or g
+    const float *g_chunk() const { return (flags & GDN_FLAG_RAW_G) ? g_cum : g; }
 };
+
+constexpr float kL2NormEps = 1e-6f;
 
 // Workspace of the SIMT pipeline: fp32 intermediates, every region 256-byte aligned.
 struct SimtWorkspace {

@@ -24,6 +24,22 @@ __device__ __forceinline__ int64_t tok(int b, int t, int h, int T, int H) {
     return (static_cast<int64_t>(b) * T + t) * H + h;
 }
 
+// Front-end q/k normalisation in shared memory: rows 0..n-1 of xs (stride KP,
+// K values) become x / sqrt(sum x^2 + eps), one warp per row; the factors go
+// to rs[i] when rs is given. Call between barriers.
+__device__ void l2norm_rows_smem(float *xs, int KP, int K, int n, float *rs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int i = warp; i < n; i += nw) {
+        float ss = 0.f;
+        for (int kk = lane; kk < K; kk += 32) ss = fmaf(xs[i * KP + kk], xs[i * KP + kk], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float r = rsqrtf(ss + kL2NormEps);
+        for (int kk = lane; kk < K; kk += 32) xs[i * KP + kk] *= r;
+        if (rs && lane == 0) rs[i] = r;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // WY build + recompute_w_u ("WarpDrive" kernel 5). One block per (chunk, h, b).
 //   L_ij = beta_i (k_i . k_j) exp(g_i - g_j), i > j;  A = (I + L)^-1
@@ -35,9 +51,10 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__restrict__ g,
                   const float *__restrict__ beta, int Tn, int H, int K, int V, int T_pad,
-                  float *__restrict__ A_ws, float *__restrict__ w_ws, float *__restrict__ u_ws) {
+                  float *__restrict__ A_ws, float *__restrict__ w_ws, float *__restrict__ u_ws,
+                  int flags, float *__restrict__ g_cum, float *__restrict__ rk_out) {
     extern __shared__ float smem[];
-    __shared__ float gs[kChunk], bs[kChunk];
+    __shared__ float gs[kChunk], bs[kChunk], rks[kChunk];
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     const int t0 = c * kChunk;
     const int n = min(kChunk, Tn - t0);
@@ -56,6 +73,21 @@ wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float 
         ks[i * KP + kk] = i < n ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
     }
     __syncthreads();
+    // Front-end: g from raw per-token log decays (chunk-local inclusive sum),
+    // k rows normalised; both written out for the later kernels.
+    if (flags & GDN_FLAG_RAW_G) {
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int i = 0; i < n; ++i) gs[i] = acc += gs[i];
+        }
+        __syncthreads();
+        if (tid < n) g_cum[tok(b, t0 + tid, h, Tn, H)] = gs[tid];
+    }
+    if (flags & GDN_FLAG_QK_L2NORM) {
+        l2norm_rows_smem(ks, KP, K, n, rks);
+        __syncthreads();
+        if (tid < n) rk_out[tok(b, t0 + tid, h, Tn, H)] = rks[tid];
+    }
 
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
         const int i = idx >> 6, j = idx & 63;
@@ -121,7 +153,7 @@ __global__ void __launch_bounds__(kThreads)
 chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float *__restrict__ w_ws,
                const float *__restrict__ u_ws, const float *__restrict__ h0, int Tn, int H, int K,
                int V, int NT, int T_pad, float *__restrict__ h_ws, float *__restrict__ vn_ws,
-               float *__restrict__ h_final) {
+               float *__restrict__ h_final, const float *__restrict__ rk) {
     extern __shared__ float smem[];
     __shared__ float gs[kChunk];
     const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -150,7 +182,8 @@ chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float
         for (int idx = tid; idx < kChunk * K; idx += kThreads) {
             const int i = idx / K, kk = idx - i * K;
             ws[i * KP + kk] = w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk];
-            ks[i * KP + kk] = i < n ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
+            const int64_t r = tok(b, t0 + i, h, Tn, H);
+            ks[i * KP + kk] = i < n ? to_f32(k[r * K + kk]) * (rk ? rk[r] : 1.f) : 0.f;
         }
         for (int idx = tid; idx < kChunk * kBV; idx += kThreads) {
             const int i = idx / kBV, nn = idx - i * kBV;
@@ -205,7 +238,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ g,
                const float *__restrict__ h_ws, const float *__restrict__ vn_ws, int Tn, int H,
-               int K, int V, int NT, int T_pad, float scale, T *__restrict__ o) {
+               int K, int V, int NT, int T_pad, float scale, T *__restrict__ o, int flags) {
     extern __shared__ float smem[];
     __shared__ float gs[kChunk];
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -226,6 +259,11 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
         ks[i * KP + kk] = ok ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
     }
     __syncthreads();
+    if (flags & GDN_FLAG_QK_L2NORM) {
+        l2norm_rows_smem(qs, KP, K, n, nullptr);
+        l2norm_rows_smem(ks, KP, K, n, nullptr);
+        __syncthreads();
+    }
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
         const int i = idx >> 6, j = idx & 63;
         float val = 0.f;
@@ -292,13 +330,17 @@ cudaError_t run(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Ma
     const dim3 chunks(a.NT, a.H, a.B);
     if ((e = m.mark(0, s)) != cudaSuccess) return e;
     wy_prepare_kernel<T><<<chunks, kThreads, s1, s>>>(k, v, a.g, a.beta, a.T, a.H, a.K, a.V,
-                                                     a.T_pad, ws.A, ws.w, ws.u);
+                                                     a.T_pad, ws.A, ws.w, ws.u, a.flags, a.g_cum,
+                                                     a.rk);
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
+    const float *rk = (a.flags & GDN_FLAG_QK_L2NORM) ? a.rk : nullptr;
     chunk_h_kernel<T><<<dim3(a.V / kBV, a.H, a.B), kThreads, s2, s>>>(
-        k, a.g, ws.w, ws.u, a.h0, a.T, a.H, a.K, a.V, a.NT, a.T_pad, ws.h, ws.v_new, a.h_final);
+        k, a.g_chunk(), ws.w, ws.u, a.h0, a.T, a.H, a.K, a.V, a.NT, a.T_pad, ws.h, ws.v_new,
+        a.h_final, rk);
     if ((e = m.mark(2, s)) != cudaSuccess) return e;
-    chunk_o_kernel<T><<<chunks, kThreads, s3, s>>>(q, k, a.g, ws.h, ws.v_new, a.T, a.H, a.K, a.V,
-                                                  a.NT, a.T_pad, a.scale, static_cast<T *>(a.o));
+    chunk_o_kernel<T><<<chunks, kThreads, s3, s>>>(q, k, a.g_chunk(), ws.h, ws.v_new, a.T, a.H, a.K,
+                                                  a.V, a.NT, a.T_pad, a.scale,
+                                                  static_cast<T *>(a.o), a.flags);
     if ((e = m.mark(3, s)) != cudaSuccess) return e;
     return cudaGetLastError();
 }

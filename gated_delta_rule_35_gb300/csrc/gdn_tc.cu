@@ -131,23 +131,27 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                     const float *__restrict__ g, const float *__restrict__ h0,
                     float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
-                    float scale, int l2_prefetch, uint32_t *status) {
+                    float scale, int l2_prefetch, uint32_t *status, int l2norm,
+                    const float *__restrict__ rk) {
     using Lay = TcLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so
     // that every access through it stays a shared-memory access.
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    // Per chunk slot (c & 3), 0 past T where marked: g; exp(g) (0); exp(g_last - g)
-    // (0); and the two factors of exp(g_i - g_j) about g_ref = g_last / 2,
-    // scale exp(g_i - g_ref) (0) and exp(g_ref - g_j) (0), usable while |g_last|
-    // stays small enough for both to be finite fp32 numbers (flag fz_s).
-    float *g_s = reinterpret_cast<float *>(sm + Lay::kG);
-    float *eg_s = g_s + 256;
-    float *gate_s = g_s + 512;
-    float *rf_s = g_s + 768;
-    float *cf_s = g_s + 1024;
-    int *fz_s = reinterpret_cast<int *>(g_s + 1280);
+    // Per chunk slot (c & 3), 0 past T where marked, with rq_i and rk_j the
+    // q and k rows' normalisation factors (1 without the front-end norm):
+    // exp(g) rq (0); exp(g_last - g) rk (0); and the row and column factors of
+    // scale rq_i rk_j exp(g_i - g_j): about g_ref = g_last / 2, scale rq
+    // exp(g_i - g_ref) (0) and rk exp(g_ref - g_j) (0), usable while |g_last|
+    // stays small enough for both to be finite fp32 numbers (flag fz_s); else
+    // the exponents g_i + ln rq_i and g_j - ln rk_j.
+    float *tab = reinterpret_cast<float *>(sm + Lay::kG);   // first 256 floats unused
+    float *eg_s = tab + 256;
+    float *gate_s = tab + 512;
+    float *rf_s = tab + 768;
+    float *cf_s = tab + 1024;
+    int *fz_s = reinterpret_cast<int *>(tab + 1280);
     Bars *bs = reinterpret_cast<Bars *>(sm + Lay::kBar);
     volatile uint32_t *abort = &bs->abort;
 
@@ -348,13 +352,20 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             return (ptid < 64 && c < NT) ? g[(static_cast<int64_t>(b) * T + min(T, c * 64 + 64) - 1) * H + h]
                                          : 0.f;
         };
-        float g_next = load_g(0), gl_next = load_gl(0);
+        // k rows' normalisation factors, from the WY kernel
+        auto load_rk = [&](int c) {
+            const int t = c * 64 + ptid;
+            return (l2norm && ptid < 64 && c < NT && t < T) ? rk[(static_cast<int64_t>(b) * T + t) * H + h]
+                                                           : 1.f;
+        };
+        float g_next = load_g(0), gl_next = load_gl(0), rk_next = load_rk(0);
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1, gs = c & 3;
             const int n = min(64, T - c * 64);
-            const float g_cur = g_next, gl = gl_next;
+            const float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
             g_next = load_g(c + 1);
             gl_next = load_gl(c + 1);
+            rk_next = load_rk(c + 1);
             // Decay tables of chunk c in slot c % 4. Their previous reader, chunk
             // c - 4, finished before U(c - 3) was issued, and stage s landing for
             // chunk c needs HT(c - 2). For the same reason the next phase of
@@ -362,14 +373,41 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // this one has passed.
             if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort)) break;
             if (ptid < 64) {
+                float rq = 1.f;
+                if (l2norm) {
+                    // |q_i|^2 from the stage's q tile (rows 0-63 of the stacked
+                    // operand; the swizzle only permutes 16-byte chunks in a row)
+                    const unsigned char *qrow = sm + s * Lay::kStage + Lay::kStAbig + ptid * 128;
+                    float ss = 0.f;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qrow + kb * 16384 + j * 16);
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __uint_as_float(w4[e] << 16);
+                                const float hi = __uint_as_float(w4[e] & 0xffff0000u);
+                                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                            }
+                        }
+                    rq = rsqrtf(ss + kL2NormEps);
+                }
                 const float gref = 0.5f * gl;
-                g_s[gs * 64 + ptid] = g_cur;
-                eg_s[gs * 64 + ptid] = ptid < n ? __expf(g_cur) : 0.f;
-                gate_s[gs * 64 + ptid] = ptid < n ? __expf(gl - g_cur) : 0.f;
-                rf_s[gs * 64 + ptid] = ptid < n ? scale * __expf(g_cur - gref) : 0.f;
-                cf_s[gs * 64 + ptid] = ptid < n ? __expf(gref - g_cur) : 0.f;
                 // |g_i - g_ref| <= |g_last| / 2 for cumulative log decays in [g_last, 0]
-                if (ptid == 0) fz_s[gs] = fabsf(gl) <= 160.f;
+                const bool fzc = fabsf(gl) <= 160.f;
+                const bool ok = ptid < n;
+                eg_s[gs * 64 + ptid] = ok ? __expf(g_cur) * rq : 0.f;
+                gate_s[gs * 64 + ptid] = ok ? __expf(gl - g_cur) * rk_cur : 0.f;
+                if (fzc) {
+                    rf_s[gs * 64 + ptid] = ok ? scale * __expf(g_cur - gref) * rq : 0.f;
+                    cf_s[gs * 64 + ptid] = ok ? __expf(gref - g_cur) * rk_cur : 0.f;
+                } else {
+                    rf_s[gs * 64 + ptid] = l2norm ? g_cur + __logf(rq) : g_cur;
+                    cf_s[gs * 64 + ptid] = l2norm ? g_cur - __logf(rk_cur) : g_cur;
+                }
+                if (ptid == 0) fz_s[gs] = fzc;
             }
             mbar_arrive(&bs->g_ready[gs]);
         }
@@ -456,10 +494,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                 spin_bar(&bs->big_done, c & 1, abort))))
                 break;
             tc_fence_after_sync();
-            const float *gc = g_s + gs * 64;
             if (upper) {
                 const bool fz = fz_s[gs];
-                const float gi = gc[row], ri = rf_s[gs * 64 + row];
+                const float ri = rf_s[gs * 64 + row];
                 const float *cfc = cf_s + gs * 64;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
@@ -467,10 +504,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float v[16];
                     if (j0 <= (q4 & 1) * 32 + 31) {
                         float fj[16];
-                        const float *src = fz ? cfc : gc;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
-                            const float4 f4 = *reinterpret_cast<const float4 *>(src + j0 + 4 * m);
+                            const float4 f4 = *reinterpret_cast<const float4 *>(cfc + j0 + 4 * m);
                             fj[4 * m] = f4.x;
                             fj[4 * m + 1] = f4.y;
                             fj[4 * m + 2] = f4.z;
@@ -483,7 +519,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         } else {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
-                                const float d = (j0 + e <= row) ? gi - fj[e] : -INFINITY;
+                                const float d = (j0 + e <= row) ? ri - fj[e] : -INFINITY;
                                 v[e] = scale * v[e] * __expf(d);
                             }
                         }
@@ -625,8 +661,8 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(a.V / kTcBV) * a.H * a.B;
     gdn_fused_tc_kernel<K><<<dim3(a.V / kTcBV, a.H, a.B), kTcThreads, smem, s>>>(
-        mq, mk, mv, ma, a.g, a.h0, a.h_final, static_cast<__nv_bfloat16 *>(a.o), a.T, a.H, a.V,
-        a.scale, ctas <= sms ? 1 : 0, a.status);
+        mq, mk, mv, ma, a.g_chunk(), a.h0, a.h_final, static_cast<__nv_bfloat16 *>(a.o), a.T, a.H,
+        a.V, a.scale, ctas <= sms ? 1 : 0, a.status, (a.flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, a.rk);
     return cudaGetLastError();
 }
 

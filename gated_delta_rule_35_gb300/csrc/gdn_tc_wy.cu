@@ -23,6 +23,14 @@
 //   epi     A diag(beta), A diag(beta exp(g)) -> bf16 -> TMA store
 // The correction products run with bf16 operands and fp32 accumulation; the
 // block-diagonal part and the subtractions stay fp32.
+//
+// Front-end (problem flags): with GDN_FLAG_RAW_G the chunk's g is the inclusive
+// sum of the raw per-token log decays, taken here and written to g_cum for the
+// fused kernel; with GDN_FLAG_QK_L2NORM each k row's factor
+// r_i = 1 / sqrt(|k_i|^2 + eps) is taken from the k tile and written to rk. The
+// normalised rows never exist: L_ij gains r_i r_j and the second output's
+// column scale gains r_j (w = A diag(beta exp(g)) diag(r) k), while the Gram
+// MMA still reads the k tile as loaded.
 #include "gdn_internal.h"
 #include "tc_common.cuh"
 
@@ -46,15 +54,17 @@ struct WyLayout {
     static constexpr uint32_t kY = kXU + 16384;            // Y1, then Y2 (bf16, rows along N)
     static constexpr uint32_t kOut = kY + 8192;            // A diag(beta) staging
     static constexpr uint32_t kLd = kOut + 8192;           // diagonal blocks fp32 [4][16][17]
-    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;   // g, beta, beta exp(g), cf; barriers
-    static constexpr uint32_t kBytes = kMisc + 1280;
+    // g, beta, beta exp(g) r, cf, r (64 floats each), a scan total; barriers
+    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;
+    static constexpr uint32_t kBar = kMisc + 1344;
+    static constexpr uint32_t kBytes = kBar + 256;
 };
 
 template <int K>
 __global__ void __launch_bounds__(kWyThreads, 4)
 gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_a,
                  const float *__restrict__ g, const float *__restrict__ beta, int T, int H,
-                 uint32_t *status) {
+                 uint32_t *status, int flags, float *__restrict__ g_cum, float *__restrict__ rk_out) {
     using Lay = WyLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -67,7 +77,9 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // beta_i exp(g_i - g_ref) it gives beta_i exp(g_i - g_j) without an
     // exponential per element, while |g_last| keeps both factors finite
     float *cf_s = g_s + 192;
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kMisc + 1024);
+    float *rk_s = g_s + 256;    // the k rows' normalisation factors (1 without it)
+    float *tot_s = g_s + 320;   // raw-g scan: total of tokens 0-31
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kBar);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
 
@@ -89,18 +101,36 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int kb = 0; kb < KB; ++kb)
             tma_load_4d(sm + Lay::kK + kb * 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
     }
-    const float g_last = g[(static_cast<int64_t>(b) * T + t0 + n - 1) * H + h];
+    const bool raw_g = flags & GDN_FLAG_RAW_G, l2norm = flags & GDN_FLAG_QK_L2NORM;
+    const int64_t my_row = (static_cast<int64_t>(b) * T + t0 + tid) * H + h;
+    float gv = 0.f, bv = 0.f;
+    if (tid < n) {
+        gv = g[my_row];
+        bv = beta[my_row];
+    }
+    if (raw_g) {
+        // inclusive sum over the chunk: tokens 0-31 in warp 0, 32-63 in warp 1
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, gv, off);
+            if (lane >= off) gv += y;
+        }
+        if (tid == 31) *tot_s = gv;
+        __syncthreads();
+        if (warp == 1) gv += *tot_s;
+        if (tid >= n) gv = 0.f;
+        else if (tid < 64) g_cum[my_row] = gv;
+    }
+    if (tid < 64) {
+        g_s[tid] = gv;
+        b_s[tid] = bv;
+        rk_s[tid] = 1.f;
+    }
+    __syncthreads();
+    const float g_last = g_s[n - 1];
     const float g_ref = 0.5f * g_last;
     const bool fz = fabsf(g_last) <= 160.f;   // |g_i - g_ref| <= |g_last| / 2 for decays <= 0
     if (tid < 64) {
-        float gv = 0.f, bv = 0.f;
-        if (tid < n) {
-            const int64_t row = (static_cast<int64_t>(b) * T + t0 + tid) * H + h;
-            gv = g[row];
-            bv = beta[row];
-        }
-        g_s[tid] = gv;
-        b_s[tid] = bv;
         eb_s[tid] = bv * __expf(gv);
         cf_s[tid] = tid < n ? __expf(g_ref - gv) : 0.f;
     }
@@ -115,7 +145,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     // One MMA group issued by thread 0 (A K-major, B K-major or rows-along-N),
     // then everyone waits for it.
-    auto mma = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
+    auto mma_issue = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
         if (tid == 0) {
             tc_fence_after_sync();
             const uint32_t id = idesc_bf16(M, 64, false, b_mn);
@@ -127,9 +157,15 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             }
             mma_commit(bar_mma);
         }
+    };
+    auto mma_wait = [&]() {
         fail |= !mbar_wait(bar_mma, phase, kWyWaitNs);
         phase ^= 1;
         tc_fence_after_sync();
+    };
+    auto mma = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
+        mma_issue(M, a, bop, b_mn, ksteps);
+        mma_wait();
     };
     // This thread's accumulator row, 16 columns at a time.
     auto load16 = [&](int blk, float *v) {
@@ -144,11 +180,34 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // rows past the k tile are whatever follows it (their products are unused),
     // and two full warps form L instead of four half-empty ones
     if (__syncthreads_or(fail)) goto done;
-    mma(128, s_k, s_k, false, K / 16);
+    mma_issue(128, s_k, s_k, false, K / 16);
+    if (l2norm && tid < 64) {
+        // |k_i|^2 from the k tile while the Gram runs (the swizzle permutes the
+        // 16-byte chunks within a row, which a sum of squares does not see)
+        float ss = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(sm + Lay::kK + kb * 8192 + tid * 128 + j * 16);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                }
+            }
+        const float r = rsqrtf(ss + kL2NormEps);
+        rk_s[tid] = r;
+        cf_s[tid] *= r;
+        eb_s[tid] *= r;
+        if (tid < n) rk_out[my_row] = r;
+    }
+    mma_wait();
     if (__syncthreads_or(fail)) goto done;
     if (warp < 2) {
         const int r = warp * 32 + lane, rb = r >> 4;
-        const float gr = r >= 0 ? g_s[r] : 0.f, br = r >= 0 ? b_s[r] : 0.f;
+        const float gr = g_s[r], br = b_s[r] * rk_s[r];
         const float rf = br * __expf(gr - g_ref);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
@@ -171,7 +230,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     for (int e = 0; e < 16; ++e) {
                         const int j = blk * 16 + e;
                         const float d = (j < r) ? gr - g_s[j] : -INFINITY;
-                        v[e] = br * v[e] * __expf(d);
+                        v[e] = br * v[e] * rk_s[j] * __expf(d);
                     }
                 }
                 if (blk == rb) {
@@ -322,8 +381,8 @@ cudaError_t launch_wy(const Args &a, void *abeta, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(gdn_wy_tc_kernel<K>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gdn_wy_tc_kernel<K><<<dim3(a.NT, a.H, a.B), kWyThreads, smem, s>>>(mk, ma, a.g, a.beta, a.T,
-                                                                       a.H, a.status);
+    gdn_wy_tc_kernel<K><<<dim3(a.NT, a.H, a.B), kWyThreads, smem, s>>>(
+        mk, ma, a.g, a.beta, a.T, a.H, a.status, a.flags, a.g_cum, a.rk);
     return cudaGetLastError();
 }
 

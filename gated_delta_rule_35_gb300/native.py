@@ -138,14 +138,16 @@ def _check_inputs(q, k, v, g, beta, h0):
 
 def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
               algo: str = "auto", workspace=None, out=None, final_state=None, stream=None,
-              events=None):
+              events=None, raw_g: bool = False, qk_l2norm: bool = False):
     """Chunked gated-delta-rule forward on CUDA tensors. Returns (o, h_final or None).
 
     q, k [B,T,H,K] and v [B,T,H,V] (float32 or bfloat16), g and beta [B,T,H]
     float32 (g: chunk-local cumulative log-decay), h0 [B,H,K,V] float32 or None.
-    ``workspace``/``out``/``final_state`` may be passed to reuse buffers."""
+    ``workspace``/``out``/``final_state`` may be passed to reuse buffers.
+    ``raw_g``: g holds per-token log decays, summed per chunk in the kernels;
+    ``qk_l2norm``: q and k rows are L2-normalised in the kernels (eps 1e-6)."""
     B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
-    p = problem(B, T, H, K, V, q.dtype, algo)
+    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
     need = workspace_bytes(p)
     if need == 0:
         raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_chunk_fwd_workspace_bytes")
@@ -174,11 +176,12 @@ STAGES = ("A", "w", "u", "v_new", "h", "A_beta")
 
 
 def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = "simt",
-                     stages=("A", "w", "u", "v_new", "h")):
+                     stages=("A", "w", "u", "v_new", "h"), raw_g: bool = False,
+                     qk_l2norm: bool = False):
     """Forward plus the requested exported intermediates (fp32 tensors): A, w, u,
     v_new, h (SIMT path) or A_beta = A diag(beta) (tensor-core path)."""
     B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
-    p = problem(B, T, H, K, V, q.dtype, algo)
+    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
     NT = (T + CHUNK - 1) // CHUNK
     Tp = NT * CHUNK
     f32 = dict(dtype=torch.float32, device=q.device)
@@ -203,7 +206,7 @@ def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = 
 
 
 def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None, out=None,
-                stream=None):
+                stream=None, qk_l2norm: bool = False):
     """Recurrent step(s) of the rule on CUDA tensors: advances every sequence by
     its T tokens and returns (o, state_out).
 
@@ -211,7 +214,8 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
     float32, gamma the per-token log decay itself (not a cumulative sum);
     state [B,H,K,V] float32 (an h_final of chunk_fwd). ``state_out=None``
     updates ``state`` in place; pass ``state_out=state`` for the same, or
-    another buffer to keep ``state``."""
+    another buffer to keep ``state``. ``qk_l2norm`` normalises the q and k
+    rows in the kernel (eps 1e-6)."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     dev = q.device
@@ -232,7 +236,7 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
         if not t.is_contiguous() or t.device != dev:
             raise ValueError("all tensors must be contiguous and on the same device")
     o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
-    p = problem(B, T, H, K, V, q.dtype, "auto")
+    p = problem(B, T, H, K, V, q.dtype, "auto", flags_of(False, qk_l2norm))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     st = lib().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
                                _ptr(beta), float(scale), _ptr(state), _ptr(so), _ptr(o),
@@ -255,13 +259,14 @@ def check_device_status(workspace, stream=None) -> int:
 
 
 def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
-                   algo: str = "auto", device=None):
+                   algo: str = "auto", device=None, raw_g: bool = False, qk_l2norm: bool = False):
     """Host-tensor front end: copies the inputs to the GPU, runs chunk_fwd and
     copies o (and h_final) back into pinned host tensors, synchronously."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     dq, dk, dv, dg, db = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
     dh0 = None if h0 is None else h0.to(dev, non_blocking=True)
-    o, hf = chunk_fwd(dq, dk, dv, dg, db, scale, dh0, output_final_state, algo)
+    o, hf = chunk_fwd(dq, dk, dv, dg, db, scale, dh0, output_final_state, algo, raw_g=raw_g,
+                      qk_l2norm=qk_l2norm)
     ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     ho.copy_(o, non_blocking=True)
     hhf = None

@@ -135,3 +135,17 @@ def test_decode_launches():
         ["gdn_decode_step_kernel"]
     assert native.decode_launches(native.problem(4, 0, 16, 128, 128, native.GDN_BF16)) == []
     assert native.decode_launches(native.problem(4, 1, 16, 96, 128, native.GDN_BF16)) == []
+
+
+def test_flags_validated():
+    """Known front-end bits are accepted by every path; unknown bits are rejected."""
+    for algo in ("simt", "tc"):
+        for flags in (1, 2, 3):
+            p = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo, flags)
+            assert native.workspace_bytes(p) > native.workspace_bytes(
+                native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo)) - 1
+    bad = native.problem(1, 64, 1, 64, 64, native.GDN_BF16, "auto", 4)
+    assert native.workspace_bytes(bad) == 0
+    assert _call(bad) == native.GDN_ERR_INVALID_ARG
+    assert _decode(native.problem(1, 1, 1, 64, 64, native.GDN_BF16, "auto", 8)) == \
+        native.GDN_ERR_INVALID_ARG
