@@ -7,4 +7,5 @@ the CUDA path and never imports it.
   recurrence  token-by-token fp64 recurrence in plain C (``gdn_ref.c``)
   chunked     fp64 NumPy chunked form exporting every intermediate stage
   frontend    fp64 input steps: chunk-local cumsum of raw log decays, q/k L2 norm
+  epilogue    fp64 gated RMSNorm of the output rows
 """
