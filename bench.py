@@ -17,8 +17,10 @@ only), each step a bounded sample of the workload's (b, h) sequences.
 The line also carries "decode": the recurrent decode step timed on its own
 workload (256 sequences x 16 heads, one token, K = V = 128, bf16) against the
 HBM roofline of reading and writing the fp32 state once (--no-decode skips it);
-and "frontend": the same step on raw inputs with the chunk-local cumsum of g
-and the q/k L2 norm done in the kernels (--no-frontend skips it).
+"frontend": the same step on raw inputs with the chunk-local cumsum of g
+and the q/k L2 norm done in the kernels (--no-frontend skips it); and
+"output_norm": the same step with the gated RMSNorm output stage
+(--no-output-norm skips it).
 """
 from __future__ import annotations
 
@@ -400,6 +402,47 @@ def bench_frontend(args, w, world, dev, flush):
             "inputs": "q, k unnormalised N(0,1); g per-token log decays; scale K^-0.5"}
 
 
+def bench_output_norm(args, w, world, dev, flush, d):
+    """The same step with the gated RMSNorm output stage (gate and norm weight
+    read, o normalised before its rounding; the tensor-core path runs each
+    head's V tiles as a cluster). Timed like the main step."""
+    from gated_delta_rule_35_gb300 import chunk_fwd, native
+    from gated_delta_rule_35_gb300.inputs import make_output_norm
+
+    gate, weight = make_output_norm(w.B, w.T, w.H, w.V, dtype=w.dtype, seed=w.seed)
+    gate, weight = gate.to(dev), weight.to(dev)
+    p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, args.algo)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
+    hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(10, min(args.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+
+    def step():
+        chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=args.algo,
+                  workspace=ws, out=o, final_state=hf, stream=stream, gate=gate,
+                  norm_weight=weight, norm_eps=1e-6)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n / 1e3, world, dev)
+    return {"workload": w.name + "_gated_rmsnorm", "steps_timed": n, "ms_per_step": 1e3 * t,
+            "tokens_per_s": w.B * w.T * world / t, "kernels": native.launches(p),
+            "gpu_launches": len(native.launches(p)) * n,
+            "extra_bytes_per_token_head": 2 * w.V,
+            "inputs": "gate N(0,1) in the I/O dtype, norm weight 1 + 0.1 N(0,1), eps 1e-6"}
+
+
 def bench_decode(args, world, dev):
     """The decode step on its own workload: one token for each of B*H heads, the
     state [B,H,K,V] fp32 read and written in place once per call. The state
@@ -555,6 +598,7 @@ def bench_ours(args, w, world, rank, local):
 
     dec = None if args.no_decode else bench_decode(args, world, dev)
     fe = None if args.no_frontend else bench_frontend(args, w, world, dev, flush)
+    on = None if args.no_output_norm else bench_output_norm(args, w, world, dev, flush, d)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -572,7 +616,7 @@ def bench_ours(args, w, world, rank, local):
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
             "kernels": kernels,
             "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
-            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe,
+            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe, "output_norm": on,
         }
         print(json.dumps(line), flush=True)
 
@@ -589,6 +633,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-frontend", action="store_true",
                     help="skip the in-kernel front-end measurement")
+    ap.add_argument("--no-output-norm", action="store_true",
+                    help="skip the gated RMSNorm output-stage measurement")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="target CPU time of the oracle baseline sample")
     args = ap.parse_args()

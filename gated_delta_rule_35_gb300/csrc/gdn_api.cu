@@ -47,12 +47,14 @@ size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
 gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
                const float *beta, float scale, const float *h0, void *o, float *h_final,
                void *workspace, size_t workspace_bytes, const gdn_stage_exports *ex,
-               const Marks &marks, cudaStream_t stream) {
+               const Marks &marks, cudaStream_t stream, const gdn_output_norm *norm = nullptr) {
     gdn_status st = check_problem(p);
     if (st != GDN_OK) return st;
     const bool empty = p->T == 0;
     if (!empty && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, g, beta, h0, o, h_final, workspace};
+    if (norm && (!norm->gate || !norm->weight || !(norm->eps >= 0.f))) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, h0, o, h_final, workspace,
+                          norm ? norm->gate : nullptr, norm ? norm->weight : nullptr};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
     const gdn_algo algo = resolve_algo(p);
@@ -71,6 +73,11 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     a.o = o; a.h_final = h_final;
     a.status = static_cast<uint32_t *>(workspace);
     a.flags = p->flags;
+    if (norm) {
+        a.gate = norm->gate;
+        a.norm_w = norm->weight;
+        a.norm_eps = norm->eps;
+    }
     char *front = static_cast<char *>(workspace) + kStatusBytes;
     const size_t plane = align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
     a.g_cum = reinterpret_cast<float *>(front);
@@ -153,6 +160,22 @@ GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p, const void *q, c
     m.n = n_events;
     return gdn::run(p, q, k, v, g, beta, scale, h0, o, h_final, workspace, workspace_bytes,
                     nullptr, m, static_cast<cudaStream_t>(stream));
+}
+
+GDN_API gdn_status gdn_chunk_fwd_ex(const gdn_problem *p, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta, float scale,
+                                    const float *h0, const gdn_output_norm *norm, void *o,
+                                    float *h_final, void *workspace, size_t workspace_bytes,
+                                    void *const *events, int32_t n_events, void *stream) {
+    gdn::Marks m;
+    if (events) {
+        const int n = gdn::launches(p, nullptr, 0);
+        if (n == 0 || n_events < n + 1) return GDN_ERR_INVALID_ARG;
+        m.ev = reinterpret_cast<cudaEvent_t const *>(events);
+        m.n = n_events;
+    }
+    return gdn::run(p, q, k, v, g, beta, scale, h0, o, h_final, workspace, workspace_bytes,
+                    nullptr, m, static_cast<cudaStream_t>(stream), norm);
 }
 
 GDN_API gdn_status gdn_chunk_fwd_stages(const gdn_problem *p, const void *q, const void *k,

@@ -35,6 +35,10 @@ struct Args {
     float *rk;      // [B, T, H] fp32 workspace
     // g as the kernels after the first one read it: g_cum or g
     const float *g_chunk() const { return (flags & GDN_FLAG_RAW_G) ? g_cum : g; }
+    // Output stage (gated RMSNorm over V); gate == nullptr: plain o.
+    const void *gate = nullptr;
+    const float *norm_w = nullptr;
+    float norm_eps = 0.f;
 };
 
 constexpr float kL2NormEps = 1e-6f;

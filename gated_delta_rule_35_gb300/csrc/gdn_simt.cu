@@ -238,7 +238,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ g,
                const float *__restrict__ h_ws, const float *__restrict__ vn_ws, int Tn, int H,
-               int K, int V, int NT, int T_pad, float scale, T *__restrict__ o, int flags) {
+               int K, int V, int NT, int T_pad, float scale, T *__restrict__ o, int flags,
+               const T *__restrict__ gate, const float *__restrict__ norm_w, float norm_eps) {
     extern __shared__ float smem[];
     __shared__ float gs[kChunk];
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -250,6 +251,8 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
     float *Ps = ks + kChunk * KP;      // [64][65]
     float *hs = Ps + kChunk * 65;      // [K][65]
     float *vs = hs + K * 65;           // [64][65]
+    float *os = vs + kChunk * 65;      // [64][V + 1] fp32 o rows, output stage only
+    const int OP = V + 1;
 
     if (tid < kChunk) gs[tid] = tid < n ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
     for (int idx = tid; idx < kChunk * K; idx += kThreads) {
@@ -293,8 +296,29 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
             for (int kk = 0; kk < K; ++kk) inter = fmaf(qs[i * KP + kk], hs[kk * 65 + nn], inter);
             float intra = 0.f;
             for (int j = 0; j <= i; ++j) intra = fmaf(Ps[i * 65 + j], vs[j * 65 + nn], intra);
-            store_as(&o[tok(b, t0 + i, h, Tn, H) * V + v0 + nn],
-                     scale * (expf(gs[i]) * inter + intra));
+            const float oi = scale * (expf(gs[i]) * inter + intra);
+            if (gate)
+                os[i * OP + v0 + nn] = oi;
+            else
+                store_as(&o[tok(b, t0 + i, h, Tn, H) * V + v0 + nn], oi);
+        }
+    }
+    if (gate) {
+        // gated RMSNorm over the V values of each row, one warp per row
+        __syncthreads();
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int i = warp; i < n; i += kThreads / 32) {
+            float ss = 0.f;
+            for (int nn = lane; nn < V; nn += 32) ss = fmaf(os[i * OP + nn], os[i * OP + nn], ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float rstd = rsqrtf(ss / V + norm_eps);
+            const int64_t r = tok(b, t0 + i, h, Tn, H) * V;
+            for (int nn = lane; nn < V; nn += 32) {
+                const float z = to_f32(gate[r + nn]);
+                const float sg = 1.f / (1.f + expf(-z));
+                store_as(&o[r + nn], os[i * OP + nn] * rstd * norm_w[nn] * sg);
+            }
         }
     }
 }
@@ -310,14 +334,18 @@ size_t prepare_smem(int K) { return sizeof(float) * (kChunk * (K + 1) + 3 * kChu
 size_t chunk_h_smem(int K) {
     return sizeof(float) * (K * kBV + 2 * kChunk * (K + 1) + kChunk * (kBV + 1));
 }
-size_t chunk_o_smem(int K) { return sizeof(float) * (2 * kChunk * (K + 1) + kChunk * 65 + K * 65 + kChunk * 65); }
+size_t chunk_o_smem(int K, int V, bool normed) {
+    return sizeof(float) * (2 * kChunk * (K + 1) + kChunk * 65 + K * 65 + kChunk * 65 +
+                            (normed ? kChunk * (V + 1) : 0));
+}
 
 template <typename T>
 cudaError_t run(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Marks &m) {
     const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k),
             *v = static_cast<const T *>(a.v);
     cudaError_t e;
-    const size_t s1 = prepare_smem(a.K), s2 = chunk_h_smem(a.K), s3 = chunk_o_smem(a.K);
+    const size_t s1 = prepare_smem(a.K), s2 = chunk_h_smem(a.K),
+                 s3 = chunk_o_smem(a.K, a.V, a.gate != nullptr);
     if ((e = cudaFuncSetAttribute(wy_prepare_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(s1))) != cudaSuccess)
         return e;
@@ -340,7 +368,9 @@ cudaError_t run(const Args &a, const SimtWorkspace &ws, cudaStream_t s, const Ma
     if ((e = m.mark(2, s)) != cudaSuccess) return e;
     chunk_o_kernel<T><<<chunks, kThreads, s3, s>>>(q, k, a.g_chunk(), ws.h, ws.v_new, a.T, a.H, a.K,
                                                   a.V, a.NT, a.T_pad, a.scale,
-                                                  static_cast<T *>(a.o), a.flags);
+                                                  static_cast<T *>(a.o), a.flags,
+                                                  static_cast<const T *>(a.gate), a.norm_w,
+                                                  a.norm_eps);
     if ((e = m.mark(3, s)) != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -64,11 +64,17 @@ struct TcLayout {
     static constexpr uint32_t kVG = kVN + 8192;                  // v_g
     static constexpr uint32_t kG = kVG + 8192;                   // decay tables, 4 chunk slots
     static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
-    static constexpr uint32_t kBytes = kBar + 256;
+    // output stage: row sums of squares, [2 chunk slots][4 ranks x 2 halves][64 rows]
+    static constexpr uint32_t kRed = kBar + 256;
+    static constexpr uint32_t kBytes = kRed + 2 * 8 * 64 * 4;
 };
 
 // TMEM columns: X-region [X (64) | QK (64)], O (64), W (K), HT (K).
 constexpr uint32_t kColX = 0, kColQK = 64, kColO = 128, kColW = 192, kColHT = 320;
+// With the output stage O is double-buffered (chunk parity), the second copy
+// in the columns after HT, so that a chunk's normalisation can wait for the
+// cluster's row sums while the next chunk runs.
+constexpr uint32_t kColO2 = 448;
 
 struct Bars {
     uint64_t full[2], empty[2];                     // TMA stages
@@ -77,6 +83,7 @@ struct Bars {
     uint64_t w_ready;                               // w epilogue
     uint64_t xo_ready, vn_ready, hs_ready;          // chain group
     uint64_t drain;                                 // every MMA issued is done
+    uint64_t norm_bar[2];                           // output stage: row sums of the cluster
     uint32_t abort, tmem;
 };
 
@@ -85,6 +92,21 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+// wait_bar for a barrier completed by other CTAs of the cluster (acquire at
+// cluster scope).
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
+                                                 volatile uint32_t *abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kWaitNs) {
             *abort = 1;
@@ -125,15 +147,19 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
 }
 
-template <int K>
+// GATED: the output stage (gated RMSNorm over V) with the V tiles of a head as
+// one cluster of nrank_arg CTAs; without it the cluster code is compiled out.
+template <int K, bool GATED>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                     const float *__restrict__ g, const float *__restrict__ h0,
                     float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
                     float scale, int l2_prefetch, uint32_t *status, int l2norm,
-                    const float *__restrict__ rk) {
+                    const float *__restrict__ rk, const __nv_bfloat16 *__restrict__ gate,
+                    const float *__restrict__ norm_w, float norm_eps, int nrank_arg) {
     using Lay = TcLayout<K>;
+    const int nrank = GATED ? nrank_arg : 0;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so
@@ -182,6 +208,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_init(&bs->vn_ready, kChainThreads / 2);
         mbar_init(&bs->hs_ready, kChainThreads);
         mbar_init(&bs->drain, 1);
+        // output stage: one local arrival (with the expected bytes) per chunk;
+        // the row sums of every CTA of the cluster arrive as transactions
+        if (nrank)
+            for (int i = 0; i < 2; ++i) mbar_init(&bs->norm_bar[i], 1);
         bs->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
@@ -191,6 +221,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     tc_fence_before_sync();
     __syncthreads();
+    // With the output stage the V tiles of one head run as a cluster (rank =
+    // V tile); its barriers must be initialised before any CTA arrives on them.
+    if (nrank) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem = bs->tmem;
     const uint32_t s_base = smem_u32(sm);
@@ -228,9 +261,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // O += [P; .] v_new of chunk cp
             auto issue_pv = [&](int cp) {
                 const uint32_t vn = s_vn;
+                const uint32_t ocol = (GATED && (cp & 1)) ? kColO2 : kColO;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColO, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
+                    mma_bf16(tmem + ocol, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
                              smem_desc(vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, 1);
                 mma_commit(&bs->o_done);
             };
@@ -376,14 +410,16 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 float rq = 1.f;
                 if (l2norm) {
                     // |q_i|^2 from the stage's q tile (rows 0-63 of the stacked
-                    // operand; the swizzle only permutes 16-byte chunks in a row)
+                    // operand; the swizzle only permutes 16-byte chunks in a
+                    // row, and chunk j ^ (row % 8) keeps 8 rows on distinct banks)
                     const unsigned char *qrow = sm + s * Lay::kStage + Lay::kStAbig + ptid * 128;
                     float ss = 0.f;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(qrow + kb * 16384 + j * 16);
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qrow + kb * 16384 +
+                                                                             ((j ^ (ptid & 7)) * 16));
                             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -485,6 +521,77 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tc_fence_before_sync();
         mbar_arrive(&bs->hs_ready);
         bool ok = true;
+        // Output stage (gated RMSNorm over the head's V columns), in two parts
+        // per chunk so that the cluster exchange overlaps the next chunk:
+        // part 1, after o_done(c), sends this thread's sum of squares over its
+        // 32 columns to every CTA of the cluster (slot c % 2, entry rank * 2 +
+        // half) and prefetches the gate; part 2, after the next chunk's O seed,
+        // waits for all sums, reads O(c) again and writes the output. A slot is
+        // next written for chunk c + 2, which needs every thread of the
+        // cluster to have arrived for chunk c + 1, i.e. to have finished part 2
+        // of chunk c: neither the sums nor the barrier phase can be overtaken.
+        // The sums travel as asynchronous stores that complete bytes of the
+        // receiving CTA's barrier, so the sender needs no memory fence.
+        auto gated_send = [&](int c) {
+            const uint32_t ob = (c & 1) ? kColO2 : kColO;
+            float v0[16], v1[16];
+            tmem_ld16f(tmem + ob + lane_off + col0, v0);
+            tmem_ld16f(tmem + ob + lane_off + col0 + 16, v1);
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ss = fmaf(v0[e], v0[e], fmaf(v1[e], v1[e], ss));
+            const int tc0 = c * 64;
+            if (row < min(64, T - tc0))
+                prefetch_l2(gate + ((static_cast<int64_t>(b) * T + tc0 + row) * H + h) * V +
+                            vt * kTcBV + col0);
+            const int slot = c & 1;
+            const uint32_t red = s_base + Lay::kRed + ((slot * 8 + vt * 2 + hf) * 64 + row) * 4;
+            const uint32_t nb = smem_u32(&bs->norm_bar[slot]);
+            // this CTA expects one sum from each of the cluster's o-epilogue threads
+            if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&bs->norm_bar[slot], nrank * 128 * 4);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
+        };
+        auto gated_finish = [&](int c) -> bool {
+            const int slot = c & 1;
+            if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (c >> 1) & 1, abort))) return false;
+            const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 512;
+            float tot = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < 2 * nrank) tot += sums[i * 64 + row];
+            const float rstd = rsqrtf(tot / V + norm_eps);
+            const uint32_t ob = (c & 1) ? kColO2 : kColO;
+            float v0[16], v1[16];
+            tmem_ld16f(tmem + ob + lane_off + col0, v0);
+            tmem_ld16f(tmem + ob + lane_off + col0 + 16, v1);
+            const int tc0 = c * 64;
+            if (row < min(64, T - tc0)) {
+                const int64_t oi = ((static_cast<int64_t>(b) * T + tc0 + row) * H + h) * V +
+                                   vt * kTcBV + col0;
+                const float *wv = norm_w + vt * kTcBV + col0;
+                float y[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 zr = reinterpret_cast<const uint4 *>(gate + oi)[i];
+                    const uint32_t w4[4] = {zr.x, zr.y, zr.z, zr.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = i * 8 + 2 * e;
+                        const float z0 = __uint_as_float(w4[e] << 16);
+                        const float z1 = __uint_as_float(w4[e] & 0xffff0000u);
+                        const float o0 = j < 16 ? v0[j] : v1[j - 16];
+                        const float o1 = j + 1 < 16 ? v0[j + 1] : v1[j - 15];
+                        y[j] = o0 * rstd * wv[j] * __fdividef(1.f, 1.f + __expf(-z0));
+                        y[j + 1] = o1 * rstd * wv[j + 1] * __fdividef(1.f, 1.f + __expf(-z1));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) store_bf16x8_global(o + oi + i * 8, y + i * 8);
+            }
+            return true;
+        };
         float g_last_next = NT > 1 ? g_last_of(1) : 0.f;
         for (int c = 0; c < NT; ++c) {
             const int t0 = c * 64, n = min(64, T - t0), gs = c & 3;
@@ -536,6 +643,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tmem_st16(tmem + kColQK + lane_off + col0 + 16, z);
                 }
                 const float so = scale * eg_s[gs * 64 + row];
+                const uint32_t ocol = (GATED && (c & 1)) ? kColO2 : kColO;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     uint32_t r[16];
@@ -543,12 +651,14 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(so * __uint_as_float(r[e]));
-                    tmem_st16(tmem + kColO + lane_off + col0 + half * 16, r);
+                    tmem_st16(tmem + ocol + lane_off + col0 + half * 16, r);
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&bs->xo_ready);
+                // previous chunk's output stage, part 2, while this chunk's MMAs run
+                if (GATED && c >= 1 && !(ok = gated_finish(c - 1))) break;
             } else {
                 if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort)))) break;
                 const float gate = gate_s[gs * 64 + row];
@@ -596,19 +706,25 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (upper) {
                 if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort)))) break;
                 tc_fence_after_sync();
-                __nv_bfloat16 *dst = o + ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V +
-                                     vt * kTcBV + col0;
+                const int64_t oi = ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V +
+                                   vt * kTcBV + col0;
+                if (!nrank) {
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float v[16];
-                    tmem_ld16f(tmem + kColO + lane_off + col0 + half * 16, v);
-                    if (row < n) {
-                        store_bf16x8_global(dst + half * 16, v);
-                        store_bf16x8_global(dst + half * 16 + 8, v + 8);
+                    for (int half = 0; half < 2; ++half) {
+                        float v[16];
+                        tmem_ld16f(tmem + kColO + lane_off + col0 + half * 16, v);
+                        if (row < n) {
+                            store_bf16x8_global(o + oi + half * 16, v);
+                            store_bf16x8_global(o + oi + half * 16 + 8, v + 8);
+                        }
                     }
+                } else {
+                    gated_send(c);   // output stage, part 1
                 }
             }
         }
+        // output stage, part 2 of the last chunk
+        if (GATED && upper && warp_all(ok)) ok = gated_finish(NT - 1);
         // final state straight from tensor memory
         if (warp_all(ok) && h_final) {
             tc_fence_after_sync();
@@ -625,6 +741,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     tc_fence_before_sync();
     __syncthreads();
+    // no CTA of a cluster leaves while another may still write its shared memory
+    if (nrank) cluster_sync();
     if (tid == 0 && *abort) atomicOr(status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
@@ -652,17 +770,42 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
         !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
-    const int smem = static_cast<int>(TcLayout<K>::kBytes + 1024);
-    cudaError_t e = cudaFuncSetAttribute(gdn_fused_tc_kernel<K>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the row-sum region at the end is only used (and only allocated) with the output stage
+    const int smem = static_cast<int>((a.gate ? TcLayout<K>::kBytes : TcLayout<K>::kRed) + 1024);
+    const auto kernel = a.gate ? gdn_fused_tc_kernel<K, true> : gdn_fused_tc_kernel<K, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(a.V / kTcBV) * a.H * a.B;
-    gdn_fused_tc_kernel<K><<<dim3(a.V / kTcBV, a.H, a.B), kTcThreads, smem, s>>>(
-        mq, mk, mv, ma, a.g_chunk(), a.h0, a.h_final, static_cast<__nv_bfloat16 *>(a.o), a.T, a.H,
-        a.V, a.scale, ctas <= sms ? 1 : 0, a.status, (a.flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, a.rk);
+    const int nrank = a.gate ? a.V / kTcBV : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.V / kTcBV, a.H, a.B);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nrank;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = nrank ? 1 : 0;
+    // kernel arguments, in order, for the untyped launch call
+    const float *g_arg = a.g_chunk(), *h0_arg = a.h0, *rk_arg = a.rk, *nw_arg = a.norm_w;
+    float *hf_arg = a.h_final;
+    __nv_bfloat16 *o_arg = static_cast<__nv_bfloat16 *>(a.o);
+    const __nv_bfloat16 *gate_arg = static_cast<const __nv_bfloat16 *>(a.gate);
+    int T_arg = a.T, H_arg = a.H, V_arg = a.V, pf_arg = ctas <= sms ? 1 : 0;
+    int norm_arg = (a.flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, nrank_arg = nrank;
+    float scale_arg = a.scale, eps_arg = a.norm_eps;
+    uint32_t *status_arg = a.status;
+    void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
+                    &scale_arg, &pf_arg, &status_arg, &norm_arg, &rk_arg, &gate_arg, &nw_arg,
+                    &eps_arg, &nrank_arg};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

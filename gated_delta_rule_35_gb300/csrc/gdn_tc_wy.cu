@@ -182,14 +182,17 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (__syncthreads_or(fail)) goto done;
     mma_issue(128, s_k, s_k, false, K / 16);
     if (l2norm && tid < 64) {
-        // |k_i|^2 from the k tile while the Gram runs (the swizzle permutes the
-        // 16-byte chunks within a row, which a sum of squares does not see)
+        // |k_i|^2 from the k tile while the Gram runs. The 128-byte swizzle
+        // permutes the 16-byte chunks within a row, which a sum of squares does
+        // not see; visiting chunk j ^ (row % 8) keeps 8 consecutive rows on
+        // different banks.
         float ss = 0.f;
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(sm + Lay::kK + kb * 8192 + tid * 128 + j * 16);
+                const uint4 u = *reinterpret_cast<const uint4 *>(sm + Lay::kK + kb * 8192 + tid * 128 +
+                                                                 ((j ^ (tid & 7)) * 16));
                 const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {

@@ -73,6 +73,50 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     return true;
 }
 
+// Brings the line holding `p` into L2 ahead of a later load.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `saddr` (this CTA's shared address) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster that
+// completes 4 bytes of the transaction count of `cbar` (an mbarrier in that
+// same CTA) once the data is there: no fence is needed on the sending side.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t caddr, float v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+                 "r"(__float_as_uint(v)), "r"(cbar)
+                 : "memory");
+}
+// mbar_try_wait with acquire at cluster scope (the waiter may be suspended).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+// Every thread of every CTA of the cluster; orders earlier shared-memory
+// accesses (including remote ones) before later ones.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tcgen05.mma operands, TMA stores).

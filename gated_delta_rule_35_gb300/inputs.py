@@ -127,6 +127,15 @@ def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", 
     }
 
 
+def make_output_norm(B: int, T: int, H: int, V: int, *, dtype: str = "bf16", seed: int = 0):
+    """Gate [B,T,H,V] ~ N(0,1) in the I/O dtype and norm weight [V] ~ 1 + 0.1 N(0,1)
+    fp32, the extra inputs of the gated RMSNorm output stage (own generator)."""
+    gen = torch.Generator("cpu").manual_seed(seed + 7919)
+    gate = torch.randn(B, T, H, V, generator=gen).to(TORCH_DTYPE[dtype]).contiguous()
+    weight = (1.0 + 0.1 * torch.randn(V, generator=gen)).contiguous()
+    return gate, weight
+
+
 def make_workload(name: str, **overrides) -> dict:
     """Inputs of a named workload; ``overrides`` may change B/T/H (e.g. a sample)."""
     w = WORKLOADS[name] if name in WORKLOADS else DECODE_WORKLOADS[name]

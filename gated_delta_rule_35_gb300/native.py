@@ -25,7 +25,7 @@ CHUNK = 64
 EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stages",
            "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
            "gdn_chunk_fwd_noalloc", "gdn_decode_step", "gdn_decode_step_launches",
-           "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_ex", "gdn_decode_step_ex", "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -38,6 +38,11 @@ class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("algo", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class OutputNorm(ctypes.Structure):
+    """gdn_output_norm: gated RMSNorm of the output rows."""
+    _fields_ = [("gate", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("eps", ctypes.c_float)]
 
 
 class StageExports(ctypes.Structure):
@@ -72,6 +77,13 @@ def lib():
                                                         ctypes.c_int32, vp]
         L.gdn_check_device_status.restype = ctypes.c_int
         L.gdn_check_device_status.argtypes = [vp, vp]
+        L.gdn_chunk_fwd_ex.restype = ctypes.c_int
+        L.gdn_chunk_fwd_ex.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                       ctypes.POINTER(OutputNorm), vp, vp, vp, sz,
+                                       ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32, vp]
+        L.gdn_decode_step_ex.restype = ctypes.c_int
+        L.gdn_decode_step_ex.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                         ctypes.POINTER(OutputNorm), vp, vp]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         L.gdn_decode_step_launches.restype = ctypes.c_int32
@@ -136,17 +148,37 @@ def _check_inputs(q, k, v, g, beta, h0):
     return B, T, H, K, V
 
 
+def _output_norm(gate, weight, eps, shape, like):
+    if gate is None and weight is None:
+        return None
+    if gate is None or weight is None:
+        raise ValueError("the output stage needs both gate and norm_weight")
+    if gate.shape != shape or gate.dtype != like.dtype or not gate.is_contiguous() \
+            or gate.device != like.device:
+        raise ValueError(f"gate must be contiguous {tuple(shape)} in the input dtype")
+    if weight.shape != (shape[-1],) or weight.dtype != torch.float32 or not weight.is_contiguous() \
+            or weight.device != like.device:
+        raise ValueError("norm_weight must be contiguous float32 [V]")
+    return OutputNorm(ctypes.c_void_p(gate.data_ptr()), ctypes.c_void_p(weight.data_ptr()),
+                      float(eps))
+
+
 def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
               algo: str = "auto", workspace=None, out=None, final_state=None, stream=None,
-              events=None, raw_g: bool = False, qk_l2norm: bool = False):
+              events=None, raw_g: bool = False, qk_l2norm: bool = False, gate=None,
+              norm_weight=None, norm_eps: float = 1e-6):
     """Chunked gated-delta-rule forward on CUDA tensors. Returns (o, h_final or None).
 
     q, k [B,T,H,K] and v [B,T,H,V] (float32 or bfloat16), g and beta [B,T,H]
     float32 (g: chunk-local cumulative log-decay), h0 [B,H,K,V] float32 or None.
     ``workspace``/``out``/``final_state`` may be passed to reuse buffers.
     ``raw_g``: g holds per-token log decays, summed per chunk in the kernels;
-    ``qk_l2norm``: q and k rows are L2-normalised in the kernels (eps 1e-6)."""
+    ``qk_l2norm``: q and k rows are L2-normalised in the kernels (eps 1e-6).
+    ``gate`` [B,T,H,V] (q's dtype) with ``norm_weight`` [V] float32: the output
+    rows pass through the gated RMSNorm o * rsqrt(mean o^2 + norm_eps) *
+    norm_weight * sigmoid(gate) before their rounding."""
     B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
+    norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)
     p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
     need = workspace_bytes(p)
     if need == 0:
@@ -161,7 +193,12 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
             _ptr(h0), _ptr(o), _ptr(hf), _ptr(workspace), workspace.numel())
-    if events is None:
+    if norm is not None:
+        arr = None if events is None else (ctypes.c_void_p * len(events))(*events)
+        st = lib().gdn_chunk_fwd_ex(*args[:8], ctypes.byref(norm), *args[8:], arr,
+                                    0 if events is None else len(events),
+                                    ctypes.c_void_p(s.cuda_stream))
+    elif events is None:
         st = lib().gdn_chunk_fwd(*args, ctypes.c_void_p(s.cuda_stream))
     else:
         # events: raw cudaEvent_t handles (ints); markers between the kernels
@@ -206,7 +243,8 @@ def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = 
 
 
 def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None, out=None,
-                stream=None, qk_l2norm: bool = False):
+                stream=None, qk_l2norm: bool = False, gate=None, norm_weight=None,
+                norm_eps: float = 1e-6):
     """Recurrent step(s) of the rule on CUDA tensors: advances every sequence by
     its T tokens and returns (o, state_out).
 
@@ -215,7 +253,8 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
     state [B,H,K,V] float32 (an h_final of chunk_fwd). ``state_out=None``
     updates ``state`` in place; pass ``state_out=state`` for the same, or
     another buffer to keep ``state``. ``qk_l2norm`` normalises the q and k
-    rows in the kernel (eps 1e-6)."""
+    rows in the kernel (eps 1e-6); ``gate``/``norm_weight`` add the output
+    stage as in chunk_fwd."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     dev = q.device
@@ -238,9 +277,11 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
     o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
     p = problem(B, T, H, K, V, q.dtype, "auto", flags_of(False, qk_l2norm))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = lib().gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
-                               _ptr(beta), float(scale), _ptr(state), _ptr(so), _ptr(o),
-                               ctypes.c_void_p(s.cuda_stream))
+    norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)
+    st = lib().gdn_decode_step_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                  _ptr(beta), float(scale), _ptr(state), _ptr(so),
+                                  None if norm is None else ctypes.byref(norm), _ptr(o),
+                                  ctypes.c_void_p(s.cuda_stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_step")
     return o, so

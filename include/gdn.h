@@ -229,6 +229,41 @@ GDN_API gdn_status gdn_decode_step(const gdn_problem *p,
 GDN_API int32_t gdn_decode_step_launches(const gdn_problem *p, const char **names,
                                          int32_t max_names);
 
+/* Output stage (optional): the gated RMSNorm that a Gated DeltaNet layer applies
+ * to the rule's output (the output stage of the "KdaSplit" decode kernel page:
+ * root of the mean square over the head's channels plus eps, norm weight, and
+ * the token's gate through a sigmoid). Each row o_t of one token and head
+ * (V values) becomes
+ *     o_t[v] * rsqrt(mean_u o_t[u]^2 + eps) * weight[v] * sigmoid(gate_t[v]),
+ * formed from the fp32 o before its one rounding to the output dtype. */
+typedef struct {
+    const void *gate;      /* [B,T,H,V] in p->dtype, required, 16-byte aligned */
+    const float *weight;   /* [V] fp32, required, 16-byte aligned */
+    float eps;             /* >= 0 */
+} gdn_output_norm;
+
+/* gdn_chunk_fwd with the optional output stage (norm == NULL: the plain o of
+ * gdn_chunk_fwd) and optional timing markers as in gdn_chunk_fwd_profiled
+ * (events == NULL: none). The tensor-core path runs the CTAs of one head's V
+ * tiles as a thread-block cluster to share the row sums; every other contract
+ * is gdn_chunk_fwd's. */
+GDN_API gdn_status gdn_chunk_fwd_ex(const gdn_problem *p,
+                                    const void *q, const void *k, const void *v,
+                                    const float *g, const float *beta, float scale,
+                                    const float *h0, const gdn_output_norm *norm,
+                                    void *o, float *h_final,
+                                    void *workspace, size_t workspace_bytes,
+                                    void *const *events, int32_t n_events, void *stream);
+
+/* gdn_decode_step with the optional output stage (norm == NULL: plain o).
+ * With it, one CTA holds a head's whole [K, V] state, so K * V <= 32768
+ * (else GDN_ERR_UNSUPPORTED). */
+GDN_API gdn_status gdn_decode_step_ex(const gdn_problem *p,
+                                      const void *q, const void *k, const void *v,
+                                      const float *gamma, const float *beta, float scale,
+                                      const float *state_in, float *state_out,
+                                      const gdn_output_norm *norm, void *o, void *stream);
+
 /* Static description of a status code. Never NULL. */
 GDN_API const char *gdn_status_string(gdn_status s);
 

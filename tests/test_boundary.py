@@ -149,3 +149,30 @@ def test_flags_validated():
     assert _call(bad) == native.GDN_ERR_INVALID_ARG
     assert _decode(native.problem(1, 1, 1, 64, 64, native.GDN_BF16, "auto", 8)) == \
         native.GDN_ERR_INVALID_ARG
+
+
+def test_output_norm_validated():
+    p = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "auto")
+    vp = ctypes.c_void_p
+    lib = native.lib()
+
+    def fwd(norm):
+        return lib.gdn_chunk_fwd_ex(ctypes.byref(p), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                    vp(FAKE), 1.0, None, ctypes.byref(norm), vp(FAKE), None,
+                                    vp(FAKE), 1 << 40, None, 0, None)
+
+    assert fwd(native.OutputNorm(None, FAKE, 1e-6)) == native.GDN_ERR_INVALID_ARG
+    assert fwd(native.OutputNorm(FAKE, None, 1e-6)) == native.GDN_ERR_INVALID_ARG
+    assert fwd(native.OutputNorm(FAKE, FAKE, -1.0)) == native.GDN_ERR_INVALID_ARG
+    assert fwd(native.OutputNorm(FAKE + 8, FAKE, 1e-6)) == native.GDN_ERR_ALIGNMENT
+
+    def dec(K, V, norm):
+        q = native.problem(2, 1, 3, K, V, native.GDN_BF16, "auto")
+        return lib.gdn_decode_step_ex(ctypes.byref(q), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                      vp(FAKE), 1.0, vp(FAKE), vp(FAKE), ctypes.byref(norm),
+                                      vp(FAKE), None)
+
+    ok = native.OutputNorm(FAKE, FAKE, 1e-6)
+    assert dec(128, 48, ok) == native.GDN_ERR_UNSUPPORTED     # V not a slice width
+    assert dec(256, 256, ok) == native.GDN_ERR_UNSUPPORTED    # K V > 32768
+    assert dec(128, 128, native.OutputNorm(None, FAKE, 1e-6)) == native.GDN_ERR_INVALID_ARG

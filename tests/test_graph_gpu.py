@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from gated_delta_rule_35_gb300 import chunk_fwd, decode_step, native
-from gated_delta_rule_35_gb300.inputs import make_inputs
+from gated_delta_rule_35_gb300.inputs import make_inputs, make_output_norm
 
 pytestmark = pytest.mark.gpu
 
@@ -49,24 +49,30 @@ def test_decode_steps_replay_from_a_graph():
 
 
 @pytest.mark.parametrize("algo", ["simt", "tc"])
-def test_chunk_fwd_replays_from_a_graph(algo):
+@pytest.mark.parametrize("gated", [False, True])
+def test_chunk_fwd_replays_from_a_graph(algo, gated):
+    """With the output stage the tensor-core path is a cluster launch."""
     B, T, H, K, V = 2, 200, 4, 128, 128
     p = native.problem(B, T, H, K, V, torch.bfloat16, algo)
     if native.workspace_bytes(p) == 0:
         pytest.skip(f"{algo} not built")
     x = gpu(make_inputs(B, T, H, K, V, dtype="bf16", seed=52, h0_std=0.1))
     args = (x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, x["h0"])
-    o_e, hf_e = chunk_fwd(*args, algo=algo)
+    kw = {}
+    if gated:
+        gate, weight = make_output_norm(B, T, H, V, seed=52)
+        kw = dict(gate=gate.cuda(), norm_weight=weight.cuda())
+    o_e, hf_e = chunk_fwd(*args, algo=algo, **kw)
     ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
     o = torch.empty_like(o_e)
     hf = torch.empty_like(hf_e)
-    chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf)   # warm-up
+    chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf, **kw)   # warm-up
     torch.cuda.synchronize()
     o.fill_(float("nan"))
     hf.fill_(float("nan"))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf)
+        chunk_fwd(*args, algo=algo, workspace=ws, out=o, final_state=hf, **kw)
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o, o_e) and torch.equal(hf, hf_e)

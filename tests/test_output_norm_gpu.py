@@ -1,0 +1,116 @@
+"""The gated RMSNorm output stage against the fp64 oracle (recurrence, then
+``oracle.epilogue.gated_rmsnorm``), element by element, on both chunked paths
+and the decode step. Tolerances are the plain path's (relative Frobenius 1e-4
+fp32, 2e-2 bf16; decode 1e-5 fp32 and 2.5e-3 bf16, its state 1e-5): the stage
+is formed in fp32 from the same o before its one rounding."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import epilogue, frontend, recurrence
+from tests.pins import rel
+from gated_delta_rule_35_gb300 import chunk_fwd, decode_step, native
+from gated_delta_rule_35_gb300.inputs import make_inputs, make_output_norm, to_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+EPS = 1e-6
+
+
+def have_algo(algo, K, V, dtype):
+    return native.workspace_bytes(native.problem(1, 64, 1, K, V, TORCH[dtype], algo)) > 0
+
+
+def gpu(x):
+    return {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+
+
+def oracle(x, gate, weight, scale=1.0, raw_g=False, l2norm=False, chunk=64):
+    q, k, g = frontend.prepare(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["g"]), raw_g=raw_g,
+                               qk_l2norm=l2norm)
+    o, hf = recurrence.forward(q, k, to_f64(x["v"]), g, to_f64(x["beta"]), scale,
+                               to_f64(x["h0"]), chunk=chunk)
+    return epilogue.gated_rmsnorm(o, to_f64(gate), to_f64(weight), EPS), hf
+
+
+@pytest.mark.parametrize("algo", ["simt", "tc"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 256), (64, 192)])
+@pytest.mark.parametrize("T", [1, 64, 65, 200])
+def test_chunked_output_norm(algo, dtype, K, V, T):
+    if not have_algo(algo, K, V, dtype):
+        pytest.skip(f"{algo} not built for K={K} V={V} {dtype}")
+    B, H = 2, 3
+    seed = 500 + T + K + V
+    x = make_inputs(B, T, H, K, V, dtype=dtype, seed=seed, h0_std=0.1)
+    gate, weight = make_output_norm(B, T, H, V, dtype=dtype, seed=seed)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=algo,
+                      gate=gate.cuda(), norm_weight=weight.cuda(), norm_eps=EPS)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, gate, weight)
+    o, hf = o.float().cpu().numpy(), hf.cpu().numpy()
+    assert np.isfinite(o).all()
+    assert rel(o, o_ref) < TOL[dtype], rel(o, o_ref)
+    assert rel(hf, hf_ref) < TOL[dtype], rel(hf, hf_ref)
+
+
+@pytest.mark.parametrize("algo", ["simt", "tc"])
+def test_front_end_and_output_stage_together(algo):
+    """Raw g, unnormalised q and k, and the gated RMSNorm in one call."""
+    if not have_algo(algo, 128, 128, "bf16"):
+        pytest.skip("not built")
+    B, T, H, K, V = 2, 150, 2, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=61, h0_std=0.1, raw=True)
+    gate, weight = make_output_norm(B, T, H, V, seed=61)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], K ** -0.5, d["h0"], algo=algo,
+                      raw_g=True, qk_l2norm=True, gate=gate.cuda(), norm_weight=weight.cuda(),
+                      norm_eps=EPS)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, gate, weight, K ** -0.5, raw_g=True, l2norm=True)
+    assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+
+
+def test_output_norm_full_size_sampled():
+    """The default workload's shape with the output stage through 'auto' (the
+    tensor-core path with two-CTA clusters), on sampled sequences."""
+    B, T, H, K, V = 4, 2048, 16, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=1)
+    gate, weight = make_output_norm(B, T, H, V, seed=1)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None, gate=gate.cuda(),
+                      norm_weight=weight.cuda(), norm_eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    for b, h in [(0, 0), (3, 15), (1, 9)]:
+        sub = {n: x[n][b:b + 1, :, h:h + 1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+        sub["h0"] = None
+        o_ref, hf_ref = oracle(sub, gate[b:b + 1, :, h:h + 1], weight)
+        assert rel(o[b:b + 1, :, h:h + 1].float().cpu().numpy(), o_ref) < TOL["bf16"], (b, h)
+        assert rel(hf[b:b + 1, h:h + 1].cpu().numpy(), hf_ref) < TOL["bf16"], (b, h)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(3, 2, 4, 128, 128), (2, 1, 5, 64, 64), (1, 3, 2, 128, 256),
+                                   (4, 1, 2, 64, 16)])
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_decode_output_norm(dtype, shape, l2norm):
+    B, T, H, K, V = shape
+    x = make_inputs(B, T, H, K, V, dtype=dtype, seed=B * 7 + T + V, h0_std=0.1, raw=l2norm,
+                    chunk=1)
+    gate, weight = make_output_norm(B, T, H, V, dtype=dtype, seed=B + V)
+    s0 = x["h0"]
+    d = gpu(x)
+    state = s0.cuda()
+    scale = K ** -0.5 if l2norm else 1.0
+    o, s1 = decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale,
+                        qk_l2norm=l2norm, gate=gate.cuda(), norm_weight=weight.cuda(),
+                        norm_eps=EPS)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle(x, gate, weight, scale, l2norm=l2norm, chunk=1)
+    assert rel(o.float().cpu().numpy(), o_ref) < (1e-5 if dtype == "f32" else 2.5e-3)
+    assert rel(s1.cpu().numpy(), s_ref) < 1e-5
