@@ -26,9 +26,15 @@
  * consume), so gamma_t = g_t - g_{t-1} inside a chunk and gamma_t = g_t at the
  * first token of a chunk. The difference of two fp32 values is exact in fp64.
  *
- * Layout: q, k [B,T,H,K]; v, o [B,T,H,V]; g, beta [B,T,H]; h0, h_final
- * [B,H,K,V]; all fp64, contiguous. h0 may be NULL (zero state), h_final may be
- * NULL (not written).
+ * Per-channel decay (the KDA variant: the decay is a K-vector, one factor per
+ * row of S, as in the "KdaSplit" decode kernel page, where each state row is
+ * scaled by its own decay before the read): with per_channel set, g is
+ * [B,T,H,K], gamma_t is a K-vector read from g the same way, and the decay
+ * step is S[i, :] <- exp(gamma_t[i]) * S[i, :]. Everything else is unchanged.
+ *
+ * Layout: q, k [B,T,H,K]; v, o [B,T,H,V]; g, beta [B,T,H] (g [B,T,H,K] with
+ * per_channel); h0, h_final [B,H,K,V]; all fp64, contiguous. h0 may be NULL
+ * (zero state), h_final may be NULL (not written).
  *
  * Optional exports (NULL = not written), used to check the stages of a chunked
  * implementation against the recurrence:
@@ -44,7 +50,7 @@
 #include <string.h>
 
 typedef struct {
-    int B, T, H, K, V, chunk;
+    int B, T, H, K, V, chunk, per_channel;
     const double *q, *k, *v, *g, *beta;
     double scale;
     const double *h0;
@@ -67,9 +73,6 @@ static void run_sequence(const job_t *j, int b, int h, double *S, double *d)
         const double *qt = j->q + row * K;
         const double *kt = j->k + row * K;
         const double *vt = j->v + row * V;
-        const double gt = j->g[row];
-        const double gamma = (t % j->chunk == 0) ? gt : gt - j->g[row - H];
-        const double a = exp(gamma);
         const double bt = j->beta[row];
 
         if (j->h_chunks && t % j->chunk == 0) {
@@ -77,8 +80,25 @@ static void run_sequence(const job_t *j, int b, int h, double *S, double *d)
             const size_t slot = ((size_t)b * NT + t / j->chunk) * H + h;
             memcpy(j->h_chunks + slot * kv, S, kv * sizeof(double));
         }
-        for (size_t e = 0; e < kv; ++e)
-            S[e] *= a;
+        if (!j->per_channel) {
+            const double gt = j->g[row];
+            const double gamma = (t % j->chunk == 0) ? gt : gt - j->g[row - H];
+            const double a = exp(gamma);
+            for (size_t e = 0; e < kv; ++e)
+                S[e] *= a;
+        } else {
+            /* row i of S decays by its own channel's factor */
+            const double *gk = j->g + row * K;
+            for (int i = 0; i < K; ++i) {
+                /* inside a chunk: minus the same channel of token t - 1 (row - H) */
+                const double gamma_i =
+                    (t % j->chunk == 0) ? gk[i] : gk[i] - j->g[(row - H) * K + i];
+                const double ai = exp(gamma_i);
+                double *Si = S + (size_t)i * V;
+                for (int c = 0; c < V; ++c)
+                    Si[c] *= ai;
+            }
+        }
         for (int c = 0; c < V; ++c) {
             double r = 0.0;
             for (int i = 0; i < K; ++i)
@@ -124,7 +144,7 @@ static void *worker(void *arg)
 
 /* Returns 0 on success, 1 on bad arguments, 2 on host allocation failure.
  * Sequences whose thread could not be started run on the calling thread. */
-int gdn_oracle_forward_ex(int B, int T, int H, int K, int V, int chunk,
+int gdn_oracle_forward_pc(int B, int T, int H, int K, int V, int chunk, int per_channel,
                           const double *q, const double *k, const double *v,
                           const double *g, const double *beta, double scale,
                           const double *h0, double *o, double *h_final,
@@ -149,6 +169,7 @@ int gdn_oracle_forward_ex(int B, int T, int H, int K, int V, int chunk,
     for (int i = 0; i < nthreads; ++i) {
         job_t *j = &jobs[i];
         j->B = B; j->T = T; j->H = H; j->K = K; j->V = V; j->chunk = chunk;
+        j->per_channel = per_channel;
         j->q = q; j->k = k; j->v = v; j->g = g; j->beta = beta; j->scale = scale;
         j->h0 = h0; j->o = o; j->h_final = h_final;
         j->h_chunks = h_chunks; j->delta = delta;
@@ -169,6 +190,16 @@ int gdn_oracle_forward_ex(int B, int T, int H, int K, int V, int chunk,
     free(jobs);
     free(th);
     return rc;
+}
+
+int gdn_oracle_forward_ex(int B, int T, int H, int K, int V, int chunk,
+                          const double *q, const double *k, const double *v,
+                          const double *g, const double *beta, double scale,
+                          const double *h0, double *o, double *h_final,
+                          double *h_chunks, double *delta, int nthreads)
+{
+    return gdn_oracle_forward_pc(B, T, H, K, V, chunk, 0, q, k, v, g, beta, scale, h0, o,
+                                 h_final, h_chunks, delta, nthreads);
 }
 
 int gdn_oracle_forward(int B, int T, int H, int K, int V, int chunk,

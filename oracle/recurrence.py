@@ -44,8 +44,8 @@ def load(path: Path | None = None):
 
 def _bind(lib):
     dp = ctypes.POINTER(ctypes.c_double)
-    lib.gdn_oracle_forward_ex.restype = ctypes.c_int
-    lib.gdn_oracle_forward_ex.argtypes = [ctypes.c_int] * 6 + [dp] * 5 + [ctypes.c_double] + \
+    lib.gdn_oracle_forward_pc.restype = ctypes.c_int
+    lib.gdn_oracle_forward_pc.argtypes = [ctypes.c_int] * 7 + [dp] * 5 + [ctypes.c_double] + \
         [dp] * 5 + [ctypes.c_int]
     return lib
 
@@ -67,12 +67,14 @@ def default_threads() -> int:
 def forward(q, k, v, g, beta, scale=1.0, h0=None, *, chunk: int = 64, nthreads: int | None = None,
             lib=None, stages: bool = False):
     """Token-by-token fp64 recurrence. Arrays in [B,T,H,*] layout; returns (o, h_final),
-    or with ``stages`` (o, h_final, h_chunks [B,NT,H,K,V], delta [B,T,H,V])."""
+    or with ``stages`` (o, h_final, h_chunks [B,NT,H,K,V], delta [B,T,H,V]).
+    g [B,T,H] is the scalar decay; g [B,T,H,K] is the per-channel (KDA) decay."""
     q, k, v, g, beta, h0 = map(_f64, (q, k, v, g, beta, h0))
     B, T, H, K = q.shape
     V = v.shape[-1]
+    per_channel = g.ndim == 4
     assert k.shape == (B, T, H, K) and v.shape == (B, T, H, V)
-    assert g.shape == (B, T, H) and beta.shape == (B, T, H)
+    assert g.shape == ((B, T, H, K) if per_channel else (B, T, H)) and beta.shape == (B, T, H)
     assert h0 is None or h0.shape == (B, H, K, V)
     o = np.zeros((B, T, H, V))
     hf = np.zeros((B, H, K, V))
@@ -81,7 +83,8 @@ def forward(q, k, v, g, beta, scale=1.0, h0=None, *, chunk: int = 64, nthreads: 
         hc = np.zeros((B, (T + chunk - 1) // chunk, H, K, V))
         dl = np.zeros((B, T, H, V))
     lib = lib or load()
-    rc = lib.gdn_oracle_forward_ex(B, T, H, K, V, chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+    rc = lib.gdn_oracle_forward_pc(B, T, H, K, V, chunk, int(per_channel), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(g),
                                    _ptr(beta), float(scale), _ptr(h0), _ptr(o), _ptr(hf),
                                    _ptr(hc), _ptr(dl), int(nthreads or default_threads()))
     if rc != 0:
