@@ -20,7 +20,8 @@ HBM roofline of reading and writing the fp32 state once (--no-decode skips it);
 "frontend": the same step on raw inputs with the chunk-local cumsum of g
 and the q/k L2 norm done in the kernels (--no-frontend skips it); and
 "output_norm": the same step with the gated RMSNorm output stage
-(--no-output-norm skips it).
+(--no-output-norm skips it); "per_channel": the chunked step and the decode
+step with per-channel (KDA) decay (--no-per-channel skips it).
 """
 from __future__ import annotations
 
@@ -443,6 +444,61 @@ def bench_output_norm(args, w, world, dev, flush, d):
             "inputs": "gate N(0,1) in the I/O dtype, norm weight 1 + 0.1 N(0,1), eps 1e-6"}
 
 
+def bench_per_channel(args, w, world, dev, flush):
+    """Per-channel (KDA) decay: the chunked step on the same shape (one decay per
+    key channel, CUDA-core pipeline) and the decode step on the decode workload
+    with a per-channel gamma [B,T,H,K]."""
+    from gated_delta_rule_35_gb300 import chunk_fwd, decode_step, native
+
+    x = make_inputs(w.B, w.T, w.H, w.K, w.V, dtype=w.dtype, seed=w.seed, h0_std=w.h0_std,
+                    per_channel=True)
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    flags = native.flags_of(per_channel=True)
+    p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, "auto", flags)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, n, flush_each):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for _ in range(args.warmup):
+            if flush_each:
+                flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            if flush_each:
+                flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n / 1e3, world, dev)
+
+    t_chunk = timed(lambda: chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"],
+                                      workspace=ws, stream=stream, per_channel_decay=True),
+                    max(5, min(args.steps, 20)), True)
+    wd = DECODE_WORKLOADS[DECODE_WORKLOAD]
+    y = make_inputs(wd.B, wd.T, wd.H, wd.K, wd.V, dtype=wd.dtype, seed=wd.seed, h0_std=wd.h0_std,
+                    chunk=1, per_channel=True)
+    dy = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in y.items()}
+    o = torch.empty((wd.B, wd.T, wd.H, wd.V), dtype=dy["q"].dtype, device=dev)
+    t_dec = timed(lambda: decode_step(dy["q"], dy["k"], dy["v"], dy["g"], dy["beta"], dy["h0"],
+                                      1.0, out=o, stream=stream, per_channel_decay=True),
+                  max(10, min(args.steps, 100)), False)
+    heads = wd.B * wd.H
+    es = DSIZE[wd.dtype]
+    nbytes = heads * wd.K * wd.V * 8 + heads * wd.T * ((2 * wd.K + 2 * wd.V) * es + 4 * wd.K + 4)
+    peaks = load_peaks()
+    return {"chunked": {"workload": w.name + "_per_channel", "ms_per_step": 1e3 * t_chunk,
+                        "tokens_per_s": w.B * w.T * world / t_chunk, "kernels": native.launches(p)},
+            "decode": {"workload": wd.name + "_per_channel", "ms_per_call": 1e3 * t_dec,
+                       "algorithmic_bytes_per_call": nbytes,
+                       "roofline": {"bound": "hbm", "achieved": nbytes / t_dec / 1e9,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": nbytes / t_dec / 1e9 / peaks["hbm_gbs"]}}}
+
+
 def bench_decode(args, world, dev):
     """The decode step on its own workload: one token for each of B*H heads, the
     state [B,H,K,V] fp32 read and written in place once per call. The state
@@ -599,6 +655,7 @@ def bench_ours(args, w, world, rank, local):
     dec = None if args.no_decode else bench_decode(args, world, dev)
     fe = None if args.no_frontend else bench_frontend(args, w, world, dev, flush)
     on = None if args.no_output_norm else bench_output_norm(args, w, world, dev, flush, d)
+    pcd = None if args.no_per_channel else bench_per_channel(args, w, world, dev, flush)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -616,7 +673,7 @@ def bench_ours(args, w, world, rank, local):
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
             "kernels": kernels,
             "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
-            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe, "output_norm": on,
+            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe, "output_norm": on, "per_channel": pcd,
         }
         print(json.dumps(line), flush=True)
 
@@ -635,6 +692,8 @@ def main():
                     help="skip the in-kernel front-end measurement")
     ap.add_argument("--no-output-norm", action="store_true",
                     help="skip the gated RMSNorm output-stage measurement")
+    ap.add_argument("--no-per-channel", action="store_true",
+                    help="skip the per-channel (KDA) decay measurements")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="target CPU time of the oracle baseline sample")
     args = ap.parse_args()

@@ -15,7 +15,9 @@ gdn_status check_problem(const gdn_problem *p) {
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
-    if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+    if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
+    if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && p->algo == GDN_ALGO_TC)
+        return GDN_ERR_UNSUPPORTED;   // per-channel decay runs on the SIMT pipeline
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
     if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
     // Every index is computed in 64 bits; B*T*H rows must still fit a grid.
@@ -28,13 +30,19 @@ gdn_status check_problem(const gdn_problem *p) {
 
 gdn_algo resolve_algo(const gdn_problem *p) {
     if (p->algo != GDN_ALGO_AUTO) return static_cast<gdn_algo>(p->algo);
+    if (p->flags & GDN_FLAG_PER_CHANNEL_DECAY) return GDN_ALGO_SIMT;
     return tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)) ? GDN_ALGO_TC
                                                                        : GDN_ALGO_SIMT;
 }
 
-// Front-end region: g_cum and rk, one fp32 per token-head each.
+// Front-end region: g_cum (one fp32 per token-head, or per token-head-channel
+// with per-channel decay) and rk (one per token-head).
+size_t g_cum_bytes(const gdn_problem *p) {
+    const size_t per = (p->flags & GDN_FLAG_PER_CHANNEL_DECAY) ? p->K : 1;
+    return align_up(static_cast<size_t>(p->B) * p->T * p->H * per * sizeof(float));
+}
 size_t front_bytes(const gdn_problem *p) {
-    return 2 * align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
+    return g_cum_bytes(p) + align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
 }
 
 size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
@@ -79,9 +87,8 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         a.norm_eps = norm->eps;
     }
     char *front = static_cast<char *>(workspace) + kStatusBytes;
-    const size_t plane = align_up(static_cast<size_t>(p->B) * p->T * p->H * sizeof(float));
     a.g_cum = reinterpret_cast<float *>(front);
-    a.rk = reinterpret_cast<float *>(front + plane);
+    a.rk = reinterpret_cast<float *>(front + g_cum_bytes(p));
     void *body = empty ? front : front + front_bytes(p);
 
     cudaError_t e;

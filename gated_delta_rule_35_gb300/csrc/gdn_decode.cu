@@ -20,6 +20,10 @@
 //
 // With the output stage (gated RMSNorm over V) one CTA holds a head's whole
 // state (VS = V), so the row's mean square is a sum inside the CTA.
+//
+// With per-channel decay (GDN_FLAG_PER_CHANNEL_DECAY, gamma [B,T,H,K]) row i
+// of S decays by exp(gamma[i]); each thread scales its rows before the pass,
+// so the reads below always see the decayed state.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -64,6 +68,7 @@ struct DecodeParams {
     E *o;
     int T, H, V;
     int l2norm;               // GDN_FLAG_QK_L2NORM
+    int per_channel;          // GDN_FLAG_PER_CHANNEL_DECAY
     const E *gate;            // output stage, or nullptr
     const float *norm_w;
     float norm_eps;
@@ -75,15 +80,22 @@ struct DecodeParams {
 // shuffles; with VS = 256 a row group spans two warps. Either way each
 // (slot, column) of the partial-sum buffers has exactly one writer.
 // Threads of a CTA, and CTAs per SM asked of the compiler: 1024 threads per SM
-// at 64 registers each keeps 128 KB of state loads in flight on every SM.
+// at 64 registers each keeps 128 KB of state loads in flight on every SM (768
+// threads at up to 85 registers for the per-channel mode's extra factors).
 constexpr int decode_threads(int K, int VS) { return K * VS / (kRows * kCols); }
-constexpr int decode_min_blocks(int K, int VS) {
-    return decode_threads(K, VS) >= 1024 ? 1 : 1024 / decode_threads(K, VS);
+constexpr int decode_min_blocks(int K, int VS, int threads_per_sm = 1024) {
+    return decode_threads(K, VS) >= threads_per_sm ? 1 : threads_per_sm / decode_threads(K, VS);
 }
 
-template <typename E, int K, int VS>
-__global__ void __launch_bounds__(decode_threads(K, VS), decode_min_blocks(K, VS))
+// MODE 0 (plain): no front-end norm, per-channel decay or output stage, all
+// compiled out; MODE 1: per-channel decay only; MODE 2: every option as a
+// runtime switch (more registers, fewer CTAs per SM).
+template <typename E, int K, int VS, int MODE>
+__global__ void __launch_bounds__(decode_threads(K, VS),
+                                  MODE == 0 ? decode_min_blocks(K, VS)
+                                            : MODE == 1 ? decode_min_blocks(K, VS, 768) : 1)
 gdn_decode_step_kernel(const DecodeParams<E> p) {
+    constexpr bool PLAIN = MODE == 0;
     constexpr int CG = VS / kCols;                    // column groups
     constexpr int NT = CG * (K / kRows);              // threads
     constexpr int NW = NT / 32;                       // warps
@@ -103,7 +115,8 @@ gdn_decode_step_kernel(const DecodeParams<E> p) {
     const int col0 = blockIdx.x * VS;
     const size_t bh = static_cast<size_t>(b) * H + h;
     const size_t s_off = (bh * K + rg * kRows) * V + col0 + cg * kCols;
-    const bool norm = p.l2norm != 0, gated = p.gate != nullptr;
+    const bool norm = MODE == 2 && p.l2norm != 0, gated = MODE == 2 && p.gate != nullptr;
+    const bool per_channel = MODE == 1 || (MODE == 2 && p.per_channel != 0);
 
     float S[kRows][kCols];
 #pragma unroll
@@ -118,7 +131,33 @@ gdn_decode_step_kernel(const DecodeParams<E> p) {
         float kk[kRows], qq[kRows];
         load8(p.k + row * K + rg * kRows, kk);
         load8(p.q + row * K + rg * kRows, qq);
-        const float alpha = expf(p.gamma[row]);
+        // The decay: a scalar alpha (mode 0) or one factor per row (mode 1,
+        // ar[i]) enters the sums and the update as a factor; mode 2 decays the
+        // rows first, S <- diag(alpha) S, and alpha below is 1.
+        float alpha = 1.f;
+        float ar[kRows];
+        if (PLAIN) {
+            alpha = expf(p.gamma[row]);
+        } else if (MODE == 1) {
+            load8(p.gamma + row * K + rg * kRows, ar);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) ar[i] = expf(ar[i]);
+        } else if (per_channel) {
+            float ga[kRows];
+            load8(p.gamma + row * K + rg * kRows, ga);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                const float a = expf(ga[i]);
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) S[i][c] *= a;
+            }
+        } else {
+            const float a = expf(p.gamma[row]);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i)
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) S[i][c] *= a;
+        }
 
         // Partial S^T k, S^T q over this thread's rows, k . q (and |k|^2, |q|^2).
         float pk[kCols], pq[kCols], kq = 0.f, k2 = 0.f, q2 = 0.f;
@@ -127,12 +166,16 @@ gdn_decode_step_kernel(const DecodeParams<E> p) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             kq = fmaf(kk[i], qq[i], kq);
-            k2 = fmaf(kk[i], kk[i], k2);
-            q2 = fmaf(qq[i], qq[i], q2);
+            if (MODE == 2) {
+                k2 = fmaf(kk[i], kk[i], k2);
+                q2 = fmaf(qq[i], qq[i], q2);
+            }
+            const float ki = MODE == 1 ? ar[i] * kk[i] : kk[i];
+            const float qi = MODE == 1 ? ar[i] * qq[i] : qq[i];
 #pragma unroll
             for (int c = 0; c < kCols; ++c) {
-                pk[c] = fmaf(S[i][c], kk[i], pk[c]);
-                pq[c] = fmaf(S[i][c], qq[i], pq[c]);
+                pk[c] = fmaf(S[i][c], ki, pk[c]);
+                pq[c] = fmaf(S[i][c], qi, pq[c]);
             }
         }
         // Sum over the row groups of the warp (lanes that share cg).
@@ -144,8 +187,10 @@ gdn_decode_step_kernel(const DecodeParams<E> p) {
                 pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], off);
             }
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
-            k2 += __shfl_xor_sync(0xffffffffu, k2, off);
-            q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+            if (MODE == 2) {
+                k2 += __shfl_xor_sync(0xffffffffu, k2, off);
+                q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+            }
         }
         if (lane < CW) {
 #pragma unroll
@@ -205,7 +250,9 @@ gdn_decode_step_kernel(const DecodeParams<E> p) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
 #pragma unroll
-            for (int c = 0; c < kCols; ++c) S[i][c] = fmaf(kk[i], dd[c], alpha * S[i][c]);
+            for (int c = 0; c < kCols; ++c)
+                S[i][c] = fmaf(kk[i], dd[c],
+                               PLAIN ? alpha * S[i][c] : MODE == 1 ? ar[i] * S[i][c] : S[i][c]);
         // The next token's writes to red_* and delta_s follow this token's
         // second barrier and its own first barrier, after every read above.
     }
@@ -224,7 +271,7 @@ gdn_status check_decode(const gdn_problem *p, const gdn_output_norm *norm) {
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
         return GDN_ERR_INVALID_ARG;
-    if (p->flags & ~(GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+    if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
     if (norm && (!norm->gate || !norm->weight || !(norm->eps >= 0.f))) return GDN_ERR_INVALID_ARG;
     if (p->algo == GDN_ALGO_TC) return GDN_ERR_UNSUPPORTED;
     if (p->K % 64 != 0 || p->K > 256) return GDN_ERR_UNSUPPORTED;
@@ -257,7 +304,13 @@ cudaError_t launch(const gdn_problem *pr, const DecodeParams<E> &p, cudaStream_t
     } else {
         constexpr int threads = decode_threads(K, VS);
         const dim3 grid(pr->V / VS, pr->H, pr->B);
-        gdn_decode_step_kernel<E, K, VS><<<grid, threads, 0, s>>>(p);
+        const bool other = p.l2norm || p.gate;
+        if (other)
+            gdn_decode_step_kernel<E, K, VS, 2><<<grid, threads, 0, s>>>(p);
+        else if (p.per_channel)
+            gdn_decode_step_kernel<E, K, VS, 1><<<grid, threads, 0, s>>>(p);
+        else
+            gdn_decode_step_kernel<E, K, VS, 0><<<grid, threads, 0, s>>>(p);
         return cudaGetLastError();
     }
 }
@@ -291,6 +344,7 @@ cudaError_t dispatch(int vs, const gdn_problem *pr, const void *q, const void *k
     p.H = pr->H;
     p.V = pr->V;
     p.l2norm = (pr->flags & GDN_FLAG_QK_L2NORM) ? 1 : 0;
+    p.per_channel = (pr->flags & GDN_FLAG_PER_CHANNEL_DECAY) ? 1 : 0;
     p.gate = norm ? static_cast<const E *>(norm->gate) : nullptr;
     p.norm_w = norm ? norm->weight : nullptr;
     p.norm_eps = norm ? norm->eps : 0.f;

@@ -31,7 +31,7 @@ struct Args {
     // to g_cum, which the later kernels read; with GDN_FLAG_QK_L2NORM the first
     // kernel writes each k row's factor 1 / sqrt(|k|^2 + eps) to rk.
     int flags;
-    float *g_cum;   // [B, T, H] fp32 workspace
+    float *g_cum;   // [B, T, H] fp32 workspace ([B, T, H, K] with per-channel decay)
     float *rk;      // [B, T, H] fp32 workspace
     // g as the kernels after the first one read it: g_cum or g
     const float *g_chunk() const { return (flags & GDN_FLAG_RAW_G) ? g_cum : g; }
@@ -42,6 +42,7 @@ struct Args {
 };
 
 constexpr float kL2NormEps = 1e-6f;
+constexpr int kKnownFlags = GDN_FLAG_RAW_G | GDN_FLAG_QK_L2NORM | GDN_FLAG_PER_CHANNEL_DECAY;
 
 // Workspace of the SIMT pipeline: fp32 intermediates, every region 256-byte aligned.
 struct SimtWorkspace {

@@ -14,6 +14,7 @@ Recipe (one ``torch.Generator('cpu')`` per workload, drawn in this order):
   (``chunk=1`` leaves the per-token log-decay itself, the decode step's gamma);
   with ``raw=True`` q and k are left unnormalised (and q unscaled) and g is
   the per-token log-decay itself: the inputs of the in-kernel front-end;
+  with ``per_channel=True`` g_raw is [B,T,H,K], one decay per key channel;
   h0 = h0_std * h0_raw. q, k, v are then cast to the compute dtype; g, beta and
   h0 stay fp32.
 
@@ -95,16 +96,18 @@ def chunk_local_cumsum(x: torch.Tensor, chunk: int = CHUNK) -> torch.Tensor:
 
 def make_inputs(B: int, T: int, H: int, K: int, V: int, *, dtype: str = "bf16", seed: int = 0,
                 h0_std: float = 0.0, g_mean: float = 0.0, g_div: float = 16.0,
-                beta_mean: float = 0.0, chunk: int = CHUNK, raw: bool = False) -> dict:
+                beta_mean: float = 0.0, chunk: int = CHUNK, raw: bool = False,
+                per_channel: bool = False) -> dict:
     """Return CPU tensors q,k,v (dtype), g, beta (fp32) and h0 (fp32 or None).
     g is the per-token log-decay summed within chunks of ``chunk`` tokens;
-    ``raw`` skips the q/k normalisation and the sum (same draws)."""
+    ``raw`` skips the q/k normalisation and the sum (same draws);
+    ``per_channel`` draws one decay per key channel (g [B,T,H,K])."""
     gen = torch.Generator("cpu").manual_seed(seed)
     q = torch.randn(B, T, H, K, generator=gen)
     k = torch.randn(B, T, H, K, generator=gen)
     v = torch.randn(B, T, H, V, generator=gen)
     beta_raw = torch.randn(B, T, H, generator=gen)
-    g_raw = torch.randn(B, T, H, generator=gen)
+    g_raw = torch.randn((B, T, H, K) if per_channel else (B, T, H), generator=gen)
     h0 = None
     if h0_std > 0:
         h0 = torch.randn(B, H, K, V, generator=gen) * h0_std

@@ -16,7 +16,7 @@ LIB_PATH = Path(__file__).resolve().parent / "lib" / "libgdn.so"
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGNMENT = 0, 1, 2, 3
 GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 GDN_F32, GDN_BF16 = 0, 1
-GDN_FLAG_RAW_G, GDN_FLAG_QK_L2NORM = 1, 2
+GDN_FLAG_RAW_G, GDN_FLAG_QK_L2NORM, GDN_FLAG_PER_CHANNEL_DECAY = 1, 2, 4
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
 CHUNK = 64
@@ -101,8 +101,9 @@ def status_string(s: int) -> str:
     return lib().gdn_status_string(int(s)).decode()
 
 
-def flags_of(raw_g: bool = False, qk_l2norm: bool = False) -> int:
-    return (GDN_FLAG_RAW_G if raw_g else 0) | (GDN_FLAG_QK_L2NORM if qk_l2norm else 0)
+def flags_of(raw_g: bool = False, qk_l2norm: bool = False, per_channel: bool = False) -> int:
+    return ((GDN_FLAG_RAW_G if raw_g else 0) | (GDN_FLAG_QK_L2NORM if qk_l2norm else 0)
+            | (GDN_FLAG_PER_CHANNEL_DECAY if per_channel else 0))
 
 
 def problem(B, T, H, K, V, dtype, algo="auto", flags: int = 0) -> Problem:
@@ -127,7 +128,7 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _check_inputs(q, k, v, g, beta, h0):
+def _check_inputs(q, k, v, g, beta, h0, per_channel: bool = False):
     B, T, H, K = q.shape
     V = v.shape[-1]
     dev = q.device
@@ -137,9 +138,11 @@ def _check_inputs(q, k, v, g, beta, h0):
         raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
-    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or g.shape != (B, T, H) \
+    g_shape = (B, T, H, K) if per_channel else (B, T, H)
+    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or g.shape != g_shape \
             or beta.shape != (B, T, H):
-        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], g, beta [B,T,H]")
+        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], beta [B,T,H], g [B,T,H] "
+                         "([B,T,H,K] with per-channel decay)")
     if h0 is not None and (h0.shape != (B, H, K, V) or h0.dtype != torch.float32):
         raise ValueError("h0 must be float32 [B,H,K,V]")
     for t in (q, k, v, g, beta, h0):
@@ -166,7 +169,7 @@ def _output_norm(gate, weight, eps, shape, like):
 def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
               algo: str = "auto", workspace=None, out=None, final_state=None, stream=None,
               events=None, raw_g: bool = False, qk_l2norm: bool = False, gate=None,
-              norm_weight=None, norm_eps: float = 1e-6):
+              norm_weight=None, norm_eps: float = 1e-6, per_channel_decay: bool = False):
     """Chunked gated-delta-rule forward on CUDA tensors. Returns (o, h_final or None).
 
     q, k [B,T,H,K] and v [B,T,H,V] (float32 or bfloat16), g and beta [B,T,H]
@@ -176,10 +179,12 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     ``qk_l2norm``: q and k rows are L2-normalised in the kernels (eps 1e-6).
     ``gate`` [B,T,H,V] (q's dtype) with ``norm_weight`` [V] float32: the output
     rows pass through the gated RMSNorm o * rsqrt(mean o^2 + norm_eps) *
-    norm_weight * sigmoid(gate) before their rounding."""
-    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
+    norm_weight * sigmoid(gate) before their rounding.
+    ``per_channel_decay``: g is [B,T,H,K], one decay per key channel (the KDA
+    variant; CUDA-core pipeline)."""
+    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0, per_channel_decay)
     norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)
-    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
+    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm, per_channel_decay))
     need = workspace_bytes(p)
     if need == 0:
         raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_chunk_fwd_workspace_bytes")
@@ -214,11 +219,11 @@ STAGES = ("A", "w", "u", "v_new", "h", "A_beta")
 
 def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = "simt",
                      stages=("A", "w", "u", "v_new", "h"), raw_g: bool = False,
-                     qk_l2norm: bool = False):
+                     qk_l2norm: bool = False, per_channel_decay: bool = False):
     """Forward plus the requested exported intermediates (fp32 tensors): A, w, u,
     v_new, h (SIMT path) or A_beta = A diag(beta) (tensor-core path)."""
-    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0)
-    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
+    B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0, per_channel_decay)
+    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm, per_channel_decay))
     NT = (T + CHUNK - 1) // CHUNK
     Tp = NT * CHUNK
     f32 = dict(dtype=torch.float32, device=q.device)
@@ -244,7 +249,7 @@ def chunk_fwd_stages(q, k, v, g, beta, scale: float = 1.0, h0=None, algo: str = 
 
 def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None, out=None,
                 stream=None, qk_l2norm: bool = False, gate=None, norm_weight=None,
-                norm_eps: float = 1e-6):
+                norm_eps: float = 1e-6, per_channel_decay: bool = False):
     """Recurrent step(s) of the rule on CUDA tensors: advances every sequence by
     its T tokens and returns (o, state_out).
 
@@ -264,9 +269,11 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
         raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
     if gamma.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("gamma and beta must be float32")
-    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or gamma.shape != (B, T, H) \
+    g_shape = (B, T, H, K) if per_channel_decay else (B, T, H)
+    if k.shape != (B, T, H, K) or v.shape[:3] != (B, T, H) or gamma.shape != g_shape \
             or beta.shape != (B, T, H):
-        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], gamma, beta [B,T,H]")
+        raise ValueError("shapes must be q,k [B,T,H,K], v [B,T,H,V], beta [B,T,H], gamma "
+                         "[B,T,H] ([B,T,H,K] with per-channel decay)")
     so = state if state_out is None else state_out
     for st in (state, so):
         if st.shape != (B, H, K, V) or st.dtype != torch.float32:
@@ -275,7 +282,7 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
         if not t.is_contiguous() or t.device != dev:
             raise ValueError("all tensors must be contiguous and on the same device")
     o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
-    p = problem(B, T, H, K, V, q.dtype, "auto", flags_of(False, qk_l2norm))
+    p = problem(B, T, H, K, V, q.dtype, "auto", flags_of(False, qk_l2norm, per_channel_decay))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)
     st = lib().gdn_decode_step_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),

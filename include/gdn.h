@@ -84,11 +84,20 @@ typedef enum {
  *    is replaced by x / sqrt(sum_i x_i^2 + 1e-6) before use; scale still
  *    multiplies o, i.e. it scales the normalised q. The normalised rows are
  *    never rounded back to the input dtype.
+ *  - GDN_FLAG_PER_CHANNEL_DECAY: the decay is a K-vector per token (the KDA
+ *    variant of the "KdaSplit" decode kernel page, where each state row decays
+ *    by its own factor): g is [B,T,H,K] fp32 and the decay step becomes
+ *    S[i, :] <- exp(gamma_t[i]) S[i, :]; in the chunked form every
+ *    exp(g_i - g_j) becomes a per-channel factor inside the k and q products.
+ *    It combines with the other flags (the cumulative sum is then per
+ *    channel). The chunked forward runs it on the CUDA-core pipeline only:
+ *    GDN_ALGO_TC gives GDN_ERR_UNSUPPORTED and GDN_ALGO_AUTO picks SIMT.
  * gdn_decode_step always takes raw gamma and accepts either g flag; it
- * honours GDN_FLAG_QK_L2NORM. */
+ * honours GDN_FLAG_QK_L2NORM and GDN_FLAG_PER_CHANNEL_DECAY (gamma [B,T,H,K]). */
 enum {
     GDN_FLAG_RAW_G = 1,
-    GDN_FLAG_QK_L2NORM = 2
+    GDN_FLAG_QK_L2NORM = 2,
+    GDN_FLAG_PER_CHANNEL_DECAY = 4
 };
 
 /* Problem description. K in {64, 128}; V a multiple of 64 in [64, 256];

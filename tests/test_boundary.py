@@ -144,10 +144,10 @@ def test_flags_validated():
             p = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo, flags)
             assert native.workspace_bytes(p) > native.workspace_bytes(
                 native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo)) - 1
-    bad = native.problem(1, 64, 1, 64, 64, native.GDN_BF16, "auto", 4)
+    bad = native.problem(1, 64, 1, 64, 64, native.GDN_BF16, "auto", 8)
     assert native.workspace_bytes(bad) == 0
     assert _call(bad) == native.GDN_ERR_INVALID_ARG
-    assert _decode(native.problem(1, 1, 1, 64, 64, native.GDN_BF16, "auto", 8)) == \
+    assert _decode(native.problem(1, 1, 1, 64, 64, native.GDN_BF16, "auto", 16)) == \
         native.GDN_ERR_INVALID_ARG
 
 
@@ -176,3 +176,17 @@ def test_output_norm_validated():
     assert dec(128, 48, ok) == native.GDN_ERR_UNSUPPORTED     # V not a slice width
     assert dec(256, 256, ok) == native.GDN_ERR_UNSUPPORTED    # K V > 32768
     assert dec(128, 128, native.OutputNorm(None, FAKE, 1e-6)) == native.GDN_ERR_INVALID_ARG
+
+
+def test_per_channel_flag_routes_to_simt():
+    flags = native.GDN_FLAG_PER_CHANNEL_DECAY
+    p_tc = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "tc", flags)
+    assert native.workspace_bytes(p_tc) == 0
+    assert _call(p_tc) == native.GDN_ERR_UNSUPPORTED
+    p_auto = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "auto", flags)
+    p_simt = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "simt", flags)
+    assert native.workspace_bytes(p_auto) == native.workspace_bytes(p_simt) > 0
+    # the front-end's g region holds one value per channel with this flag
+    plain = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "simt")
+    assert native.workspace_bytes(p_simt) - native.workspace_bytes(plain) >= 2 * 100 * 3 * 127 * 4 - 256
+    assert native.launches(p_auto) == ["wy_prepare_kernel", "chunk_h_kernel", "chunk_o_kernel"]

@@ -1,0 +1,136 @@
+"""Per-channel (KDA) decay, problem flag GDN_FLAG_PER_CHANNEL_DECAY, against the
+fp64 oracle's per-channel recurrence, element by element.
+
+The chunked forward runs it on the CUDA-core pipeline (fp32 arithmetic), the
+decode step in its own kernel. Tolerances: relative Frobenius 1e-4 for fp32
+inputs and 2e-2 for bf16 inputs (the plain path's); the exported stages 1e-5;
+decode 1e-5 (state, fp32 o) and 2.5e-3 (bf16 o)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import epilogue, frontend, recurrence
+from tests.pins import rel
+from gated_delta_rule_35_gb300 import GdnError, chunk_fwd, chunk_fwd_stages, decode_step, native
+from gated_delta_rule_35_gb300.inputs import make_inputs, make_output_norm, to_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def gpu(x):
+    return {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+
+
+def oracle(x, scale=1.0, raw_g=False, l2norm=False, chunk=64, stages=False):
+    q, k, g = frontend.prepare(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["g"]), raw_g=raw_g,
+                               qk_l2norm=l2norm)
+    return recurrence.forward(q, k, to_f64(x["v"]), g, to_f64(x["beta"]), scale,
+                              to_f64(x["h0"]), chunk=chunk, stages=stages)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 256)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_kda_chunked_parity(dtype, K, V, T):
+    x = make_inputs(2, T, 3, K, V, dtype=dtype, seed=700 + T + K + V, h0_std=0.1,
+                    per_channel=True)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"],
+                      per_channel_decay=True)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x)
+    o, hf = o.float().cpu().numpy(), hf.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(hf).all()
+    assert rel(o, o_ref) < TOL[dtype], rel(o, o_ref)
+    assert rel(hf, hf_ref) < TOL[dtype], rel(hf, hf_ref)
+
+
+@pytest.mark.parametrize("g_div", [1.0, 0.2])
+def test_kda_strong_and_uneven_decay(g_div):
+    """Channels decaying at very different rates, some near exp(-300) over a chunk."""
+    x = make_inputs(2, 150, 2, 128, 128, dtype="f32", seed=71, h0_std=0.1, per_channel=True,
+                    g_div=g_div)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"],
+                      per_channel_decay=True)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x)
+    assert rel(o.cpu().numpy(), o_ref) < TOL["f32"]
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["f32"]
+
+
+def test_kda_stages_against_recurrence():
+    """The state entering each chunk and the per-token correction d_t (v_new)
+    of the CUDA-core pipeline against the recurrence's exports."""
+    T = 150
+    x = make_inputs(2, T, 2, 64, 64, dtype="f32", seed=72, h0_std=0.1, per_channel=True)
+    d = gpu(x)
+    st = chunk_fwd_stages(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="simt",
+                          stages=("v_new", "h"), per_channel_decay=True)
+    torch.cuda.synchronize()
+    _, _, hc, dl = oracle(x, stages=True)
+    assert rel(st["h"].cpu().numpy(), hc) < 1e-5
+    assert rel(st["v_new"][:, :T].cpu().numpy(), dl) < 1e-5
+
+
+def test_kda_with_front_end_and_output_stage():
+    B, T, H, K, V = 2, 130, 2, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=73, h0_std=0.1, raw=True, per_channel=True)
+    gate, weight = make_output_norm(B, T, H, V, seed=73)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], K ** -0.5, d["h0"], raw_g=True,
+                      qk_l2norm=True, gate=gate.cuda(), norm_weight=weight.cuda(),
+                      per_channel_decay=True)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, K ** -0.5, raw_g=True, l2norm=True)
+    o_ref = epilogue.gated_rmsnorm(o_ref, to_f64(gate), to_f64(weight), 1e-6)
+    assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+
+
+def test_kda_tensor_core_request_is_refused():
+    x = gpu(make_inputs(1, 64, 1, 64, 64, dtype="bf16", seed=74, per_channel=True))
+    with pytest.raises(GdnError) as e:
+        chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None, algo="tc",
+                  per_channel_decay=True)
+    assert e.value.status == native.GDN_ERR_UNSUPPORTED
+    p = native.problem(4, 2048, 16, 128, 128, torch.bfloat16, "auto",
+                       native.flags_of(per_channel=True))
+    assert native.launches(p) == ["wy_prepare_kernel", "chunk_h_kernel", "chunk_o_kernel"]
+
+
+def test_kda_full_size_sampled():
+    """The default workload's shape with per-channel decay through 'auto'."""
+    B, T, H, K, V = 4, 2048, 16, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=1, per_channel=True)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None,
+                      per_channel_decay=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(hf).all()
+    for b, h in [(0, 0), (3, 15), (2, 4)]:
+        sub = {n: x[n][b:b + 1, :, h:h + 1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+        sub["h0"] = None
+        o_ref, hf_ref = oracle(sub)
+        assert rel(o[b:b + 1, :, h:h + 1].float().cpu().numpy(), o_ref) < TOL["bf16"], (b, h)
+        assert rel(hf[b:b + 1, h:h + 1].cpu().numpy(), hf_ref) < TOL["bf16"], (b, h)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(3, 2, 4, 128, 128), (20, 1, 16, 64, 128), (1, 3, 2, 256, 48)])
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_kda_decode(dtype, shape, l2norm):
+    B, T, H, K, V = shape
+    x = make_inputs(B, T, H, K, V, dtype=dtype, seed=B + T + K, h0_std=0.1, raw=l2norm, chunk=1,
+                    per_channel=True)
+    d = gpu(x)
+    state = x["h0"].cuda()
+    scale = K ** -0.5 if l2norm else 1.0
+    o, s1 = decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale,
+                        qk_l2norm=l2norm, per_channel_decay=True)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle(x, scale, l2norm=l2norm, chunk=1)
+    assert rel(o.float().cpu().numpy(), o_ref) < (1e-5 if dtype == "f32" else 2.5e-3)
+    assert rel(s1.cpu().numpy(), s_ref) < 1e-5
