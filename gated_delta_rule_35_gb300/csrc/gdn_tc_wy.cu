@@ -18,11 +18,11 @@
 //   epi     L (fp32 16x16 diagonal blocks, bf16 N1 | N2 stacked)
 //   SIMT    X: forward substitution on the diagonal blocks (fp32)
 //   MMA 2   [Y1; U] = [N1; N2] X
-//   MMA 3   [X Y1; U Y1] = [X; U] Y1  ->  A0 = X - X Y1, Y2 = U - U Y1
-//   MMA 4   Z = A0 Y2                  ->  A  = A0 - Z
+//   MMA 3   [A0; Y2] = [X; U] + [X; U] (-Y1)   (accumulator preloaded with X, keeps U)
+//   MMA 4   A = A0 + A0 (-Y2)                   (accumulator keeps A0)
 //   epi     A diag(beta), A diag(beta exp(g)) -> bf16 -> TMA store
 // The correction products run with bf16 operands and fp32 accumulation; the
-// block-diagonal part and the subtractions stay fp32.
+// block-diagonal part and the subtractions stay fp32 (in the accumulator).
 //
 // Front-end (problem flags): with GDN_FLAG_RAW_G the chunk's g is the inclusive
 // sum of the raw per-token log decays, taken here and written to g_cum for the
@@ -51,17 +51,22 @@ struct WyLayout {
     static constexpr uint32_t kKBytes = (KB * 8192 > 16384) ? KB * 8192 : 16384;
     static constexpr uint32_t kN = 0;
     static constexpr uint32_t kXU = kKBytes;               // [X; U] stacked, then A0 (bf16)
-    static constexpr uint32_t kY = kXU + 16384;            // Y1, then Y2 (bf16, rows along N)
-    static constexpr uint32_t kOut = kY + 8192;            // A diag(beta) staging
-    static constexpr uint32_t kLd = kOut + 8192;           // diagonal blocks fp32 [4][16][17]
+    // One 8 KB region, four lives: the fp32 diagonal blocks [4][16][17] (dead
+    // once X is in [X; U]), Y1, Y2 (read by the last MMA), and finally the
+    // A diag(beta) staging of the TMA store.
+    static constexpr uint32_t kY = kXU + 16384;
+    static constexpr uint32_t kLd = kY;
+    static constexpr uint32_t kOut = kY;
     // g, beta, beta exp(g) r, cf, r (64 floats each), a scan total; barriers
-    static constexpr uint32_t kMisc = kLd + 4 * 16 * 17 * 4;
+    static constexpr uint32_t kMisc = kY + 8192;
     static constexpr uint32_t kBar = kMisc + 1344;
     static constexpr uint32_t kBytes = kBar + 256;
 };
 
 template <int K>
-__global__ void __launch_bounds__(kWyThreads, 4)
+// Five CTAs per SM (96 registers, a few spilled; 43.6 KB of shared memory
+// each): 2048 chunks then take three waves of 760 instead of four of 608.
+__global__ void __launch_bounds__(kWyThreads, 5)
 gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_a,
                  const float *__restrict__ g, const float *__restrict__ beta, int T, int H,
                  uint32_t *status, int flags, float *__restrict__ g_cum, float *__restrict__ rk_out) {
@@ -145,7 +150,8 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     // One MMA group issued by thread 0 (A K-major, B K-major or rows-along-N),
     // then everyone waits for it.
-    auto mma_issue = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
+    // acc: add to the accumulator's current contents from the first step on
+    auto mma_issue = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps, bool acc = false) {
         if (tid == 0) {
             tc_fence_after_sync();
             const uint32_t id = idesc_bf16(M, 64, false, b_mn);
@@ -153,7 +159,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const uint32_t a_off = (ks >> 2) * 8192 + (ks & 3) * 32;
                 mma_bf16(tmem, smem_desc(a + a_off, 16, 1024, kLayoutSw128),
                          smem_desc(bop + (b_mn ? ks * 2048 : a_off), 8192, 1024, kLayoutSw128), id,
-                         ks > 0);
+                         acc || ks > 0);
             }
             mma_commit(bar_mma);
         }
@@ -163,8 +169,8 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         phase ^= 1;
         tc_fence_after_sync();
     };
-    auto mma = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps) {
-        mma_issue(M, a, bop, b_mn, ksteps);
+    auto mma = [&](int M, uint32_t a, uint32_t bop, bool b_mn, int ksteps, bool acc = false) {
+        mma_issue(M, a, bop, b_mn, ksteps, acc);
         mma_wait();
     };
     // This thread's accumulator row, 16 columns at a time.
@@ -279,16 +285,24 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         __syncthreads();
     }
     // From here on thread t owns row t of the M = 128 accumulators: rows 0-63
-    // belong to X / A0, rows 64-127 to U / Y2.
+    // belong to X / A0 / A, rows 64-127 to U / Y2. The subtractions happen in
+    // the fp32 accumulator: it is loaded with X (rows 0-63) or keeps U (rows
+    // 64-127) and the next product adds [X; U] (-Y1), then [A0; U] (-Y2).
     {
         const int r = tid & 63, rb = r >> 4;
-        // keep: row r of X, then of A0 (threads < 64); row r of U (threads >= 64)
-        float keep[64];
+        // row r of X (threads < 64): its diagonal block; the rest of the row is 0
+        float xr[16];
         if (tid < 64) {
+            const float z8[8] = {};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) keep[j] = ((j >> 4) == rb) ? Ld[(rb * 16 + (r & 15)) * 17 + (j & 15)] : 0.f;
+            for (int j = 0; j < 16; ++j) xr[j] = Ld[(rb * 16 + (r & 15)) * 17 + j];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) st_bf16x8(sm + Lay::kXU + sw128(r, ch * 16), keep + ch * 8);
+            for (int ch = 0; ch < 8; ++ch) {
+                if ((ch >> 1) == rb)
+                    st_bf16x8(sm + Lay::kXU + sw128(r, ch * 16), xr + (ch & 1) * 8);
+                else
+                    st_bf16x8(sm + Lay::kXU + sw128(r, ch * 16), z8);
+            }
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -299,45 +313,58 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int blk = 0; blk < 4; ++blk) {
             float v[16];
             load16(blk, v);
-            // Y1 rows -> B operand (rows along N); U rows -> second half of [X; U]
-            unsigned char *dst = (tid < 64) ? sm + Lay::kY : sm + Lay::kXU + 8192;
-            st_bf16x8(dst + sw128(r, blk * 32), v);
-            st_bf16x8(dst + sw128(r, blk * 32 + 16), v + 8);
-            if (tid >= 64) {
+            if (tid < 64) {
+                // -Y1, the B operand (rows along N) of the next product
 #pragma unroll
-                for (int e = 0; e < 16; ++e) keep[blk * 16 + e] = v[e];
+                for (int e = 0; e < 16; ++e) v[e] = -v[e];
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32), v);
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32 + 16), v + 8);
+            } else {
+                // U, the second half of the A operand [X; U]; its fp32 copy stays
+                // in the accumulator
+                st_bf16x8(sm + Lay::kXU + 8192 + sw128(r, blk * 32), v);
+                st_bf16x8(sm + Lay::kXU + 8192 + sw128(r, blk * 32 + 16), v + 8);
             }
+        }
+        if (tid < 64) {
+            // the accumulator's rows 0-63 start the next product from X
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                uint32_t t[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) t[e] = blk == rb ? __float_as_uint(xr[e]) : 0u;
+                tmem_st16(tmem + lane_off + blk * 16, t);
+            }
+            tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        // ---- [X Y1; U Y1] = [X; U] Y1
-        mma(128, s_xu, s_y, true, 4);
+        // ---- [A0; Y2] = [X; U] + [X; U] (-Y1)
+        mma(128, s_xu, s_y, true, 4, true);
         if (__syncthreads_or(fail)) goto done;
         tc_fence_before_sync();
-        __syncthreads();   // every MMA operand read before A0 / Y2 overwrite them
+        __syncthreads();   // every MMA operand read before A0 / -Y2 overwrite them
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
             float v[16];
             load16(blk, v);
             if (tid < 64) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) keep[blk * 16 + e] -= v[e];   // A0 = X - X Y1
-                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32), keep + blk * 16);
-                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32 + 16), keep + blk * 16 + 8);
+                // A0 as the next A operand (its fp32 copy stays in the accumulator)
+                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32), v);
+                st_bf16x8(sm + Lay::kXU + sw128(r, blk * 32 + 16), v + 8);
             } else {
-                float y2[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) y2[e] = keep[blk * 16 + e] - v[e];   // Y2 = U - U Y1
-                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32), y2);
-                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32 + 16), y2 + 8);
+                for (int e = 0; e < 16; ++e) v[e] = -v[e];
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32), v);
+                st_bf16x8(sm + Lay::kY + sw128(r, blk * 32 + 16), v + 8);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        // ---- Z = A0 Y2 (rows 64-127 of the operand are unused)
-        mma(128, s_xu, s_y, true, 4);
+        // ---- A = A0 + A0 (-Y2) in rows 0-63 (rows 64-127 of the product are unused)
+        mma(128, s_xu, s_y, true, 4, true);
         if (__syncthreads_or(fail)) goto done;
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
@@ -349,7 +376,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 float v2[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = keep[blk * 16 + e] - v[e];
+                    const float a = v[e];
                     v[e] = a * b_s[blk * 16 + e];
                     v2[e] = a * eb_s[blk * 16 + e];
                 }
@@ -366,7 +393,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tma_store_4d(&tm_a, sm + Lay::kOut, 0, h, t0, b);
         tma_store_4d(&tm_a, sm + Lay::kN, 64, h, t0, b);
         bulk_commit_group();
-        bulk_wait_group0();
+        bulk_wait_group_read0();   // only the shared source must outlive the CTA
     }
 done:
     if (tid == 0 && fail) atomicOr(status, 2u);
