@@ -25,7 +25,8 @@ CHUNK = 64
 EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stages",
            "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
            "gdn_chunk_fwd_noalloc", "gdn_decode_step", "gdn_decode_step_launches",
-           "gdn_chunk_fwd_ex", "gdn_decode_step_ex", "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_ex", "gdn_decode_step_ex", "gdn_chunk_fwd_host_bytes",
+           "gdn_chunk_fwd_host", "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -84,6 +85,11 @@ def lib():
         L.gdn_decode_step_ex.restype = ctypes.c_int
         L.gdn_decode_step_ex.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                          ctypes.POINTER(OutputNorm), vp, vp]
+        L.gdn_chunk_fwd_host_bytes.restype = sz
+        L.gdn_chunk_fwd_host_bytes.argtypes = [pp, ctypes.c_int32]
+        L.gdn_chunk_fwd_host.restype = ctypes.c_int
+        L.gdn_chunk_fwd_host.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, sz,
+                                         ctypes.c_int32, vp, vp]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [pp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         L.gdn_decode_step_launches.restype = ctypes.c_int32
@@ -306,22 +312,57 @@ def check_device_status(workspace, stream=None) -> int:
     return int(lib().gdn_check_device_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream)))
 
 
+_host_streams: dict = {}
+
+
+def _pipeline_streams(dev, n: int):
+    """n side streams of ``dev``, created once and reused by every host call."""
+    key = (dev.index, n)
+    if key not in _host_streams:
+        _host_streams[key] = [torch.cuda.Stream(dev) for _ in range(n)]
+    return _host_streams[key]
+
+
 def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
-                   algo: str = "auto", device=None, raw_g: bool = False, qk_l2norm: bool = False):
-    """Host-tensor front end: copies the inputs to the GPU, runs chunk_fwd and
-    copies o (and h_final) back into pinned host tensors, synchronously."""
+                   algo: str = "auto", device=None, raw_g: bool = False, qk_l2norm: bool = False,
+                   pieces: int = 4):
+    """Host-tensor front end (gdn_chunk_fwd_host): host inputs in, host outputs
+    out; returns when o (and h_final) are in pinned host tensors. Pinned inputs
+    let the library overlap the copies of one span of T (up to ``pieces``
+    64-aligned spans) with the kernels of the previous one. torch supplies the
+    device buffer and the two side streams."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    dq, dk, dv, dg, db = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
-    dh0 = None if h0 is None else h0.to(dev, non_blocking=True)
-    o, hf = chunk_fwd(dq, dk, dv, dg, db, scale, dh0, output_final_state, algo, raw_g=raw_g,
-                      qk_l2norm=qk_l2norm)
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    ho.copy_(o, non_blocking=True)
-    hhf = None
-    if hf is not None:
-        hhf = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
-        hhf.copy_(hf, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    for t in (q, k, v, g, beta, h0):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError("chunk_fwd_host takes contiguous host tensors")
+    if q.dtype not in DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
+    need = int(lib().gdn_chunk_fwd_host_bytes(ctypes.byref(p), int(pieces)))
+    if need == 0:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_host_bytes")
+    with torch.cuda.device(dev):
+        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+        sa, sb = _pipeline_streams(dev, 2)
+        main = torch.cuda.current_stream(dev)
+        sa.wait_stream(main)
+        sb.wait_stream(main)
+        ho = torch.empty((B, T, H, V), dtype=q.dtype, pin_memory=True)
+        hhf = torch.empty((B, H, K, V), dtype=torch.float32, pin_memory=True) \
+            if output_final_state else None
+        st = lib().gdn_chunk_fwd_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                      _ptr(beta), float(scale), _ptr(h0), _ptr(ho), _ptr(hhf),
+                                      _ptr(buf), need, int(pieces),
+                                      ctypes.c_void_p(sa.cuda_stream),
+                                      ctypes.c_void_p(sb.cuda_stream))
+        buf.record_stream(sa)
+        buf.record_stream(sb)
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd_host")
     return ho, hhf
 
 

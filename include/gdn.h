@@ -164,6 +164,32 @@ GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p,
                                           void *workspace, size_t workspace_bytes,
                                           void *const *events, int32_t n_events, void *stream);
 
+/* The forward from and to HOST memory, for callers whose tensors live there:
+ * q, k, v, g, beta, h0 (or NULL) are host buffers in the layouts above; o and
+ * h_final (or NULL) are host buffers the results are written to. Page-locked
+ * (pinned) host buffers let the copies run asynchronously and overlap.
+ *
+ * The sequence is cut into up to `pieces` spans of T (1..16 spans, each a
+ * multiple of 64 tokens, all batch rows and heads at once) so that the
+ * host-to-device copies of one span (on `stream_a`) overlap the kernels and the
+ * device-to-host copies of the previous one (on `stream_b`); each span starts
+ * from the previous span's final state. The call creates and destroys one
+ * event per span to order the two streams. `device_buffer` (device memory of at
+ * least gdn_chunk_fwd_host_bytes(p, pieces) bytes, 256-byte aligned) holds the
+ * device copies of the inputs and outputs, two state buffers and one span's
+ * workspace. Both streams must be distinct, caller-created streams of the
+ * current device. The call returns when o and h_final are in host memory (it
+ * synchronises both streams); errors are reported as for gdn_chunk_fwd. Same results as
+ * gdn_chunk_fwd up to rounding (the state crosses a span boundary in fp32;
+ * with one span they are identical). */
+GDN_API size_t gdn_chunk_fwd_host_bytes(const gdn_problem *p, int32_t pieces);
+GDN_API gdn_status gdn_chunk_fwd_host(const gdn_problem *p,
+                                      const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float scale,
+                                      const float *h0, void *o, float *h_final,
+                                      void *device_buffer, size_t device_bytes,
+                                      int32_t pieces, void *stream_a, void *stream_b);
+
 /* Waits for `stream`, then reads and clears the device status word kept in the
  * first bytes of `workspace`: GDN_ERR_DEVICE_TIMEOUT if a bounded device wait
  * of an earlier call on this workspace gave up, GDN_OK otherwise (or
