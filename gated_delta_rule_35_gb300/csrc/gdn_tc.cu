@@ -224,6 +224,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // With the output stage the V tiles of one head run as a cluster (rank =
     // V tile); its barriers must be initialised before any CTA arrives on them.
     if (nrank) cluster_sync();
+    // The setup above overlaps the WY kernel's last CTAs; everything below may
+    // read its output.
+    griddep_wait();
     tc_fence_after_sync();
     const uint32_t tmem = bs->tmem;
     const uint32_t s_base = smem_u32(sm);
@@ -785,13 +788,17 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = nrank;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    // may start while the WY kernel before it in the stream finishes (it waits
+    // for that kernel's output after its own setup)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = nrank;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = nrank ? 1 : 0;
+    cfg.numAttrs = nrank ? 2 : 1;
     // kernel arguments, in order, for the untyped launch call
     const float *g_arg = a.g_chunk(), *h0_arg = a.h0, *rk_arg = a.rk, *nw_arg = a.norm_w;
     float *hf_arg = a.h_final;

@@ -97,6 +97,8 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tmem_alloc(tmem_slot, 64);
         tmem_relinquish();
     }
+    // the fused kernel that follows may be scheduled as SMs free up
+    griddep_launch_dependents();
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);

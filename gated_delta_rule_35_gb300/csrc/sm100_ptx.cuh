@@ -78,6 +78,16 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start while its predecessor in the stream still runs;
+// griddep_wait blocks until that predecessor has completed and its memory is
+// visible, and the predecessor's griddep_launch_dependents lets the dependent
+// grid be scheduled before it exits.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
