@@ -89,20 +89,24 @@ wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float 
     float *ks = smem;                  // [64][K+1]
     float *Ls = ks + kChunk * KP;      // [64][65]
     float *As = Ls + kChunk * 65;      // [64][65]
-    float *xs = As + kChunk * 65;      // [64][65] slice of v * beta
+    float *xs = As + kChunk * 65;      // [64][64] slice of v * beta (rows read as float4)
     // per-channel decay: g of the chunk's tokens, [64][K+1]
     const bool pc = flags & GDN_FLAG_PER_CHANNEL_DECAY;
-    float *gk = xs + kChunk * 65;
+    float *gk = xs + kChunk * 64;
 
     if (tid < kChunk) {
         gs[tid] = (!pc && tid < n) ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
         bs[tid] = tid < n ? beta[tok(b, t0 + tid, h, Tn, H)] : 0.f;
     }
-#pragma unroll 8
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, kk = idx - i * K;
-        ks[i * KP + kk] = i < n ? to_f32(k[tok(b, t0 + i, h, Tn, H) * K + kk]) : 0.f;
-        if (pc) gk[i * KP + kk] = i < n ? g[tok(b, t0 + i, h, Tn, H) * K + kk] : 0.f;
+#pragma unroll 4
+    for (int idx = tid; idx < kChunk * K / 4; idx += kThreads) {
+        const int i = idx / (K / 4), kk = (idx - i * (K / 4)) * 4;
+        const int64_t r = tok(b, t0 + i, h, Tn, H) * K + kk;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ks[i * KP + kk + e] = i < n ? to_f32(k[r + e]) : 0.f;
+            if (pc) gk[i * KP + kk + e] = i < n ? g[r + e] : 0.f;
+        }
     }
     __syncthreads();
     // Front-end: g from raw per-token log decays (chunk-local inclusive sum,
@@ -134,26 +138,51 @@ wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float 
     // (ks <- k exp(g - r), gk <- k exp(r - g)) when the chunk's decays allow
     const bool pc_fz = pc && factor_per_channel(ks, ks, gk, rs, KP, K, n);
 
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float val = 0.f;
-        if (i > j && i < n) {
-            float dot = 0.f;
-            if (pc_fz) {
-                for (int kk = 0; kk < K; ++kk) dot = fmaf(ks[i * KP + kk], gk[j * KP + kk], dot);
-                val = bs[i] * dot;
-            } else if (pc) {
-                // sum_d k_id k_jd exp(g_id - g_jd): each channel its own decay
-                for (int kk = 0; kk < K; ++kk)
-                    dot = fmaf(ks[i * KP + kk] * ks[j * KP + kk],
-                               expf(gk[i * KP + kk] - gk[j * KP + kk]), dot);
-                val = bs[i] * dot;
-            } else {
-                for (int kk = 0; kk < K; ++kk) dot = fmaf(ks[i * KP + kk], ks[j * KP + kk], dot);
-                val = bs[i] * dot * expf(gs[i] - gs[j]);
+    // L, 4 x 4 tiles per thread (rows 4 ti.., columns 4 tj..; tiles above the
+    // diagonal stay 0)
+    {
+        const int i0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+        float acc[4][4] = {};
+        if (c0 < i0 + 3 && i0 < n) {
+            const float *kb = pc_fz ? gk : ks;
+            for (int kk = 0; kk < K; ++kk) {
+                float ki[4], kj[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    ki[r] = ks[(i0 + r) * KP + kk];
+                    kj[r] = kb[(c0 + r) * KP + kk];
+                }
+                if (pc && !pc_fz) {
+                    // sum_d k_id k_jd exp(g_id - g_jd): each channel its own decay
+                    float gi[4], gj[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        gi[r] = gk[(i0 + r) * KP + kk];
+                        gj[r] = gk[(c0 + r) * KP + kk];
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            acc[r][cc] = fmaf(ki[r] * kj[cc], expf(gi[r] - gj[cc]), acc[r][cc]);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) acc[r][cc] = fmaf(ki[r], kj[cc], acc[r][cc]);
+                }
             }
         }
-        Ls[i * 65 + j] = val;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int i = i0 + r, j = c0 + cc;
+                float val = 0.f;
+                if (i > j && i < n)
+                    val = bs[i] * (pc ? acc[r][cc] : acc[r][cc] * expf(gs[i] - gs[j]));
+                Ls[i * 65 + j] = val;
+            }
     }
     __syncthreads();
 
@@ -175,29 +204,68 @@ wy_prepare_kernel(const T *__restrict__ k, const T *__restrict__ v, const float 
     }
     __syncthreads();
 
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        A_ws[tok(b, t0 + i, h, T_pad, H) * kChunk + j] = As[i * 65 + j];
+#pragma unroll 4
+    for (int idx = tid; idx < kChunk * 16; idx += kThreads) {
+        const int i = idx >> 4, j4 = (idx & 15) * 4;
+        *reinterpret_cast<float4 *>(&A_ws[tok(b, t0 + i, h, T_pad, H) * kChunk + j4]) =
+            make_float4(As[i * 65 + j4], As[i * 65 + j4 + 1], As[i * 65 + j4 + 2], As[i * 65 + j4 + 3]);
     }
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, kk = idx - i * K;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(As[i * 65 + j], ks[j * KP + kk], acc);
-        w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk] = acc;
+    // w = A (scaled k), 4 x 4 tiles; A is 0 above the diagonal, so a tile of
+    // rows i0.. needs columns j < i0 + 4 only
+    for (int t = tid; t < 16 * (K / 4); t += kThreads) {
+        const int i0 = (t / (K / 4)) * 4, c0 = (t % (K / 4)) * 4;
+        float acc[4][4] = {};
+        for (int j = 0; j < i0 + 4; ++j) {
+            float kv[4], av[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                kv[r] = ks[j * KP + c0 + r];
+                av[r] = As[(i0 + r) * 65 + j];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) acc[r][cc] = fmaf(av[r], kv[cc], acc[r][cc]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4 *>(&w_ws[tok(b, t0 + i0 + r, h, T_pad, H) * K + c0]) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
     }
     for (int vs = 0; vs < V; vs += 64) {
         __syncthreads();
-#pragma unroll 8
-        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
-            const int j = idx >> 6, nn = idx & 63;
-            xs[j * 65 + nn] = j < n ? bs[j] * to_f32(v[tok(b, t0 + j, h, Tn, H) * V + vs + nn]) : 0.f;
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * 16; idx += kThreads) {
+            const int j = idx >> 4, n4 = (idx & 15) * 4;
+            const int64_t r = tok(b, t0 + j, h, Tn, H) * V + vs + n4;
+            const float bj = j < n ? bs[j] : 0.f;
+            float4 x;
+            x.x = j < n ? bj * to_f32(v[r]) : 0.f;
+            x.y = j < n ? bj * to_f32(v[r + 1]) : 0.f;
+            x.z = j < n ? bj * to_f32(v[r + 2]) : 0.f;
+            x.w = j < n ? bj * to_f32(v[r + 3]) : 0.f;
+            *reinterpret_cast<float4 *>(&xs[j * 64 + n4]) = x;
         }
         __syncthreads();
-        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
-            const int i = idx >> 6, nn = idx & 63;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc = fmaf(As[i * 65 + j], xs[j * 65 + nn], acc);
-            u_ws[tok(b, t0 + i, h, T_pad, H) * V + vs + nn] = acc;
+        {
+            // u = A (v * beta), one 4 x 4 tile per thread
+            const int i0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+            float acc[4][4] = {};
+            for (int j = 0; j < i0 + 4; ++j) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(&xs[j * 64 + c0]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float av = As[(i0 + r) * 65 + j];
+                    acc[r][0] = fmaf(av, x4.x, acc[r][0]);
+                    acc[r][1] = fmaf(av, x4.y, acc[r][1]);
+                    acc[r][2] = fmaf(av, x4.z, acc[r][2]);
+                    acc[r][3] = fmaf(av, x4.w, acc[r][3]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<float4 *>(&u_ws[tok(b, t0 + i0 + r, h, T_pad, H) * V + vs + c0]) =
+                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
     }
 }
@@ -220,8 +288,8 @@ chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float
     float *hs = smem;                   // [K][kBV]
     float *ws = hs + K * kBV;           // [64][K+1]
     float *ks = ws + kChunk * KP;       // [64][K+1]
-    float *vs = ks + kChunk * KP;       // [64][kBV + 1]: u, then v_new, then v_gated
-    constexpr int VP = kBV + 1;
+    float *vs = ks + kChunk * KP;       // [64][kBV]: u, then v_new, then v_gated
+    constexpr int VP = kBV;             // rows of 16 floats, read as float4
     // per-channel decay: the chunk's g, [64][K+1]
     const bool pc = flags & GDN_FLAG_PER_CHANNEL_DECAY;
     float *gk = vs + kChunk * VP;
@@ -237,44 +305,59 @@ chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float
         const int n = min(kChunk, Tn - t0);
         __syncthreads();
         const int64_t hslot = ((static_cast<int64_t>(b) * NT + c) * H + h) * K * V;
-#pragma unroll 8
-        for (int idx = tid; idx < K * kBV; idx += kThreads) {
-            const int kk = idx / kBV, nn = idx - kk * kBV;
-            h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + nn] = hs[idx];
+        // global traffic in 16-byte pieces: 4 consecutive floats (or k values)
+#pragma unroll 4
+        for (int idx = tid; idx < K * kBV / 4; idx += kThreads) {
+            const int kk = idx / (kBV / 4), n4 = (idx - kk * (kBV / 4)) * 4;
+            *reinterpret_cast<float4 *>(&h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + n4]) =
+                *reinterpret_cast<const float4 *>(&hs[kk * kBV + n4]);
         }
         if (tid < kChunk) gs[tid] = (!pc && tid < n) ? g[tok(b, t0 + tid, h, Tn, H)] : 0.f;
-#pragma unroll 8
-        for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-            const int i = idx / K, kk = idx - i * K;
-            ws[i * KP + kk] = w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk];
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * K / 4; idx += kThreads) {
+            const int i = idx / (K / 4), kk = (idx - i * (K / 4)) * 4;
+            const float4 wv = *reinterpret_cast<const float4 *>(&w_ws[tok(b, t0 + i, h, T_pad, H) * K + kk]);
+            ws[i * KP + kk] = wv.x;
+            ws[i * KP + kk + 1] = wv.y;
+            ws[i * KP + kk + 2] = wv.z;
+            ws[i * KP + kk + 3] = wv.w;
             const int64_t r = tok(b, t0 + i, h, Tn, H);
-            ks[i * KP + kk] = i < n ? to_f32(k[r * K + kk]) * (rk ? rk[r] : 1.f) : 0.f;
-            if (pc) gk[i * KP + kk] = i < n ? g[r * K + kk] : 0.f;
+            const float sc = i < n ? (rk ? rk[r] : 1.f) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ks[i * KP + kk + e] = i < n ? to_f32(k[r * K + kk + e]) * sc : 0.f;
+            if (pc) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) gk[i * KP + kk + e] = i < n ? g[r * K + kk + e] : 0.f;
+            }
         }
-#pragma unroll 8
-        for (int idx = tid; idx < kChunk * kBV; idx += kThreads) {
-            const int i = idx / kBV, nn = idx - i * kBV;
-            vs[i * VP + nn] = u_ws[tok(b, t0 + i, h, T_pad, H) * V + v0 + nn];
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * kBV / 4; idx += kThreads) {
+            const int i = idx / (kBV / 4), n4 = (idx - i * (kBV / 4)) * 4;
+            *reinterpret_cast<float4 *>(&vs[i * VP + n4]) =
+                *reinterpret_cast<const float4 *>(&u_ws[tok(b, t0 + i, h, T_pad, H) * V + v0 + n4]);
         }
         __syncthreads();
-        // v_new = u - w @ h
-        float vnew[kChunk * kBV / kThreads];
-#pragma unroll
-        for (int r = 0; r < kChunk * kBV / kThreads; ++r) {
-            const int idx = tid + r * kThreads;
-            const int i = idx / kBV, nn = idx - i * kBV;
-            float acc = vs[i * VP + nn];
-            for (int kk = 0; kk < K; ++kk) acc = fmaf(-ws[i * KP + kk], hs[kk * kBV + nn], acc);
-            vnew[r] = acc;
-            vn_ws[tok(b, t0 + i, h, T_pad, H) * V + v0 + nn] = acc;
+        // v_new = u - w @ h: thread (i, 4 columns), one w and one float4 of h
+        // per four products
+        static_assert(kChunk * kBV == 4 * kThreads, "v_new tiling");
+        const int vi = tid >> 2, vn0 = (tid & 3) * 4;
+        float4 vnew = *reinterpret_cast<const float4 *>(&vs[vi * VP + vn0]);
+#pragma unroll 4
+        for (int kk = 0; kk < K; ++kk) {
+            const float wv = ws[vi * KP + kk];
+            const float4 h4 = *reinterpret_cast<const float4 *>(&hs[kk * kBV + vn0]);
+            vnew.x = fmaf(-wv, h4.x, vnew.x);
+            vnew.y = fmaf(-wv, h4.y, vnew.y);
+            vnew.z = fmaf(-wv, h4.z, vnew.z);
+            vnew.w = fmaf(-wv, h4.w, vnew.w);
         }
+        *reinterpret_cast<float4 *>(&vn_ws[tok(b, t0 + vi, h, T_pad, H) * V + v0 + vn0]) = vnew;
         __syncthreads();
         const float glast = gs[n - 1];
-#pragma unroll
-        for (int r = 0; r < kChunk * kBV / kThreads; ++r) {
-            const int idx = tid + r * kThreads;
-            const int i = idx / kBV, nn = idx - i * kBV;
-            vs[i * VP + nn] = i < n ? (pc ? vnew[r] : vnew[r] * expf(glast - gs[i])) : 0.f;
+        {
+            const float gate = vi < n ? (pc ? 1.f : expf(glast - gs[vi])) : 0.f;
+            *reinterpret_cast<float4 *>(&vs[vi * VP + vn0]) =
+                make_float4(vnew.x * gate, vnew.y * gate, vnew.z * gate, vnew.w * gate);
         }
         if (pc) {
             // per channel the gate sits on k: k_id exp(g_last,d - g_id)
@@ -284,13 +367,32 @@ chunk_h_kernel(const T *__restrict__ k, const float *__restrict__ g, const float
             }
         }
         __syncthreads();
-        // h = h * exp(g_last) + k^T @ v_gated (row d by exp(g_last,d) per channel)
+        // h = h * exp(g_last) + k^T @ v_gated (row d by exp(g_last,d) per channel):
+        // thread (K / 128 row pairs, 4 columns), two k values and one float4 of
+        // v_gated per eight products
         const float decay = expf(glast);
-        for (int idx = tid; idx < K * kBV; idx += kThreads) {
-            const int kk = idx / kBV, nn = idx - kk * kBV;
-            float acc = hs[idx] * (pc ? expf(gk[(n - 1) * KP + kk]) : decay);
-            for (int i = 0; i < n; ++i) acc = fmaf(ks[i * KP + kk], vs[i * VP + nn], acc);
-            hs[idx] = acc;
+        for (int kb = 0; kb < K; kb += 128) {
+            const int kk0 = kb + (tid >> 2) * 2, hn0 = (tid & 3) * 4;
+            if (kk0 >= K) break;   // K = 64: half the threads have no rows
+            float4 a0 = *reinterpret_cast<const float4 *>(&hs[kk0 * kBV + hn0]);
+            float4 a1 = *reinterpret_cast<const float4 *>(&hs[(kk0 + 1) * kBV + hn0]);
+            const float d0 = pc ? expf(gk[(n - 1) * KP + kk0]) : decay;
+            const float d1 = pc ? expf(gk[(n - 1) * KP + kk0 + 1]) : decay;
+            a0 = make_float4(a0.x * d0, a0.y * d0, a0.z * d0, a0.w * d0);
+            a1 = make_float4(a1.x * d1, a1.y * d1, a1.z * d1, a1.w * d1);
+#pragma unroll 4
+            for (int i = 0; i < n; ++i) {
+                const float k0 = ks[i * KP + kk0], k1 = ks[i * KP + kk0 + 1];
+                const float4 v4 = *reinterpret_cast<const float4 *>(&vs[i * VP + hn0]);
+                a0.x = fmaf(k0, v4.x, a0.x); a0.y = fmaf(k0, v4.y, a0.y);
+                a0.z = fmaf(k0, v4.z, a0.z); a0.w = fmaf(k0, v4.w, a0.w);
+                a1.x = fmaf(k1, v4.x, a1.x); a1.y = fmaf(k1, v4.y, a1.y);
+                a1.z = fmaf(k1, v4.z, a1.z); a1.w = fmaf(k1, v4.w, a1.w);
+            }
+            // every thread read its own rows of hs above; all reads of hs in this
+            // chunk (v_new) finished before the last barrier
+            *reinterpret_cast<float4 *>(&hs[kk0 * kBV + hn0]) = a0;
+            *reinterpret_cast<float4 *>(&hs[(kk0 + 1) * kBV + hn0]) = a1;
         }
     }
     if (h_final) {
@@ -324,11 +426,11 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
     float *qs = smem;                  // [64][K+1]
     float *ks = qs + kChunk * KP;      // [64][K+1]
     float *Ps = ks + kChunk * KP;      // [64][65]
-    float *hs = Ps + kChunk * 65;      // [K][65]
-    float *vs = hs + K * 65;           // [64][65]
+    float *hs = Ps + kChunk * 65;      // [K][64] (rows read as float4)
+    float *vs = hs + K * 64;           // [64][64]
     // [64][V + 1] fp32 o rows (output stage only), sharing its space with the
     // per-channel g [64][K + 1], which is not read once o rows are written
-    float *os = vs + kChunk * 65;
+    float *os = vs + kChunk * 64;
     const int OP = V + 1;
     const bool pc = flags & GDN_FLAG_PER_CHANNEL_DECAY;
     float *gk = os;
@@ -351,25 +453,50 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
     // per-channel decay, factored (qs <- q exp(g - r), gk <- k exp(r - g)) when
     // the chunk's decays allow
     const bool pc_fz = pc && factor_per_channel(qs, ks, gk, rs, KP, K, n);
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float val = 0.f;
-        if (j <= i && i < n) {
-            float dot = 0.f;
-            if (pc_fz) {
-                for (int kk = 0; kk < K; ++kk) dot = fmaf(qs[i * KP + kk], gk[j * KP + kk], dot);
-                val = dot;
-            } else if (pc) {
-                for (int kk = 0; kk < K; ++kk)
-                    dot = fmaf(qs[i * KP + kk] * ks[j * KP + kk],
-                               expf(gk[i * KP + kk] - gk[j * KP + kk]), dot);
-                val = dot;
-            } else {
-                for (int kk = 0; kk < K; ++kk) dot = fmaf(qs[i * KP + kk], ks[j * KP + kk], dot);
-                val = dot * expf(gs[i] - gs[j]);
+    // Thread (ti, tj) owns rows 4 ti .. 4 ti + 3 and columns 4 tj .. 4 tj + 3 of
+    // each 64 x 64 product: eight shared loads (or five with a float4) per
+    // sixteen products.
+    const int i0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    {
+        float acc[4][4] = {};
+        if (c0 <= i0 + 3 && i0 < n) {   // tiles wholly above the diagonal stay 0
+            const float *kb = pc_fz ? gk : ks;
+            for (int kk = 0; kk < K; ++kk) {
+                float qv[4], kv[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    qv[r] = qs[(i0 + r) * KP + kk];
+                    kv[r] = kb[(c0 + r) * KP + kk];
+                }
+                if (pc && !pc_fz) {
+                    float gq[4], gj[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        gq[r] = gk[(i0 + r) * KP + kk];
+                        gj[r] = gk[(c0 + r) * KP + kk];
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            acc[r][cc] = fmaf(qv[r] * kv[cc], expf(gq[r] - gj[cc]), acc[r][cc]);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) acc[r][cc] = fmaf(qv[r], kv[cc], acc[r][cc]);
+                }
             }
         }
-        Ps[i * 65 + j] = val;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int i = i0 + r, j = c0 + cc;
+                float val = 0.f;
+                if (j <= i && i < n) val = pc ? acc[r][cc] : acc[r][cc] * expf(gs[i] - gs[j]);
+                Ps[i * 65 + j] = val;
+            }
     }
     if (pc) {
         // inter term per channel: (q_i * exp(g_i)) . h; gs stays 0 so exp(gs) = 1
@@ -383,28 +510,58 @@ chunk_o_kernel(const T *__restrict__ q, const T *__restrict__ k, const float *__
     for (int v0 = 0; v0 < V; v0 += 64) {
         __syncthreads();
 #pragma unroll 8
-        for (int idx = tid; idx < K * 64; idx += kThreads) {
-            const int kk = idx >> 6, nn = idx & 63;
-            hs[kk * 65 + nn] = h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + nn];
+        for (int idx = tid; idx < K * 16; idx += kThreads) {
+            const int kk = idx >> 4, n4 = (idx & 15) * 4;
+            *reinterpret_cast<float4 *>(&hs[kk * 64 + n4]) = *reinterpret_cast<const float4 *>(
+                &h_ws[hslot + static_cast<int64_t>(kk) * V + v0 + n4]);
         }
 #pragma unroll 8
-        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
-            const int j = idx >> 6, nn = idx & 63;
-            vs[j * 65 + nn] = vn_ws[tok(b, t0 + j, h, T_pad, H) * V + v0 + nn];
+        for (int idx = tid; idx < kChunk * 16; idx += kThreads) {
+            const int j = idx >> 4, n4 = (idx & 15) * 4;
+            *reinterpret_cast<float4 *>(&vs[j * 64 + n4]) = *reinterpret_cast<const float4 *>(
+                &vn_ws[tok(b, t0 + j, h, T_pad, H) * V + v0 + n4]);
         }
         __syncthreads();
-        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
-            const int i = idx >> 6, nn = idx & 63;
-            if (i >= n) continue;
-            float inter = 0.f;
-            for (int kk = 0; kk < K; ++kk) inter = fmaf(qs[i * KP + kk], hs[kk * 65 + nn], inter);
-            float intra = 0.f;
-            for (int j = 0; j <= i; ++j) intra = fmaf(Ps[i * 65 + j], vs[j * 65 + nn], intra);
-            const float oi = scale * (expf(gs[i]) * inter + intra);
-            if (gate)
-                os[i * OP + v0 + nn] = oi;
-            else
-                store_as(&o[tok(b, t0 + i, h, Tn, H) * V + v0 + nn], oi);
+        if (i0 < n) {
+            float inter[4][4] = {}, intra[4][4] = {};
+            for (int kk = 0; kk < K; ++kk) {
+                const float4 h4 = *reinterpret_cast<const float4 *>(&hs[kk * 64 + c0]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float qv = qs[(i0 + r) * KP + kk];
+                    inter[r][0] = fmaf(qv, h4.x, inter[r][0]);
+                    inter[r][1] = fmaf(qv, h4.y, inter[r][1]);
+                    inter[r][2] = fmaf(qv, h4.z, inter[r][2]);
+                    inter[r][3] = fmaf(qv, h4.w, inter[r][3]);
+                }
+            }
+            // P is 0 above the diagonal and past n, so the tile's last row bounds j
+            const int jmax = min(n, i0 + 4);
+            for (int j = 0; j < jmax; ++j) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(&vs[j * 64 + c0]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float pv = Ps[(i0 + r) * 65 + j];
+                    intra[r][0] = fmaf(pv, v4.x, intra[r][0]);
+                    intra[r][1] = fmaf(pv, v4.y, intra[r][1]);
+                    intra[r][2] = fmaf(pv, v4.z, intra[r][2]);
+                    intra[r][3] = fmaf(pv, v4.w, intra[r][3]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r;
+                if (i >= n) break;
+                const float e = expf(gs[i]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const float oi = scale * (e * inter[r][cc] + intra[r][cc]);
+                    if (gate)
+                        os[i * OP + v0 + c0 + cc] = oi;
+                    else
+                        store_as(&o[tok(b, t0 + i, h, Tn, H) * V + v0 + c0 + cc], oi);
+                }
+            }
         }
     }
     if (gate) {
@@ -435,15 +592,16 @@ __global__ void copy_state_kernel(const float *__restrict__ h0, float *__restric
 }
 
 size_t prepare_smem(int K, bool pc) {
-    return sizeof(float) * (kChunk * (K + 1) + 3 * kChunk * 65 + (pc ? kChunk * (K + 1) : 0));
+    return sizeof(float) * (kChunk * (K + 1) + 2 * kChunk * 65 + kChunk * 64 +
+                            (pc ? kChunk * (K + 1) : 0));
 }
 size_t chunk_h_smem(int K, bool pc) {
-    return sizeof(float) * (K * kBV + 2 * kChunk * (K + 1) + kChunk * (kBV + 1) +
+    return sizeof(float) * (K * kBV + 2 * kChunk * (K + 1) + kChunk * kBV +
                             (pc ? kChunk * (K + 1) : 0));
 }
 size_t chunk_o_smem(int K, int V, bool normed, bool pc) {
     const int tail = std::max(normed ? kChunk * (V + 1) : 0, pc ? kChunk * (K + 1) : 0);
-    return sizeof(float) * (2 * kChunk * (K + 1) + kChunk * 65 + K * 65 + kChunk * 65 + tail);
+    return sizeof(float) * (2 * kChunk * (K + 1) + kChunk * 65 + K * 64 + kChunk * 64 + tail);
 }
 
 template <typename T>
