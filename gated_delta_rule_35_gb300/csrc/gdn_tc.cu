@@ -789,16 +789,24 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
-    // may start while the WY kernel before it in the stream finishes (it waits
-    // for that kernel's output after its own setup)
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = nrank;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
+    int nattr = 0;
+    // With more CTAs than SMs the kernel may start while the WY kernel before
+    // it in the stream finishes (it waits for that kernel's output after its
+    // own setup), which saves about 5 us on B8 H64 T8192. With one wave or
+    // less the early start gains nothing and cost 20 us (1.7%) on
+    // B1 H32 T32768, so those grids launch after the WY kernel ends.
+    if (ctas > sms) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (nrank) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = nrank;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr++].val.clusterDim.z = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = nrank ? 2 : 1;
+    cfg.numAttrs = nattr;
     // kernel arguments, in order, for the untyped launch call
     const float *g_arg = a.g_chunk(), *h0_arg = a.h0, *rk_arg = a.rk, *nw_arg = a.norm_w;
     float *hf_arg = a.h_final;
