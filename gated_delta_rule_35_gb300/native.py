@@ -7,6 +7,7 @@ PyTorch fallback: if the library is missing, every call raises.
 from __future__ import annotations
 
 import ctypes
+import threading
 from pathlib import Path
 
 import torch
@@ -313,6 +314,10 @@ def check_device_status(workspace, stream=None) -> int:
 
 
 _host_streams: dict = {}
+_host_buffers: dict = {}
+_host_plans: dict = {}
+_host_events: dict = {}
+_host_lock = threading.Lock()
 
 
 def _pipeline_streams(dev, n: int):
@@ -323,15 +328,54 @@ def _pipeline_streams(dev, n: int):
     return _host_streams[key]
 
 
+def _host_plan(B, T, H, K, V, dtype, algo, flags, pieces):
+    """(problem, device bytes) of one host call, computed once per shape."""
+    key = (B, T, H, K, V, dtype, algo, flags, pieces)
+    plan = _host_plans.get(key)
+    if plan is None:
+        p = problem(B, T, H, K, V, dtype, algo, flags)
+        need = int(lib().gdn_chunk_fwd_host_bytes(ctypes.byref(p), int(pieces)))
+        if need == 0:
+            raise GdnError(GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_host_bytes")
+        if len(_host_plans) > 64:
+            _host_plans.clear()
+        plan = _host_plans[key] = (p, need)
+    return plan
+
+
+def _host_buffer(dev, need: int):
+    """The device buffer of the host calls on ``dev``, grown on demand and kept:
+    every call has finished with it when it returns."""
+    buf = _host_buffers.get(dev.index)
+    if buf is None or buf.numel() < need:
+        _host_buffers[dev.index] = None
+        buf = _host_buffers[dev.index] = torch.empty(need, dtype=torch.uint8, device=dev)
+    return buf
+
+
+def _host_out(t, shape, dtype, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    if t.device.type != "cpu" or not t.is_contiguous() or tuple(t.shape) != shape or t.dtype != dtype:
+        raise ValueError(f"{name} must be a contiguous host tensor {shape} of {dtype}")
+    return t
+
+
 def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
                    algo: str = "auto", device=None, raw_g: bool = False, qk_l2norm: bool = False,
-                   pieces: int = 4):
+                   pieces: int = 0, out=None, final_state=None):
     """Host-tensor front end (gdn_chunk_fwd_host): host inputs in, host outputs
-    out; returns when o (and h_final) are in pinned host tensors. Pinned inputs
-    let the library overlap the copies of one span of T (up to ``pieces``
-    64-aligned spans) with the kernels of the previous one. torch supplies the
-    device buffer and the two side streams."""
+    out; returns when o (and h_final) are in host tensors. Pinned inputs let the
+    library overlap the copies of one span of T (up to ``pieces`` 64-aligned
+    spans; 0: the library's choice) with the kernels of the previous one.
+    ``out`` / ``final_state``:
+    host tensors [B, T, H, V] / [B, H, K, V] fp32 to write into (pinned ones
+    allocated when None). torch supplies the device buffer and the two side
+    streams, both kept per device for later calls; a lock serialises callers,
+    and the work waits for what the caller's current stream has queued."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     B, T, H, K = q.shape
     V = v.shape[-1]
     for t in (q, k, v, g, beta, h0):
@@ -341,26 +385,24 @@ def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_s
         raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
-    p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm))
-    need = int(lib().gdn_chunk_fwd_host_bytes(ctypes.byref(p), int(pieces)))
-    if need == 0:
-        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_host_bytes")
-    with torch.cuda.device(dev):
-        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+    p, need = _host_plan(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm), pieces)
+    ho = _host_out(out, (B, T, H, V), q.dtype, "out")
+    hhf = _host_out(final_state, (B, H, K, V), torch.float32, "final_state") \
+        if output_final_state else None
+    with _host_lock:
+        buf = _host_buffer(dev, need)
         sa, sb = _pipeline_streams(dev, 2)
-        main = torch.cuda.current_stream(dev)
-        sa.wait_stream(main)
-        sb.wait_stream(main)
-        ho = torch.empty((B, T, H, V), dtype=q.dtype, pin_memory=True)
-        hhf = torch.empty((B, H, K, V), dtype=torch.float32, pin_memory=True) \
-            if output_final_state else None
+        ready = _host_events.get(dev.index)
+        if ready is None:
+            ready = _host_events[dev.index] = torch.cuda.Event()
+        ready.record(torch.cuda.current_stream(dev))
+        sa.wait_event(ready)
+        sb.wait_event(ready)
         st = lib().gdn_chunk_fwd_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                       _ptr(beta), float(scale), _ptr(h0), _ptr(ho), _ptr(hhf),
                                       _ptr(buf), need, int(pieces),
                                       ctypes.c_void_p(sa.cuda_stream),
                                       ctypes.c_void_p(sb.cuda_stream))
-        buf.record_stream(sa)
-        buf.record_stream(sb)
     if st != GDN_OK:
         raise GdnError(st, "gdn_chunk_fwd_host")
     return ho, hhf

@@ -170,7 +170,8 @@ GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p,
  * (pinned) host buffers let the copies run asynchronously and overlap.
  *
  * The sequence is cut into up to `pieces` spans of T (1..16 spans, each a
- * multiple of 64 tokens, all batch rows and heads at once) so that the
+ * multiple of 64 tokens, all batch rows and heads at once; pieces == 0 lets
+ * the library pick about one span per 32 MiB of inputs, 3 to 16) so that the
  * host-to-device copies of one span (on `stream_a`) overlap the kernels and the
  * device-to-host copies of the previous one (on `stream_b`); each span starts
  * from the previous span's final state. The call creates and destroys one

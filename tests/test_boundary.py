@@ -53,6 +53,27 @@ def test_workspace_bytes():
     assert native.workspace_bytes(native.problem(1, 0, 1, 64, 64, 0)) > 0          # T = 0 valid
 
 
+
+def test_host_entry_span_count():
+    """gdn_chunk_fwd_host_bytes: 1..16 spans, or 0 for the library's choice of
+    about one span per 32 MiB of inputs (3 to 16). The buffer holds one span's
+    workspace, so its size tells the span count apart."""
+    L = native.lib()
+
+    def host_bytes(p, pieces):
+        return int(L.gdn_chunk_fwd_host_bytes(ctypes.byref(p), pieces))
+
+    short = native.problem(4, 2048, 16, 128, 128, native.GDN_BF16)    # 102 MB of inputs
+    long = native.problem(1, 32768, 32, 128, 128, native.GDN_BF16)    # 814 MB
+    tiny = native.problem(1, 640, 1, 64, 64, native.GDN_BF16)         # 0.2 MB
+    assert host_bytes(short, 0) == host_bytes(short, 3) != host_bytes(short, 4)
+    assert host_bytes(long, 0) == host_bytes(long, 16) != host_bytes(long, 8)
+    assert host_bytes(tiny, 0) == host_bytes(tiny, 3) != host_bytes(tiny, 1)
+    for bad in (-1, 17):
+        assert host_bytes(short, bad) == 0
+    # one span's workspace at most: the buffer shrinks as the span count grows
+    assert host_bytes(long, 1) > host_bytes(long, 4) > host_bytes(long, 16)
+
 @pytest.mark.parametrize("shape,status", [
     ((0, 64, 1, 64, 64), native.GDN_ERR_INVALID_ARG),
     ((1, -1, 1, 64, 64), native.GDN_ERR_INVALID_ARG),

@@ -55,3 +55,32 @@ def test_host_entry_without_final_state_and_empty():
     h0 = torch.randn(2, 3, 64, 64)
     ho, hhf = chunk_fwd_host(e, e, e, ef, ef, 1.0, h0)
     assert ho.shape == (2, 0, 3, 64) and torch.equal(hhf, h0)
+
+
+def test_host_entry_into_given_outputs_and_growing_buffer():
+    """Caller-owned outputs are written in place; a larger problem after a
+    smaller one grows the kept device buffer, and a smaller one after it
+    reuses it, each matching the device entry."""
+    for B, T, H in [(1, 130, 2), (2, 700, 4), (1, 64, 1)]:
+        x = make_inputs(B, T, H, 128, 128, dtype="bf16", seed=97 + T, h0_std=0.1)
+        h = pinned(x)
+        out = torch.full((B, T, H, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+        fs = torch.full((B, H, 128, 128), float("nan")).pin_memory()
+        ho, hhf = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], 1.0, h["h0"],
+                                 pieces=1, out=out, final_state=fs)
+        assert ho.data_ptr() == out.data_ptr() and hhf.data_ptr() == fs.data_ptr()
+        d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+        o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"])
+        torch.cuda.synchronize()
+        assert torch.equal(out, o.cpu()) and torch.equal(fs, hf.cpu()), (B, T, H)
+
+
+def test_host_entry_rejects_bad_outputs():
+    x = pinned(make_inputs(1, 64, 1, 64, 64, dtype="bf16", seed=98))
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None)
+    with pytest.raises(ValueError):
+        chunk_fwd_host(*args, out=torch.empty(1, 64, 1, 64, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        chunk_fwd_host(*args, final_state=torch.empty(1, 1, 64, 32))
+    with pytest.raises(ValueError):
+        chunk_fwd_host(*args, out=torch.empty(1, 64, 1, 64, dtype=torch.bfloat16, device="cuda"))
