@@ -389,7 +389,7 @@ def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_s
     ho = _host_out(out, (B, T, H, V), q.dtype, "out")
     hhf = _host_out(final_state, (B, H, K, V), torch.float32, "final_state") \
         if output_final_state else None
-    with _host_lock:
+    with _host_lock, torch.cuda.device(dev):
         buf = _host_buffer(dev, need)
         sa, sb = _pipeline_streams(dev, 2)
         ready = _host_events.get(dev.index)
