@@ -46,27 +46,29 @@ template <int K>
 struct WyLayout {
     static constexpr int KB = K / 64;
     // k tile (K-major, KB blocks of 8 KB); after the Gram MMA the first 16 KB
-    // hold the stacked operand [N1; N2]
+    // hold the stacked operand [N1; N2], read only by the first merge product
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kKBytes = (KB * 8192 > 16384) ? KB * 8192 : 16384;
     static constexpr uint32_t kN = 0;
     static constexpr uint32_t kXU = kKBytes;               // [X; U] stacked, then A0 (bf16)
-    // One 8 KB region, four lives: the fp32 diagonal blocks [4][16][17] (dead
-    // once X is in [X; U]), Y1, Y2 (read by the last MMA), and finally the
+    // The fp32 diagonal blocks [4][16][17] live in the U half of [X; U] until
+    // X is built from them (U is written after the first merge product).
+    static constexpr uint32_t kLd = kXU + 8192;
+    // One 8 KB region in the [N2] half of [N1; N2], free once the first merge
+    // product has read it: Y1, Y2 (read by the last product), and finally the
     // A diag(beta) staging of the TMA store.
-    static constexpr uint32_t kY = kXU + 16384;
-    static constexpr uint32_t kLd = kY;
+    static constexpr uint32_t kY = kN + 8192;
     static constexpr uint32_t kOut = kY;
     // g, beta, beta exp(g) r, cf, r (64 floats each), a scan total; barriers
-    static constexpr uint32_t kMisc = kY + 8192;
+    static constexpr uint32_t kMisc = kXU + 16384;
     static constexpr uint32_t kBar = kMisc + 1344;
     static constexpr uint32_t kBytes = kBar + 256;
+    static_assert(16 * 17 * 4 * 4 <= 8192, "diagonal blocks fit the U half");
 };
 
 template <int K>
-// Five CTAs per SM (96 registers, a few spilled; 43.6 KB of shared memory
-// each): 2048 chunks then take three waves of 760 instead of four of 608.
-__global__ void __launch_bounds__(kWyThreads, 5)
+// Six CTAs per SM (35.4 KB of shared memory and 64 TMEM columns each).
+__global__ void __launch_bounds__(kWyThreads, 6)
 gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_a,
                  const float *__restrict__ g, const float *__restrict__ beta, int T, int H,
                  uint32_t *status, int flags, float *__restrict__ g_cum, float *__restrict__ rk_out) {
