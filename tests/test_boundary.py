@@ -211,3 +211,16 @@ def test_per_channel_flag_routes_to_simt():
     plain = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "simt")
     assert native.workspace_bytes(p_simt) - native.workspace_bytes(plain) >= 2 * 100 * 3 * 127 * 4 - 256
     assert native.launches(p_auto) == ["wy_prepare_kernel", "chunk_h_kernel", "chunk_o_kernel"]
+
+
+def test_host_binding_output_validation():
+    """chunk_fwd_host's caller-owned outputs are checked on the host before any
+    device work: shape, dtype, contiguity and host residency."""
+    import torch
+    good = torch.empty(2, 64, 3, 64, dtype=torch.bfloat16)
+    assert native._host_out(good, (2, 64, 3, 64), torch.bfloat16, "out") is good
+    for bad in (torch.empty(2, 64, 3, 32, dtype=torch.bfloat16),
+                torch.empty(2, 64, 3, 64, dtype=torch.float32),
+                torch.empty(2, 3, 64, 64, dtype=torch.bfloat16).transpose(1, 2)):
+        with pytest.raises(ValueError):
+            native._host_out(bad, (2, 64, 3, 64), torch.bfloat16, "out")
