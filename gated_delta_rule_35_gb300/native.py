@@ -158,6 +158,15 @@ def _check_inputs(q, k, v, g, beta, h0, per_channel: bool = False):
     return B, T, H, K, V
 
 
+def _given(t, shape, dtype, dev, name):
+    """A caller-supplied output buffer, checked against what the kernels write
+    into it: the library knows only the problem's sizes, so a smaller or
+    strided buffer would be written past its end."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != dev or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor {tuple(shape)} on {dev}")
+    return t
+
+
 def _output_norm(gate, weight, eps, shape, like):
     if gate is None and weight is None:
         return None
@@ -195,12 +204,17 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     need = workspace_bytes(p)
     if need == 0:
         raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_chunk_fwd_workspace_bytes")
+    if workspace is not None and (workspace.dtype != torch.uint8 or workspace.device != q.device
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    o = _given(out, (B, T, H, V), q.dtype, q.device, "out") if out is not None else \
+        torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
     hf = None
     if output_final_state:
-        hf = final_state if final_state is not None else \
+        hf = _given(final_state, (B, H, K, V), torch.float32, q.device, "final_state") \
+            if final_state is not None else \
             torch.empty((B, H, K, V), dtype=torch.float32, device=q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
@@ -288,7 +302,8 @@ def decode_step(q, k, v, gamma, beta, state, scale: float = 1.0, state_out=None,
     for t in (q, k, v, gamma, beta, state, so):
         if not t.is_contiguous() or t.device != dev:
             raise ValueError("all tensors must be contiguous and on the same device")
-    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
+    o = _given(out, (B, T, H, V), q.dtype, dev, "out") if out is not None else \
+        torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
     p = problem(B, T, H, K, V, q.dtype, "auto", flags_of(False, qk_l2norm, per_channel_decay))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)

@@ -224,3 +224,20 @@ def test_host_binding_output_validation():
                 torch.empty(2, 3, 64, 64, dtype=torch.bfloat16).transpose(1, 2)):
         with pytest.raises(ValueError):
             native._host_out(bad, (2, 64, 3, 64), torch.bfloat16, "out")
+
+
+def test_device_output_buffers_are_checked():
+    """chunk_fwd / decode_step accept caller-owned o, h_final and workspace only
+    when the kernels cannot write past them: exact shape, dtype, device and a
+    contiguous layout."""
+    import torch
+    cpu = torch.device("cpu")
+    good = torch.empty(2, 64, 3, 64, dtype=torch.bfloat16)
+    assert native._given(good, (2, 64, 3, 64), torch.bfloat16, cpu, "out") is good
+    for bad in (torch.empty(2, 63, 3, 64, dtype=torch.bfloat16),
+                torch.empty(2, 64, 3, 64, dtype=torch.float32),
+                torch.empty(2, 3, 64, 64, dtype=torch.bfloat16).transpose(1, 2)):
+        with pytest.raises(ValueError):
+            native._given(bad, (2, 64, 3, 64), torch.bfloat16, cpu, "out")
+    with pytest.raises(ValueError):
+        native._given(good, (2, 64, 3, 64), torch.bfloat16, torch.device("meta"), "out")
