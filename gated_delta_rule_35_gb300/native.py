@@ -436,7 +436,10 @@ def chunk_fwd_noalloc(q, k, v, g, beta, scale: float = 1.0, h0=None, out=None, f
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
     p = problem(B, T, H, K, V, q.dtype, "simt")
-    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    o = _given(out, (B, T, H, V), q.dtype, q.device, "out") if out is not None else \
+        torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    if final_state is not None:
+        _given(final_state, (B, H, K, V), torch.float32, q.device, "final_state")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     st = f(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
            _ptr(o), _ptr(final_state), ctypes.c_void_p(s.cuda_stream))
