@@ -40,7 +40,8 @@ sys.path.insert(0, str(ROOT))
 
 import torch  # noqa: E402
 
-from gated_delta_rule_35_gb300.inputs import (BENCH_WORKLOAD, DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
+from gated_delta_rule_35_gb300.inputs import (BENCH_WORKLOAD, DECODE_WORKLOADS, FEATURE_WORKLOAD,  # noqa: E402
+                                              WORKLOADS,
                                               make_inputs, make_workload, to_f64)
 
 DECODE_WORKLOAD = "bf16_b256_h16_t1_k128_v128_decode"
@@ -543,116 +544,183 @@ def bench_decode(args, world, dev):
                          "algorithmic_bytes_per_call": nbytes, "peak_source": peaks["_source"]}}
 
 
-def bench_ours(args, w, world, rank, local):
-    from gated_delta_rule_35_gb300 import chunk_fwd, chunk_fwd_host, native
+def step_stats(ms):
+    """Median, mean and the 10th / 90th percentiles of per-step times (ms)."""
+    xs = sorted(ms)
+    pick = lambda f: xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+    return {"steps": len(xs), "median_ms": statistics.median(xs), "mean_ms": statistics.fmean(xs),
+            "p10_ms": pick(0.1), "p90_ms": pick(0.9), "min_ms": xs[0], "max_ms": xs[-1]}
 
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
-    x = make_workload(w.name)
-    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+
+def pipeline_roofline(w, t_step_s, peaks, has_h0):
+    """The whole step against max(flops / bf16 peak, compulsory bytes / HBM)."""
+    units = w.B * w.T * w.H
+    hbytes = (2 if has_h0 else 1) * w.B * w.H * w.K * w.V * 4
+    F = flops_per_token_head(w.K, w.V) * units
+    Bt = bytes_per_token_head(w.K, w.V, DSIZE[w.dtype]) * units + hbytes
+    t_f, t_b = F / (peaks["bf16_tflops"] * 1e12), Bt / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_f, t_b)
+    return {"t_roof_us": 1e6 * t_roof, "t_meas_us": 1e6 * t_step_s, "frac": t_roof / t_step_s,
+            "flops": F, "bytes": Bt, "bound": "hbm" if t_b >= t_f else "tensor",
+            "peak_source": peaks["_source"]}
+
+
+def kernel_roofline(name, w, t_launch_s, peaks, has_h0):
+    """The dominant kernel against its bound: compulsory bytes of the launch
+    (per token-head, plus the fp32 states it reads and writes) over its time."""
+    units = w.B * w.T * w.H
+    bound, model = KERNEL_MODEL.get(name, ("hbm", _fused))
+    bpt, fpt = model(w.K, w.V, DSIZE[w.dtype])
+    state_bytes = ((2 if has_h0 else 1) * w.B * w.H * w.K * w.V * 4) if bound == "hbm" else 0
+    if bound == "hbm":
+        achieved, peak, unit = (bpt * units + state_bytes) / t_launch_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        achieved, peak, unit = fpt * units / t_launch_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:   # fp32 FMA pipe: SMs x lanes x 2 flop x max SM clock
+        peak = SMS * FP32_LANES * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        achieved, unit = fpt * units / t_launch_s / 1e12, "TFLOP/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": ncu_traffic(name, w.name), "kernel": name,
+            "kernel_ms": 1e3 * t_launch_s, "peak_source": peaks["_source"],
+            "algorithmic_per_token_head": {"bytes": bpt, "flops": fpt},
+            "algorithmic_state_bytes": state_bytes}
+
+
+def time_steps(args, w, dev, flush, steps, warmup, per_kernel=True, d=None):
+    """Device times of `steps` full forwards of workload w (L2 flushed before
+    each): per-step times from events at the ends of each step only, then
+    (per_kernel) the same steps with a marker after every kernel."""
+    from gated_delta_rule_35_gb300 import chunk_fwd, native
+
+    if d is None:
+        x = make_workload(w.name)
+        d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
     p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, args.algo)
     kernels = native.launches(p)
     nk = len(kernels)
     ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device=dev)
     o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
     hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def make_events():
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-        for e in evs:
-            e.record(stream)          # creates the underlying cudaEvent_t
-        return evs
-
-    step_events = [make_events() for _ in range(args.steps)]
-    # whole steps, markers only at their ends, so that consecutive kernels may
-    # overlap as they do in a plain call (the value); then the same steps with
-    # a marker after every kernel (the per-kernel split and the roofline)
-    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
 
     def step(evs=None):
         chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=args.algo,
                   workspace=ws, out=o, final_state=hf, stream=stream,
                   events=None if evs is None else [e.cuda_event for e in evs])
 
-    for _ in range(args.warmup):
+    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize(dev)
+    return {"d": d, "kernels": kernels, "step": step, "bounds": bounds, "stream": stream,
+            "flush": flush, "nk": nk, "per_kernel": per_kernel}
+
+
+def run_timed(t, dev, clocks=None):
+    """Runs the prepared steps; returns (per-step ms list, per-kernel ms sums, wall s)."""
+    stream, flush, step, bounds, nk = t["stream"], t["flush"], t["step"], t["bounds"], t["nk"]
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.mark_start()
+    wall0 = time.perf_counter()
+    for a, b in bounds:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if clocks is not None:
+        clocks.mark_end()
+    step_ms = [a.elapsed_time(b) for a, b in bounds]
+    per_kernel = [0.0] * nk
+    if t["per_kernel"]:
+        marks = []
+        for _ in bounds:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+            for e in evs:
+                e.record(stream)      # creates the underlying cudaEvent_t
+            flush.zero_()
+            step(evs)
+            marks.append(evs)
+        torch.cuda.synchronize(dev)
+        for evs in marks:
+            for j in range(nk):
+                per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
+    return step_ms, per_kernel, wall
+
+
+def bench_other_workloads(args, main_w, dev, flush, peaks, world):
+    """Every other bf16 workload, device-timed like the headline (median of at
+    least 50 steps, L2 flushed before each), with its pipeline and kernel
+    roofline fractions."""
+    out = {}
+    for name, w in WORKLOADS.items():
+        if name == main_w.name or w.dtype != "bf16":
+            continue
+        t = time_steps(args, w, dev, flush, max(50, args.steps), args.warmup)
+        step_ms, per_kernel, _ = run_timed(t, dev)
+        st = step_stats(step_ms)
+        t_step = max_over_ranks(st["median_ms"] / 1e3, world, dev)
+        kernels, nk = t["kernels"], t["nk"]
+        dom = max(range(nk), key=lambda j: per_kernel[j])
+        has_h0 = t["d"]["h0"] is not None
+        out[name] = {
+            "tokens_per_s": w.B * w.T * world / t_step, "ms_per_step": 1e3 * t_step,
+            "timing": st,
+            "pipeline_roofline": pipeline_roofline(w, t_step, peaks, has_h0),
+            "roofline": kernel_roofline(kernels[dom], w, per_kernel[dom] / len(step_ms) / 1e3, peaks,
+                                        has_h0),
+            "per_kernel_ms": {k: per_kernel[j] / len(step_ms) for j, k in enumerate(kernels)},
+            "kernels": kernels, "gpu_launches": nk * len(step_ms),
+        }
+        del t
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_ours(args, w, world, rank, local):
+    from gated_delta_rule_35_gb300 import chunk_fwd_host
+
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    x = make_workload(w.name)
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peaks = load_peaks()
+    t = time_steps(args, w, dev, flush, args.steps, args.warmup, d=d)
+    kernels, nk = t["kernels"], t["nk"]
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(dev)
     time.sleep(0.05)   # let the sampler take its first readings
-    clocks.mark_start()
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        bounds[i][0].record(stream)
-        step()
-        bounds[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - wall0
-    clocks.mark_end()
-    for i in range(args.steps):
-        flush.zero_()
-        step(step_events[i])
-    torch.cuda.synchronize(dev)
+    step_ms, per_kernel, wall = run_timed(t, dev, clocks)
     clk = clocks.stop()
     barrier(world)
     torch.cuda.synchronize(dev)
 
-    per_kernel = [0.0] * nk
-    total_ms = sum(a.elapsed_time(b) for a, b in bounds)
-    for evs in step_events:
-        for j in range(nk):
-            per_kernel[j] += evs[j].elapsed_time(evs[j + 1])
-    total_s = max_over_ranks(total_ms / 1e3, world, dev)
+    st = step_stats(step_ms)
+    # the value: B*T tokens per median step, max over ranks
+    t_step = max_over_ranks(st["median_ms"] / 1e3, world, dev)
     tokens_step = w.B * w.T
-    value = tokens_step * args.steps * world / total_s
-    ms_per_step = 1e3 * total_s / args.steps
+    value = tokens_step * world / t_step
+    has_h0 = d["h0"] is not None
 
-    # roofline of the dominant kernel
-    peaks = load_peaks()
     dom = max(range(nk), key=lambda j: per_kernel[j])
-    name = kernels[dom]
-    t_launch = per_kernel[dom] / args.steps / 1e3
-    units = w.B * w.T * w.H
-    bound, model = KERNEL_MODEL.get(name, ("hbm", _fused))
-    bpt, fpt = model(w.K, w.V, DSIZE[w.dtype])
-    traffic = ncu_traffic(name, w.name)
-    if bound == "hbm":
-        achieved, peak, unit = bpt * units / t_launch / 1e9, peaks["hbm_gbs"], "GB/s"
-    elif bound == "tensor":
-        achieved, peak, unit = fpt * units / t_launch / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
-    else:   # fp32 FMA pipe: SMs x lanes x 2 flop x max SM clock
-        peak = SMS * FP32_LANES * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        achieved, unit = fpt * units / t_launch / 1e12, "TFLOP/s"
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic, "kernel": name,
-                "kernel_ms": 1e3 * t_launch, "share": per_kernel[dom] / max(sum(per_kernel), 1e-12),
-                "peak_source": peaks["_source"],
-                "algorithmic_per_token_head": {"bytes": bpt, "flops": fpt}}
-    # whole-pipeline roofline: max(flops / bf16 peak, compulsory bytes / HBM)
-    hbytes = (2 if d["h0"] is not None else 1) * w.B * w.H * w.K * w.V * 4
-    F = flops_per_token_head(w.K, w.V) * units
-    Bt = bytes_per_token_head(w.K, w.V, DSIZE[w.dtype]) * units + hbytes
-    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bt / (peaks["hbm_gbs"] * 1e9))
-    pipeline = {"t_roof_us": 1e6 * t_roof, "t_meas_us": 1e3 * ms_per_step,
-                "frac": t_roof / (ms_per_step / 1e3), "flops": F, "bytes": Bt,
-                "bound": "hbm" if Bt / (peaks["hbm_gbs"] * 1e9) >= F / (peaks["bf16_tflops"] * 1e12) else "tensor",
-                "peak_source": peaks["_source"]}
+    roofline = kernel_roofline(kernels[dom], w, per_kernel[dom] / args.steps / 1e3, peaks, has_h0)
+    roofline["share"] = per_kernel[dom] / max(sum(per_kernel), 1e-12)
+    pipeline = pipeline_roofline(w, t_step, peaks, has_h0)
 
     # end to end through the public host-tensor API: H2D inputs, forward, D2H o and h_final
-    hx = {n: (t.pin_memory() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
-    h2d = sum(t.numel() * t.element_size() for n, t in hx.items() if isinstance(t, torch.Tensor))
-    d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
+    hx = {n: (t_.pin_memory() if isinstance(t_, torch.Tensor) else t_) for n, t_ in x.items()}
+    h2d = sum(t_.numel() * t_.element_size() for n, t_ in hx.items() if isinstance(t_, torch.Tensor))
+    d2h = w.B * w.T * w.H * w.V * DSIZE[w.dtype] + w.B * w.H * w.K * w.V * 4
     e2e_steps = max(1, min(args.steps, 20))
     # pinned outputs kept across steps, as a serving loop keeps its buffers
-    ho = torch.empty(tuple(o.shape), dtype=o.dtype, pin_memory=True)
-    hhf = torch.empty(tuple(hf.shape), dtype=hf.dtype, pin_memory=True)
+    ho = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, pin_memory=True)
+    hhf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, pin_memory=True)
     for _ in range(2):
         chunk_fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], 1.0, hx["h0"], algo=args.algo,
                        device=dev, out=ho, final_state=hhf)
@@ -664,11 +732,19 @@ def bench_ours(args, w, world, rank, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     e2e = {"value": tokens_step * e2e_steps * world / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del hx, ho, hhf, t
+    torch.cuda.empty_cache()
 
+    fw = WORKLOADS[FEATURE_WORKLOAD]
+    others = None if args.no_other_workloads else bench_other_workloads(args, w, dev, flush, peaks, world)
     dec = None if args.no_decode else bench_decode(args, world, dev)
-    fe = None if args.no_frontend else bench_frontend(args, w, world, dev, flush)
-    on = None if args.no_output_norm else bench_output_norm(args, w, world, dev, flush, d)
-    pcd = None if args.no_per_channel else bench_per_channel(args, w, world, dev, flush)
+    fe = None if args.no_frontend else bench_frontend(args, fw, world, dev, flush)
+    fd = None
+    if not args.no_output_norm or not args.no_per_channel:
+        fx = make_workload(fw.name)
+        fd = {n: (t_.to(dev) if isinstance(t_, torch.Tensor) else t_) for n, t_ in fx.items()}
+    on = None if args.no_output_norm else bench_output_norm(args, fw, world, dev, flush, fd)
+    pcd = None if args.no_per_channel else bench_per_channel(args, fw, world, dev, flush)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -677,17 +753,19 @@ def bench_ours(args, w, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16-in/f32-acc" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": config_of(w, args),
+            "timing": dict(st, statistic="value and ms_per_step use the median step"),
             "token_heads_per_s": value * w.H,
             "roofline": roofline, "pipeline_roofline": pipeline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": nk * args.steps,
             "kernels": kernels,
             "per_kernel_ms": {k: per_kernel[j] / args.steps for j, k in enumerate(kernels)},
             "per_kernel_note": "second pass of the same steps with a marker after every kernel",
-            "clocks": clk, "wall_timed_s": wall, "decode": dec, "frontend": fe, "output_norm": on, "per_channel": pcd,
+            "clocks": clk, "wall_timed_s": wall, "workloads": others,
+            "decode": dec, "frontend": fe, "output_norm": on, "per_channel": pcd,
         }
         print(json.dumps(line), flush=True)
 
@@ -708,6 +786,8 @@ def main():
                     help="skip the gated RMSNorm output-stage measurement")
     ap.add_argument("--no-per-channel", action="store_true",
                     help="skip the per-channel (KDA) decay measurements")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the device-timed lines of the other bf16 workloads")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="target CPU time of the oracle baseline sample")
     args = ap.parse_args()

@@ -1,10 +1,18 @@
 // Host side of the C ABI declared in include/gdn.h: argument validation,
 // workspace carving, algorithm choice and the launch sequence.
+#include <atomic>
 #include <cstring>
 
 #include "gdn_internal.h"
 
 namespace gdn {
+
+namespace {
+std::atomic<uint64_t> g_armed_stall{0};
+}  // namespace
+
+uint64_t take_armed_stall() { return g_armed_stall.exchange(0); }
+
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -91,7 +99,10 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     a.rk = reinterpret_cast<float *>(front + g_cum_bytes(p));
     void *body = empty ? front : front + front_bytes(p);
 
-    cudaError_t e;
+    // the status word starts clear on every path; only bounded waits that
+    // give up set it
+    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
     if (empty) {
         e = marks.mark(0, stream);
         if (e == cudaSuccess) e = copy_state(a, stream);
@@ -206,6 +217,10 @@ GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream) {
     if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return GDN_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_ERR_DEVICE_TIMEOUT;
+}
+
+GDN_API void gdn_debug_arm_stall(uint64_t wait_ns) {
+    gdn::g_armed_stall.store(wait_ns == 0 ? 1 : wait_ns);
 }
 
 GDN_API const char *gdn_status_string(gdn_status s) {

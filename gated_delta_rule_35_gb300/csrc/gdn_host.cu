@@ -18,7 +18,7 @@ struct HostPlan {
     size_t tok_q, tok_v, tok_g, tok_b;   // bytes per token (all heads) of q/k, v/o, g, beta
     size_t h_bytes;           // one state [B, H, K, V] fp32
     size_t ws_bytes;          // one span's workspace
-    size_t off_q, off_k, off_v, off_g, off_b, off_o, off_h0, off_h1, off_h2, off_ws, total;
+    size_t off_q, off_k, off_v, off_g, off_b, off_o, off_h0, off_h1, off_h2, off_ws, off_st, total;
 };
 
 // Spans picked for pieces == 0: the last span's kernels and output copy are
@@ -65,6 +65,7 @@ bool make_plan(const gdn_problem *p, int pieces, HostPlan *pl) {
     pl->off_h1 = take(pl->h_bytes);
     pl->off_h2 = take(pl->h_bytes);
     pl->off_ws = take(pl->ws_bytes);
+    pl->off_st = take(kMaxSpans * sizeof(uint32_t));   // each span's device status word
     pl->total = at;
     return true;
 }
@@ -145,6 +146,10 @@ GDN_API gdn_status gdn_chunk_fwd_host(const gdn_problem *p, const void *q, const
                            scale, state, dev + pl.off_o + B * t0 * pl.tok_v, next, dev + pl.off_ws,
                            pl.ws_bytes, sb);
         if (st != GDN_OK) break;
+        // the span's status word (the next span's call clears it) is kept aside
+        e = cudaMemcpyAsync(dev + pl.off_st + i * sizeof(uint32_t), dev + pl.off_ws, sizeof(uint32_t),
+                            cudaMemcpyDeviceToDevice, sb);
+        if (e != cudaSuccess) break;
         e = gdn::copy_span(static_cast<char *>(o) + t0 * pl.tok_v, T * pl.tok_v,
                            dev + pl.off_o + B * t0 * pl.tok_v, nt * pl.tok_v, nt * pl.tok_v, B,
                            cudaMemcpyDeviceToHost, sb);
@@ -155,7 +160,18 @@ GDN_API gdn_status gdn_chunk_fwd_host(const gdn_problem *p, const void *q, const
     const cudaError_t ea = cudaStreamSynchronize(sa), eb = cudaStreamSynchronize(sb);
     for (int i = 0; i < made; ++i) cudaEventDestroy(landed[i]);
     if (st != GDN_OK) return st;
-    return (e == cudaSuccess && ea == cudaSuccess && eb == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+    if (e != cudaSuccess || ea != cudaSuccess || eb != cudaSuccess) return GDN_ERR_CUDA;
+    // a span whose bounded device wait gave up has garbage outputs: report it
+    uint32_t words[gdn::kMaxSpans] = {};
+    if (p->T > 0) {
+        if (cudaMemcpyAsync(words, dev + pl.off_st, pl.spans * sizeof(uint32_t),
+                            cudaMemcpyDeviceToHost, sb) != cudaSuccess ||
+            cudaStreamSynchronize(sb) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        for (int i = 0; i < pl.spans; ++i)
+            if (words[i]) return GDN_ERR_DEVICE_TIMEOUT;
+    }
+    return GDN_OK;
 }
 
 }  // extern "C"

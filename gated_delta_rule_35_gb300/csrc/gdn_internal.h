@@ -80,6 +80,11 @@ constexpr const char *kCopyStateName = "copy_state_kernel";
 
 constexpr size_t kStatusBytes = 256;
 
+// Test hook (gdn_debug_arm_stall): the wait limit in nanoseconds for the next
+// tensor-core launch, which then withholds its first chunk's loads; 0 when
+// nothing is armed. Taking it disarms it.
+uint64_t take_armed_stall();
+
 inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
 
 }  // namespace gdn

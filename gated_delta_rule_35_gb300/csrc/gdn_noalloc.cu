@@ -1,8 +1,6 @@
 // gdn_chunk_fwd_noalloc: the chunked forward for callers that cannot allocate
 // device memory (see include/gdn.h). Its scratch is a fixed array in the
 // library's own device image instead of a caller-provided workspace.
-#include <mutex>
-
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -14,27 +12,29 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void *g_scratch_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch array on the current device. The first call on
-// a device asks the runtime for it (once, under a lock) and caches it.
+// Device address of the scratch array on the current device, looked up on
+// every call: the lookup is a host-side table read once the library's device
+// code is loaded on the device (the first call on a device loads it), and a
+// fresh lookup stays valid across a cudaDeviceReset or a re-created primary
+// context, where a cached address would dangle.
 cudaError_t scratch_address(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        if (!p) return cudaErrorInvalidSymbol;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    if (!p) return cudaErrorInvalidSymbol;
+    *out = p;
     return cudaSuccess;
+}
+
+// The stream's work must run on the current device, whose scratch array is
+// the one handed to the kernels (NULL, the legacy default stream, always
+// belongs to the current device).
+bool stream_on_current_device(cudaStream_t s) {
+    if (!s) return true;
+    int cur = -1, dev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    if (cudaStreamGetDevice(s, &dev) != cudaSuccess) return false;
+    return cur == dev;
 }
 
 }  // namespace
@@ -51,6 +51,7 @@ extern "C" GDN_API gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p, const 
     simt.algo = GDN_ALGO_SIMT;
     const size_t need = gdn_chunk_fwd_workspace_bytes(&simt);
     if (need > gdn::kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;   // beyond the fixed maximum
+    if (!gdn::stream_on_current_device(static_cast<cudaStream_t>(stream))) return GDN_ERR_INVALID_ARG;
     void *scratch = nullptr;
     if (gdn::scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
     // The SIMT pipeline writes every scratch region before reading it, so the

@@ -88,12 +88,13 @@ struct Bars {
 };
 
 // Bounded wait: false if another role aborted or the limit passed (then aborts).
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
+                                         uint64_t limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort = 1;
             return false;
         }
@@ -103,12 +104,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 // wait_bar for a barrier completed by other CTAs of the cluster (acquire at
 // cluster scope).
 __device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
-                                                 volatile uint32_t *abort) {
+                                                 volatile uint32_t *abort, uint64_t limit) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait_cluster(bar, parity)) {
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort = 1;
             return false;
         }
@@ -117,14 +118,15 @@ __device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
 }
 // Polling variant for the latency-critical roles: a suspended waiter can take
 // hundreds of cycles to resume after the phase completes.
-__device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+__device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
+                                         uint64_t limit) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test_wait(bar, parity)) return true;
         if ((i & 255) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) {
+            if (globaltimer_ns() - t0 > limit) {
                 *abort = 1;
                 return false;
             }
@@ -157,7 +159,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
                     float scale, int l2_prefetch, uint32_t *status, int l2norm,
                     const float *__restrict__ rk, const __nv_bfloat16 *__restrict__ gate,
-                    const float *__restrict__ norm_w, float norm_eps, int nrank_arg) {
+                    const float *__restrict__ norm_w, float norm_eps, int nrank_arg,
+                    uint64_t wlim, int stall) {
     using Lay = TcLayout<K>;
     const int nrank = GATED ? nrank_arg : 0;
     constexpr int KB = K / 64;
@@ -271,7 +274,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                              smem_desc(vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, 1);
                 mma_commit(&bs->o_done);
             };
-            bool ok = spin_bar(&bs->full[0], 0, abort);
+            bool ok = spin_bar(&bs->full[0], 0, abort, wlim);
             if (ok) {
                 tc_fence_after_sync();
                 issue_w(0);
@@ -281,7 +284,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int s = c & 1;
                 const uint32_t par = c & 1;
                 // X += [q; -w] [h^T | k] (q and k landed before W(c) was issued)
-                if (!(ok = spin_bar(&bs->hs_ready, par, abort) && spin_bar(&bs->w_ready, par, abort)))
+                if (!(ok = spin_bar(&bs->hs_ready, par, abort, wlim) && spin_bar(&bs->w_ready, par, abort, wlim)))
                     break;
                 tc_fence_after_sync();
                 const uint32_t st = s_base + s * Lay::kStage;
@@ -307,7 +310,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         if (mbar_test_wait(&bs->vn_ready, par)) break;
                         if ((i & 255) == 0) {
                             if (*abort) { ok = false; break; }
-                            if (globaltimer_ns() - t0 > kWaitNs) { *abort = 1; ok = false; break; }
+                            if (globaltimer_ns() - t0 > wlim) { *abort = 1; ok = false; break; }
                         }
                     }
                     if (!ok) break;
@@ -322,12 +325,12 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mma_commit(&bs->h_done);
                 mma_commit(&bs->empty[s]);   // HT(c) is the stage's last reader
                 if (w_next) {
-                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort))) break;
+                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort, wlim))) break;
                     tc_fence_after_sync();
                     issue_w(s ^ 1);
                 }
                 // once P, q h and v_new are out of the X-region: next chunk's u, then o
-                if (!(ok = spin_bar(&bs->xo_ready, par, abort))) break;
+                if (!(ok = spin_bar(&bs->xo_ready, par, abort, wlim))) break;
                 tc_fence_after_sync();
                 if (c + 1 < NT) issue_u(s ^ 1);
                 issue_pv(c);
@@ -342,7 +345,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             int issued = 0;   // chunks whose loads were issued
             for (int c = 0; c < NT; ++c) {
                 const int s = c & 1, t0 = c * 64;
-                if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort)) break;
+                if (c >= 2 && !wait_bar(&bs->empty[s], ((c >> 1) - 1) & 1, abort, wlim)) break;
+                // test hook: chunk 0's loads are withheld, so every role's first
+                // wait on them runs out and the launch reports a device timeout
+                if (stall && c == 0) continue;
                 unsigned char *st = sm + s * Lay::kStage;
                 mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 24576);
 #pragma unroll
@@ -372,7 +378,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             // no copy may still be landing in shared memory when the CTA exits
             // (after an abort the last loads may have no consumer)
-            for (int c = max(0, issued - 2); c < issued; ++c)
+            for (int c = max(stall ? 1 : 0, issued - 2); c < issued; ++c)
                 mbar_wait(&bs->full[c & 1], (c >> 1) & 1, kWaitNs);
         }
     } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
@@ -408,7 +414,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // chunk c needs HT(c - 2). For the same reason the next phase of
             // g_ready[c % 4] (chunk c + 4) cannot complete before every waiter of
             // this one has passed.
-            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort)) break;
+            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort, wlim)) break;
             if (ptid < 64) {
                 float rq = 1.f;
                 if (l2norm) {
@@ -457,7 +463,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int row = (warp & 3) * 32 + lane;
         for (int c = 0; c < NT; ++c) {
-            if (!warp_all(wait_bar(&bs->w_done, c & 1, abort))) break;
+            if (!warp_all(wait_bar(&bs->w_done, c & 1, abort, wlim))) break;
             tc_fence_after_sync();
 #pragma unroll 1
             for (int bb = 0; bb < K / 32; ++bb) {
@@ -558,7 +564,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         };
         auto gated_finish = [&](int c) -> bool {
             const int slot = c & 1;
-            if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (c >> 1) & 1, abort))) return false;
+            if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (c >> 1) & 1, abort, wlim))) return false;
             const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 512;
             float tot = 0.f;
 #pragma unroll
@@ -600,8 +606,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int t0 = c * 64, n = min(64, T - t0), gs = c & 3;
             const float d_next = (c + 1 < NT) ? __expf(g_last_next) : 1.f;
             if (c + 2 < NT) g_last_next = g_last_of(c + 2);   // one chunk ahead
-            if (!(ok = warp_all(wait_bar(&bs->g_ready[gs], (c >> 2) & 1, abort) &&
-                                spin_bar(&bs->big_done, c & 1, abort))))
+            if (!(ok = warp_all(wait_bar(&bs->g_ready[gs], (c >> 2) & 1, abort, wlim) &&
+                                spin_bar(&bs->big_done, c & 1, abort, wlim))))
                 break;
             tc_fence_after_sync();
             if (upper) {
@@ -663,7 +669,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // previous chunk's output stage, part 2, while this chunk's MMAs run
                 if (GATED && c >= 1 && !(ok = gated_finish(c - 1))) break;
             } else {
-                if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort)))) break;
+                if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort, wlim)))) break;
                 const float gate = gate_s[gs * 64 + row];
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
@@ -681,7 +687,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc_fence_before_sync();
                 mbar_arrive(&bs->vn_ready);
             }
-            if (!(ok = warp_all(spin_bar(&bs->h_done, c & 1, abort)))) break;
+            if (!(ok = warp_all(spin_bar(&bs->h_done, c & 1, abort, wlim)))) break;
             tc_fence_after_sync();
             if (c + 1 < NT) {
 #pragma unroll 1
@@ -707,7 +713,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tc_fence_before_sync();
             mbar_arrive(&bs->hs_ready);
             if (upper) {
-                if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort)))) break;
+                if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort, wlim)))) break;
                 tc_fence_after_sync();
                 const int64_t oi = ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V +
                                    vt * kTcBV + col0;
@@ -816,9 +822,15 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     int norm_arg = (a.flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, nrank_arg = nrank;
     float scale_arg = a.scale, eps_arg = a.norm_eps;
     uint32_t *status_arg = a.status;
+    uint64_t wlim_arg = kWaitNs;
+    int stall_arg = 0;
+    if (const uint64_t armed = take_armed_stall()) {
+        wlim_arg = armed;
+        stall_arg = 1;
+    }
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
                     &scale_arg, &pf_arg, &status_arg, &norm_arg, &rk_arg, &gate_arg, &nw_arg,
-                    &eps_arg, &nrank_arg};
+                    &eps_arg, &nrank_arg, &wlim_arg, &stall_arg};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -841,9 +853,8 @@ int tc_launches(const char **names, int max_names) {
 }
 
 cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
-    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
+    cudaError_t e = m.mark(0, s);
     if (e != cudaSuccess) return e;
-    if ((e = m.mark(0, s)) != cudaSuccess) return e;
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
     e = (a.K == 128) ? launch_fused<128>(a, ws, s) : launch_fused<64>(a, ws, s);

@@ -27,7 +27,7 @@ EXPORTS = ("gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_fwd_stag
            "gdn_chunk_fwd_launches", "gdn_chunk_fwd_profiled", "gdn_check_device_status",
            "gdn_chunk_fwd_noalloc", "gdn_decode_step", "gdn_decode_step_launches",
            "gdn_chunk_fwd_ex", "gdn_decode_step_ex", "gdn_chunk_fwd_host_bytes",
-           "gdn_chunk_fwd_host", "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_host", "gdn_debug_arm_stall", "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -100,6 +100,8 @@ def lib():
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_version.restype = ctypes.c_uint32
         L.gdn_version.argtypes = []
+        L.gdn_debug_arm_stall.restype = None
+        L.gdn_debug_arm_stall.argtypes = [ctypes.c_uint64]
         _lib = L
     return _lib
 
@@ -167,6 +169,21 @@ def _given(t, shape, dtype, dev, name):
     return t
 
 
+def _workspace(ws, need: int, dev):
+    """A caller-supplied workspace must be a contiguous uint8 tensor on the
+    inputs' device holding at least ``need`` bytes: the kernels and a later
+    check_device_status read the status word in that very buffer, so a
+    too-small one is an error rather than silently replaced. None: a fresh
+    one is allocated."""
+    if ws is None:
+        return torch.empty(need, dtype=torch.uint8, device=dev)
+    if ws.dtype != torch.uint8 or ws.device != dev or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    if ws.numel() < need:
+        raise ValueError(f"workspace holds {ws.numel()} bytes; this problem needs {need}")
+    return ws
+
+
 def _output_norm(gate, weight, eps, shape, like):
     if gate is None and weight is None:
         return None
@@ -204,11 +221,7 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     need = workspace_bytes(p)
     if need == 0:
         raise GdnError(GDN_ERR_UNSUPPORTED, "gdn_chunk_fwd_workspace_bytes")
-    if workspace is not None and (workspace.dtype != torch.uint8 or workspace.device != q.device
-                                  or not workspace.is_contiguous()):
-        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    workspace = _workspace(workspace, need, q.device)
     o = _given(out, (B, T, H, V), q.dtype, q.device, "out") if out is not None else \
         torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
     hf = None
@@ -321,6 +334,13 @@ def decode_launches(p: Problem) -> list[str]:
     names = (ctypes.c_char_p * 1)()
     n = int(lib().gdn_decode_step_launches(ctypes.byref(p), names, 1))
     return [names[i].decode() for i in range(n)]
+
+
+def debug_arm_stall(wait_ns: int) -> None:
+    """Test hook: the next tensor-core launch withholds its first chunk's loads,
+    so its bounded waits give up after ``wait_ns`` and it reports a device
+    timeout through check_device_status (gdn_debug_arm_stall)."""
+    lib().gdn_debug_arm_stall(int(wait_ns))
 
 
 def check_device_status(workspace, stream=None) -> int:
@@ -441,8 +461,10 @@ def chunk_fwd_noalloc(q, k, v, g, beta, scale: float = 1.0, h0=None, out=None, f
     if final_state is not None:
         _given(final_state, (B, H, K, V), torch.float32, q.device, "final_state")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    st = f(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
-           _ptr(o), _ptr(final_state), ctypes.c_void_p(s.cuda_stream))
+    # the library finds its scratch on the current device: make it the inputs'
+    with torch.cuda.device(q.device):
+        st = f(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+               _ptr(h0), _ptr(o), _ptr(final_state), ctypes.c_void_p(s.cuda_stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_chunk_fwd_noalloc")
     return o, final_state

@@ -22,9 +22,11 @@
  * Conventions shared by every entry point:
  *  - Every tensor argument is a DEVICE pointer on the current CUDA device,
  *    contiguous, row-major, 16-byte aligned. The caller owns all memory; the
- *    library allocates nothing and keeps no mutable global state between
- *    calls. Calls on different streams are independent as long as each has its
- *    own workspace.
+ *    library allocates nothing. Apart from two documented exceptions (the
+ *    fixed scratch array of gdn_chunk_fwd_noalloc and the one-shot test hook
+ *    gdn_debug_arm_stall) it keeps no mutable global state between calls, so
+ *    calls on different streams are independent as long as each has its own
+ *    workspace.
  *  - Layouts: q, k [B,T,H,K]; v, o [B,T,H,V]; g, beta [B,T,H] fp32;
  *    h0, h_final [B,H,K,V] fp32.
  *  - g is the per-token log-decay summed cumulatively *within each 64-token
@@ -180,7 +182,9 @@ GDN_API gdn_status gdn_chunk_fwd_profiled(const gdn_problem *p,
  * device copies of the inputs and outputs, two state buffers and one span's
  * workspace. Both streams must be distinct, caller-created streams of the
  * current device. The call returns when o and h_final are in host memory (it
- * synchronises both streams); errors are reported as for gdn_chunk_fwd. Same results as
+ * synchronises both streams); errors are reported as for gdn_chunk_fwd, and a
+ * bounded device wait that gave up in any span's kernels is returned as
+ * GDN_ERR_DEVICE_TIMEOUT (the outputs are then garbage). Same results as
  * gdn_chunk_fwd up to rounding (the state crosses a span boundary in fp32;
  * with one span they are identical). */
 GDN_API size_t gdn_chunk_fwd_host_bytes(const gdn_problem *p, int32_t pieces);
@@ -194,8 +198,20 @@ GDN_API gdn_status gdn_chunk_fwd_host(const gdn_problem *p,
 /* Waits for `stream`, then reads and clears the device status word kept in the
  * first bytes of `workspace`: GDN_ERR_DEVICE_TIMEOUT if a bounded device wait
  * of an earlier call on this workspace gave up, GDN_OK otherwise (or
- * GDN_ERR_CUDA if the stream itself reports an error). */
+ * GDN_ERR_CUDA if the stream itself reports an error). Every gdn_chunk_fwd
+ * call clears the word when it starts, so it reports on the last call. */
 GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream);
+
+/* Test hook for the device-timeout path; the method's pages have no
+ * counterpart. Arms a one-shot fault for the next launch of the tensor-core
+ * forward in this process: that launch withholds the input loads of its first
+ * chunk, so every role's first wait on them runs out after `wait_ns`
+ * nanoseconds (0 means 1 ns), the roles leave their loops, whatever was
+ * issued drains, and the launch records the timeout in the workspace's status
+ * word (read it with gdn_check_device_status). The outputs of that call are
+ * garbage; later calls are unaffected. Nothing traps and no wait is unbounded.
+ * Process-global: for tests only, never with concurrent callers. */
+GDN_API void gdn_debug_arm_stall(uint64_t wait_ns);
 
 /* gdn_chunk_fwd without a workspace argument, for callers that cannot allocate
  * device memory at all: code running where cudaMalloc is unavailable or
@@ -212,13 +228,16 @@ GDN_API gdn_status gdn_check_device_status(void *workspace, void *stream);
  * with GDN_ERR_WORKSPACE before anything is enqueued. Nothing here calls
  * cudaMalloc, cudaFree or an allocating library routine.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current) and may load the library's device code,
- * so make that first call before any stream capture. Every call on a device
- * shares the one array: calls whose work overlaps on the GPU (on different
- * streams, or from different threads) race and give wrong results; serialise
- * them. The array keeps the last call's contents; no call depends on them.
- * Pointer conventions, layouts and other errors are those of gdn_chunk_fwd. */
+ * Every call looks up the array's device address on the current device (a
+ * host-side lookup, so the address stays right after a cudaDeviceReset); the
+ * first call on a device may also load the library's device code, so make
+ * that first call before any stream capture. `stream` must belong to the
+ * current device (else GDN_ERR_INVALID_ARG): the array used is the current
+ * device's. Every call on a device shares the one array: calls whose work
+ * overlaps on the GPU (on different streams, or from different threads) race
+ * and give wrong results; serialise them. The array keeps the last call's
+ * contents; no call depends on them. Pointer conventions, layouts and other
+ * errors are those of gdn_chunk_fwd. */
 GDN_API gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p,
                                          const void *q, const void *k, const void *v,
                                          const float *g, const float *beta, float scale,

@@ -34,3 +34,23 @@ def test_reference_line_has_every_key():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_step_statistics_and_roofline_arithmetic():
+    """The headline uses the median step; p10/p90 bracket it; the pipeline
+    roofline fraction is max(flops / peak, bytes / HBM) over the step time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from gated_delta_rule_35_gb300.inputs import WORKLOADS
+
+    st = bench.step_stats([5.0, 1.0, 2.0, 4.0, 3.0, 100.0, 2.5, 3.5, 4.5, 1.5, 2.2])
+    assert st["median_ms"] == 3.0 and st["steps"] == 11
+    assert st["p10_ms"] <= st["median_ms"] <= st["p90_ms"] < 100.0
+    assert st["min_ms"] == 1.0 and st["max_ms"] == 100.0
+    w = WORKLOADS["bf16_b8_h64_t8192_k128_v128"]
+    peaks = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "_source": "test"}
+    r = bench.pipeline_roofline(w, 2e-3, peaks, False)
+    units = w.B * w.T * w.H
+    nbytes = 1032 * units + w.B * w.H * w.K * w.V * 4
+    assert r["bytes"] == nbytes and r["bound"] == "hbm"
+    assert abs(r["frac"] - nbytes / 6800e9 / 2e-3) < 1e-12

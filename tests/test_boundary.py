@@ -241,3 +241,21 @@ def test_device_output_buffers_are_checked():
             native._given(bad, (2, 64, 3, 64), torch.bfloat16, cpu, "out")
     with pytest.raises(ValueError):
         native._given(good, (2, 64, 3, 64), torch.bfloat16, torch.device("meta"), "out")
+
+
+def test_caller_workspace_is_checked_not_replaced():
+    """A caller workspace that is too small (or of the wrong kind) raises: the
+    kernels would otherwise use a fresh buffer while the caller later reads the
+    status word of its own, stale one."""
+    import torch
+    cpu = torch.device("cpu")
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    assert native._workspace(ws, 1024, cpu) is ws
+    assert native._workspace(None, 512, cpu).numel() == 512
+    with pytest.raises(ValueError):
+        native._workspace(ws, 1025, cpu)
+    for bad in (torch.zeros(1024, dtype=torch.int8), torch.zeros(2048, dtype=torch.uint8)[::2]):
+        with pytest.raises(ValueError):
+            native._workspace(bad, 16, cpu)
+    with pytest.raises(ValueError):
+        native._workspace(ws, 16, torch.device("meta"))
