@@ -21,17 +21,19 @@ gdn_status check_problem(const gdn_problem *p) {
     if (!p) return GDN_ERR_INVALID_ARG;
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->K <= 0 || p->V <= 0) return GDN_ERR_INVALID_ARG;
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC)
+    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC &&
+        p->algo != GDN_ALGO_TC_SINGLE)
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
-    if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && p->algo == GDN_ALGO_TC)
+    const bool tc = p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE;
+    if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && tc)
         return GDN_ERR_UNSUPPORTED;   // per-channel decay runs on the SIMT pipeline
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
     if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
     // Every index is computed in 64 bits; B*T*H rows must still fit a grid.
     if (num_chunks(p->T) > 65535 * 64LL) return GDN_ERR_UNSUPPORTED;
     if (p->H > 65535 || p->B > 65535) return GDN_ERR_UNSUPPORTED;
-    if (p->algo == GDN_ALGO_TC && !tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)))
+    if (tc && !tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)))
         return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
@@ -57,6 +59,7 @@ size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
     if (p->T == 0) return 0;
     const size_t front = front_bytes(p);
     if (algo == GDN_ALGO_TC) return front + tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+    if (algo == GDN_ALGO_TC_SINGLE) return front;   // A stays in the kernel
     return front + simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
 }
 
@@ -76,6 +79,8 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     const gdn_algo algo = resolve_algo(p);
     if (ex && algo == GDN_ALGO_TC && (ex->A || ex->w || ex->u || ex->v_new || ex->h))
         return GDN_ERR_UNSUPPORTED;
+    // the single-kernel form keeps A on chip and has no output stage
+    if (algo == GDN_ALGO_TC_SINGLE && (ex || norm)) return GDN_ERR_UNSUPPORTED;
     if (ex && algo == GDN_ALGO_SIMT && ex->A_beta) return GDN_ERR_UNSUPPORTED;
     const size_t need = kStatusBytes + body_bytes(p, algo);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
@@ -107,8 +112,8 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         e = marks.mark(0, stream);
         if (e == cudaSuccess) e = copy_state(a, stream);
         if (e == cudaSuccess) e = marks.mark(1, stream);
-    } else if (algo == GDN_ALGO_TC) {
-        e = tc_forward(a, body, stream, marks);
+    } else if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE) {
+        e = tc_forward(a, body, stream, marks, algo == GDN_ALGO_TC_SINGLE);
         if (e == cudaSuccess && ex && ex->A_beta) e = tc_export_abeta(a, body, ex->A_beta, stream);
     } else {
         const SimtWorkspace ws = simt_carve(body, a.B, a.T, a.H, a.K, a.V);
@@ -131,13 +136,16 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// Kernels of one call.
 int launches(const gdn_problem *p, const char **names, int max_names) {
     if (check_problem(p) != GDN_OK) return 0;
     if (p->T == 0) {
         if (names && max_names > 0) names[0] = kCopyStateName;
         return 1;
     }
-    if (resolve_algo(p) == GDN_ALGO_TC) return tc_launches(names, max_names);
+    const gdn_algo algo = resolve_algo(p);
+    if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE)
+        return tc_launches(algo == GDN_ALGO_TC_SINGLE, names, max_names);
     for (int i = 0; names && i < kSimtLaunches && i < max_names; ++i) names[i] = kSimtKernelNames[i];
     return kSimtLaunches;
 }

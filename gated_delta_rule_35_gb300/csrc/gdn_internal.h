@@ -64,11 +64,12 @@ cudaError_t simt_forward(const Args &a, const SimtWorkspace &ws, cudaStream_t s,
 constexpr int kSimtLaunches = 3;
 extern const char *const kSimtKernelNames[kSimtLaunches];
 
-// Tensor-core path.
+// Tensor-core path: the WY kernel writing A to the workspace followed by the
+// forward kernel reading it, or (single) one kernel that builds A itself.
 bool tc_supported(int K, int V, gdn_dtype dtype);
 size_t tc_workspace_bytes(int B, int T, int H, int K, int V);
-cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m);
-int tc_launches(const char **names, int max_names);
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, bool single);
+int tc_launches(bool single, const char **names, int max_names);
 // WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.
 cudaError_t wy_tc_forward(const Args &a, void *abeta, cudaStream_t s);
 // Converts the workspace's A diag(beta) to fp32 [B, T_pad, H, 64].

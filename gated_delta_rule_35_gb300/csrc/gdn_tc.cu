@@ -37,10 +37,14 @@ namespace {
 
 using namespace ptx;
 
-// 16 warps: 0 MMA issuer, 1 TMA producer, 2-3 and 6-7 prep group, 4-5 w
-// epilogue, 8-15 chain group. A warp reaches the TMEM lanes of quarter warp % 4.
-constexpr int kTcThreads = 512;
-constexpr int kPrepThreads = 128, kWThreads = 64, kChainThreads = 256;
+// Two-kernel form (the WY kernel writes A to the workspace): 16 warps, 0 MMA
+// issuer, 1 TMA producer, 2-3 and 6-7 prep group, 4-5 w epilogue, 8-15 chain
+// group. Single-kernel form (FA: the A build runs in this kernel): 18 warps,
+// 0 MMA issuer, 1 TMA producer, 2-3 prep group, 4-7 WY group, 8-15 chain group,
+// 16-17 w epilogue. A warp reaches the TMEM lanes of quarter warp % 4.
+template <bool FA> constexpr int tc_threads() { return FA ? 576 : 512; }
+template <bool FA> constexpr int prep_threads() { return FA ? 64 : 128; }
+constexpr int kWThreads = 64, kChainThreads = 256, kWyThreads = 128;
 constexpr int kTcBV = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
@@ -69,8 +73,53 @@ struct TcLayout {
     static constexpr uint32_t kBytes = kRed + 2 * 8 * 64 * 4;
 };
 
+// Single-kernel form: the WY matrix of every chunk is built in the kernel (the
+// WY group, one chunk ahead of its use), so A never reaches HBM. Per stage
+// [q; -w], [h^T; k] and v as above; once BIG has read a stage's q and -w, P
+// takes the q half and v_new the -w half of its first 64-feature block, and v_g
+// replaces v (read only by U). The A tiles are single-buffered, Z | A diag(beta)
+// | A', written by the WY group after the previous chunk's W and U completed.
+// The WY group keeps its own k tile (loaded a chunk ahead), [N1; N2] (Y in its
+// second half after the first merge product), [X; U] (the fp32 diagonal blocks
+// in its U half until X is built) and per-chunk tables for the prep group.
+template <int K>
+struct FaLayout {
+    static constexpr int KB = K / 64;
+    static constexpr uint32_t kStV = 2 * KB * 16384;             // [q; -w] and [h^T; k] first
+    static constexpr uint32_t kStage = kStV + 8192;
+    static constexpr uint32_t kZ = 2 * kStage, kA = kZ + 8192, kAp = kA + 8192;
+    static constexpr uint32_t kWk = kAp + 8192;                  // WY k tile, KB x 8 KB
+    static constexpr uint32_t kWn = kWk + KB * 8192;             // [N1; N2]
+    static constexpr uint32_t kWxu = kWn + 16384;                // [X; U]
+    // g, beta, beta exp(g) r, cf, r (64 floats each) and the scan total
+    static constexpr uint32_t kWmisc = kWxu + 16384;
+    // to the prep group, 4 chunk slots: the chunk's g (cumulative) and k-row factors
+    static constexpr uint32_t kWtab = kWmisc + 1536;
+    static constexpr uint32_t kG = kWtab + 2 * 4 * 64 * 4;
+    static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
+    static constexpr uint32_t kBytes = kBar + 256;
+    static_assert(kBytes + 1024 <= 232448, "fits the 227 KB of shared memory a CTA may use");
+};
+
+// Per-chunk operand tiles of both forms, by stage s.
+template <int K, bool FA>
+struct Tiles {
+    using L = TcLayout<K>;
+    using F = FaLayout<K>;
+    static constexpr uint32_t stage = FA ? F::kStage : L::kStage;
+    static constexpr uint32_t bar = FA ? F::kBar : L::kBar;
+    static constexpr uint32_t g = FA ? F::kG : L::kG;
+    __host__ __device__ static constexpr uint32_t p(int s) { return FA ? s * F::kStage : L::kP; }
+    __host__ __device__ static constexpr uint32_t vn(int s) { return FA ? s * F::kStage + 8192 : L::kVN; }
+    __host__ __device__ static constexpr uint32_t vg(int s) { return FA ? s * F::kStage + F::kStV : L::kVG; }
+    __host__ __device__ static constexpr uint32_t z(int s) { return FA ? F::kZ : s * L::kStage + L::kStZ; }
+    __host__ __device__ static constexpr uint32_t ap(int s) { return FA ? F::kAp : s * L::kStage + L::kStAp; }
+};
+
 // TMEM columns: X-region [X (64) | QK (64)], O (64), W (K), HT (K).
 constexpr uint32_t kColX = 0, kColQK = 64, kColO = 128, kColW = 192, kColHT = 320;
+// Single-kernel form: the WY group's accumulator (Gram, merge products).
+constexpr uint32_t kColWY = 448;
 // With the output stage O is double-buffered (chunk parity), the second copy
 // in the columns after HT, so that a chunk's normalisation can wait for the
 // cluster's row sums while the next chunk runs.
@@ -84,6 +133,11 @@ struct Bars {
     uint64_t xo_ready, vn_ready, hs_ready;          // chain group
     uint64_t drain;                                 // every MMA issued is done
     uint64_t norm_bar[2];                           // output stage: row sums of the cluster
+    // single-kernel form
+    uint64_t a_ready;                               // WY group: A tiles of the next chunk
+    uint64_t wu_done;                               // W and U of a chunk are done (A tiles free)
+    uint64_t wy_mma, wyk_full;                      // WY group's MMAs and k tile
+    uint64_t wy_tab[4];                             // WY group: tables of chunk slot c % 4
     uint32_t abort, tmem;
 };
 
@@ -133,6 +187,40 @@ __device__ __forceinline__ bool spin_bar(uint64_t *bar, uint32_t parity, volatil
         }
     }
 }
+// Named barrier 1 over the WY group's four warps (128 threads), and the same
+// barrier reducing a predicate with OR over them.
+__device__ __forceinline__ void wy_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool wy_any(bool x) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(x))
+        : "memory");
+    return r != 0;
+}
+// Polling with a pause between polls, for roles of several warps: a tight
+// mbarrier poll from every warp of a group takes issue slots and shared-memory
+// bandwidth from the warps doing the work (and from the tensor core's operand
+// reads); a pause of ~ns bounds the added latency to about that.
+__device__ __forceinline__ bool nap_bar(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
+                                        uint64_t limit, uint32_t ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+constexpr uint32_t kNapNs = 32;
 // A warp leaves its loop together: the tcgen05 loads that follow a wait are
 // warp-collective.
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
@@ -151,8 +239,12 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
 
 // GATED: the output stage (gated RMSNorm over V) with the V tiles of a head as
 // one cluster of nrank_arg CTAs; without it the cluster code is compiled out.
-template <int K, bool GATED>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// FA: the single-kernel form (A built here by the WY group; tm_a unused, g
+// holds raw per-token log decays when raw_g is set, else the chunk-local
+// cumulative sums; beta read here). Without FA, A diag(beta) and A' come from
+// the WY kernel through tm_a, and g (and rk) from its workspace.
+template <int K, bool GATED, bool FA>
+__global__ void __launch_bounds__(tc_threads<FA>(), 1)
 gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                     const float *__restrict__ g, const float *__restrict__ h0,
@@ -160,8 +252,13 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float scale, int l2_prefetch, uint32_t *status, int l2norm,
                     const float *__restrict__ rk, const __nv_bfloat16 *__restrict__ gate,
                     const float *__restrict__ norm_w, float norm_eps, int nrank_arg,
-                    uint64_t wlim, int stall) {
+                    uint64_t wlim, int stall, const float *__restrict__ beta, int raw_g) {
+    static_assert(!(GATED && FA), "the output stage runs on the two-kernel form");
     using Lay = TcLayout<K>;
+    using FLay = FaLayout<K>;
+    using Tl = Tiles<K, FA>;
+    constexpr int kThreads = tc_threads<FA>();
+    constexpr int kPrepThreads = prep_threads<FA>();
     const int nrank = GATED ? nrank_arg : 0;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -175,22 +272,22 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // exp(g_i - g_ref) (0) and rk exp(g_ref - g_j) (0), usable while |g_last|
     // stays small enough for both to be finite fp32 numbers (flag fz_s); else
     // the exponents g_i + ln rq_i and g_j - ln rk_j.
-    float *tab = reinterpret_cast<float *>(sm + Lay::kG);   // first 256 floats unused
+    float *tab = reinterpret_cast<float *>(sm + Tl::g);     // first 4 floats: g_last per slot (FA)
     float *eg_s = tab + 256;
     float *gate_s = tab + 512;
     float *rf_s = tab + 768;
     float *cf_s = tab + 1024;
     int *fz_s = reinterpret_cast<int *>(tab + 1280);
-    Bars *bs = reinterpret_cast<Bars *>(sm + Lay::kBar);
+    Bars *bs = reinterpret_cast<Bars *>(sm + Tl::bar);
     volatile uint32_t *abort = &bs->abort;
 
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (T + 63) / 64;
 
-    // the zero tiles of both stages, read by U as the zero halves of its operands
-    for (int i = tid; i < 1024; i += kTcThreads)
-        st_shared_v4(sm + (i >> 9) * Lay::kStage + Lay::kStZ + (i & 511) * 16, 0u, 0u, 0u, 0u);
+    // the zero tile(s), read by U as the zero half of its operand
+    for (int i = tid; i < (FA ? 512 : 1024); i += kThreads)
+        st_shared_v4(sm + Tl::z(i >> 9) + (i & 511) * 16, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(&bs->tmem, kTmemCols);
@@ -215,12 +312,19 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // the row sums of every CTA of the cluster arrive as transactions
         if (nrank)
             for (int i = 0; i < 2; ++i) mbar_init(&bs->norm_bar[i], 1);
+        if (FA) {
+            mbar_init(&bs->a_ready, kWyThreads);
+            mbar_init(&bs->wu_done, 1);
+            mbar_init(&bs->wy_mma, 1);
+            mbar_init(&bs->wyk_full, 1);
+            for (int i = 0; i < 4; ++i) mbar_init(&bs->wy_tab[i], kWyThreads);
+        }
         bs->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_a);
+        if (!FA) prefetch_tmap(&tm_a);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -242,43 +346,42 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t idBIG = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idHT = idesc_bf16(128, K, true, true);
             constexpr uint32_t idPV = idesc_bf16(128, 64, false, true);
-            const uint32_t s_p = s_base + Lay::kP;
-            const uint32_t s_vn = s_base + Lay::kVN, s_vg = s_base + Lay::kVG;
             // W = [A'; .] k, k read N-major from the stage's [h^T; k]; the rows under A'
-            // are whatever follows it (the next stage or P): their products are unused
+            // are whatever follows it: their products are unused
             auto issue_w = [&](int s) {
-                const uint32_t kt = s_base + s * Lay::kStage + Lay::kStBbig + 8192;
-                const uint32_t ap = s_base + s * Lay::kStage + Lay::kStAp;
+                const TileDesc da(s_base + Tl::ap(s), 16, 1024);
+                const TileDesc db(s_base + s * Tl::stage + Lay::kStBbig + 8192, 16384, 1024);
+                mma_bf16_k<false>(tmem + kColW, da.at(0), db.at(0), idW);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColW, smem_desc(ap + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(kt + ks * 2048, 16384, 1024, kLayoutSw128), idW, ks > 0);
+                for (int ks = 1; ks < 4; ++ks) mma_bf16_k<true>(tmem + kColW, da.at(ks * 32), db.at(ks * 2048), idW);
                 mma_commit(&bs->w_done);
             };
             // X = [0; A diag(beta)] v
             auto issue_u = [&](int s) {
-                const uint32_t st = s_base + s * Lay::kStage;
+                const TileDesc da(s_base + Tl::z(s), 16, 1024);
+                const TileDesc db(s_base + s * Tl::stage + Lay::kStV, 8192, 1024);
+                mma_bf16_k<false>(tmem + kColX, da.at(0), db.at(0), idU);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColX, smem_desc(st + Lay::kStZ + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(st + Lay::kStV + ks * 2048, 8192, 1024, kLayoutSw128), idU,
-                             ks > 0);
+                for (int ks = 1; ks < 4; ++ks) mma_bf16_k<true>(tmem + kColX, da.at(ks * 32), db.at(ks * 2048), idU);
             };
             // O += [P; .] v_new of chunk cp
             auto issue_pv = [&](int cp) {
-                const uint32_t vn = s_vn;
+                const TileDesc da(s_base + Tl::p(cp & 1), 16, 1024);
+                const TileDesc db(s_base + Tl::vn(cp & 1), 8192, 1024);
                 const uint32_t ocol = (GATED && (cp & 1)) ? kColO2 : kColO;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + ocol, smem_desc(s_p + ks * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(vn + ks * 2048, 8192, 1024, kLayoutSw128), idPV, 1);
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_k<true>(tmem + ocol, da.at(ks * 32), db.at(ks * 2048), idPV);
                 mma_commit(&bs->o_done);
             };
-            bool ok = spin_bar(&bs->full[0], 0, abort, wlim);
+            // single-kernel form: chunk c's A tiles are in (WY group) once a_ready
+            // completes its phase c
+            auto a_in = [&](int c) { return !FA || mbar_test_wait(&bs->a_ready, c & 1); };
+            bool ok = spin_bar(&bs->full[0], 0, abort, wlim) && (!FA || spin_bar(&bs->a_ready, 0, abort, wlim));
             if (ok) {
                 tc_fence_after_sync();
                 issue_w(0);
                 issue_u(0);
+                if (FA) mma_commit(&bs->wu_done);   // chunk 0's A tiles are free again
             }
             for (int c = 0; ok && c < NT; ++c) {
                 const int s = c & 1;
@@ -287,12 +390,14 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (!(ok = spin_bar(&bs->hs_ready, par, abort, wlim) && spin_bar(&bs->w_ready, par, abort, wlim)))
                     break;
                 tc_fence_after_sync();
-                const uint32_t st = s_base + s * Lay::kStage;
+                const uint32_t st = s_base + s * Tl::stage;
+                {
+                    const TileDesc da(st + Lay::kStAbig, 16, 1024), db(st + Lay::kStBbig, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem + kColX, smem_desc(st + Lay::kStAbig + off, 16, 1024, kLayoutSw128),
-                             smem_desc(st + Lay::kStBbig + off, 16, 1024, kLayoutSw128), idBIG, 1);
+                    for (int ks = 0; ks < K / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16_k<true>(tmem + kColX, da.at(off), db.at(off), idBIG);
+                    }
                 }
                 mma_commit(&bs->big_done);
                 // Next chunk's w as soon as its inputs land, if that happens before
@@ -302,7 +407,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 {
                     const uint64_t t0 = globaltimer_ns();
                     for (uint32_t i = 1;; ++i) {
-                        if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1)) {
+                        if (w_next && mbar_test_wait(&bs->full[s ^ 1], ((c + 1) >> 1) & 1) && a_in(c + 1)) {
                             tc_fence_after_sync();
                             issue_w(s ^ 1);
                             w_next = false;
@@ -317,15 +422,20 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
                 // h^T += v_g^T k
                 tc_fence_after_sync();
+                {
+                    const TileDesc da(s_base + Tl::vg(s), 0, 1024), db(st + Lay::kStBbig + 8192, 16384, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColHT, smem_desc(s_vg + ks * 2048, 0, 1024, kLayoutSw128),
-                             smem_desc(st + Lay::kStBbig + 8192 + ks * 2048, 16384, 1024, kLayoutSw128),
-                             idHT, 1);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_k<true>(tmem + kColHT, da.at(ks * 2048), db.at(ks * 2048), idHT);
+                }
                 mma_commit(&bs->h_done);
-                mma_commit(&bs->empty[s]);   // HT(c) is the stage's last reader
+                // HT(c) is the stage's last reader; in the single-kernel form P and
+                // v_new sit in the stage too, so PV(c) is
+                if (!FA) mma_commit(&bs->empty[s]);
                 if (w_next) {
-                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort, wlim))) break;
+                    if (!(ok = spin_bar(&bs->full[s ^ 1], ((c + 1) >> 1) & 1, abort, wlim) &&
+                               (!FA || spin_bar(&bs->a_ready, (c + 1) & 1, abort, wlim))))
+                        break;
                     tc_fence_after_sync();
                     issue_w(s ^ 1);
                 }
@@ -334,6 +444,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc_fence_after_sync();
                 if (c + 1 < NT) issue_u(s ^ 1);
                 issue_pv(c);
+                if (FA) {
+                    mma_commit(&bs->wu_done);   // W(c + 1) and U(c + 1): the A tiles are free
+                    mma_commit(&bs->empty[s]);
+                }
             }
             // nothing of ours may still run when the accumulators are released
             mma_commit(&bs->drain);
@@ -349,8 +463,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // test hook: chunk 0's loads are withheld, so every role's first
                 // wait on them runs out and the launch reports a device timeout
                 if (stall && c == 0) continue;
-                unsigned char *st = sm + s * Lay::kStage;
-                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + 24576);
+                unsigned char *st = sm + s * Tl::stage;
+                mbar_arrive_expect_tx(&bs->full[s], KB * 16384 + (FA ? 8192 : 24576));
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_4d(st + Lay::kStAbig + kb * 16384, &tm_q, &bs->full[s], kb * 64, h, t0, b);
@@ -358,8 +472,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                 t0, b);
                 }
                 tma_load_4d(st + Lay::kStV, &tm_v, &bs->full[s], vt * kTcBV, h, t0, b);
-                tma_load_4d(st + Lay::kStA, &tm_a, &bs->full[s], 0, h, t0, b);
-                tma_load_4d(st + Lay::kStAp, &tm_a, &bs->full[s], 64, h, t0, b);
+                if (!FA) {
+                    tma_load_4d(st + Lay::kStA, &tm_a, &bs->full[s], 0, h, t0, b);
+                    tma_load_4d(st + Lay::kStAp, &tm_a, &bs->full[s], 64, h, t0, b);
+                }
                 issued = c + 1;
                 // chunk c + 2 into L2 now, so that its stage load, two chunks from
                 // now, is served from L2 rather than HBM. Only when the grid leaves
@@ -372,8 +488,10 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         tma_prefetch_4d(&tm_k, kb * 64, h, tp, b);
                     }
                     tma_prefetch_4d(&tm_v, vt * kTcBV, h, tp, b);
-                    tma_prefetch_4d(&tm_a, 0, h, tp, b);
-                    tma_prefetch_4d(&tm_a, 64, h, tp, b);
+                    if (!FA) {
+                        tma_prefetch_4d(&tm_a, 0, h, tp, b);
+                        tma_prefetch_4d(&tm_a, 64, h, tp, b);
+                    }
                 }
             }
             // no copy may still be landing in shared memory when the CTA exits
@@ -381,11 +499,14 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int c = max(stall ? 1 : 0, issued - 2); c < issued; ++c)
                 mbar_wait(&bs->full[c & 1], (c >> 1) & 1, kWaitNs);
         }
-    } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
+    } else if (FA ? (warp == 2 || warp == 3) : (warp == 2 || warp == 3 || warp == 6 || warp == 7)) {
         // ================================================================ prep group
         // Per-chunk decay tables (A' = A diag(beta exp(g)) comes with A diag(beta)
-        // from the WY kernel).
+        // from the WY kernel or, in the single-kernel form, from the WY group,
+        // which also hands over the chunk's cumulative g and k-row factors).
         const int ptid = warp < 4 ? tid - 64 : tid - 128;
+        const float *gcum_t = reinterpret_cast<const float *>(sm + FLay::kWtab);
+        const float *rk_t = gcum_t + 256;
         // g of chunk c and of its last valid token, loaded one chunk ahead
         auto load_g = [&](int c) {
             const int t = c * 64 + ptid;
@@ -401,14 +522,25 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             return (l2norm && ptid < 64 && c < NT && t < T) ? rk[(static_cast<int64_t>(b) * T + t) * H + h]
                                                            : 1.f;
         };
-        float g_next = load_g(0), gl_next = load_gl(0), rk_next = load_rk(0);
+        float g_next = FA ? 0.f : load_g(0), gl_next = FA ? 0.f : load_gl(0);
+        float rk_next = FA ? 1.f : load_rk(0);
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1, gs = c & 3;
             const int n = min(64, T - c * 64);
-            const float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
-            g_next = load_g(c + 1);
-            gl_next = load_gl(c + 1);
-            rk_next = load_rk(c + 1);
+            float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
+            if (FA) {
+                // the WY group's tables of this chunk (slot c % 4; their next
+                // writer, chunk c + 4, needs U(c + 3), which needs these tables)
+                if (!wait_bar(&bs->wy_tab[gs], (c >> 2) & 1, abort, wlim)) break;
+                g_cur = gcum_t[gs * 64 + ptid];
+                gl = gcum_t[gs * 64 + n - 1];
+                rk_cur = rk_t[gs * 64 + ptid];
+                if (ptid == 0) tab[gs] = gl;   // the chain group's g_last of this chunk
+            } else {
+                g_next = load_g(c + 1);
+                gl_next = load_gl(c + 1);
+                rk_next = load_rk(c + 1);
+            }
             // Decay tables of chunk c in slot c % 4. Their previous reader, chunk
             // c - 4, finished before U(c - 3) was issued, and stage s landing for
             // chunk c needs HT(c - 2). For the same reason the next phase of
@@ -421,7 +553,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     // |q_i|^2 from the stage's q tile (rows 0-63 of the stacked
                     // operand; the swizzle only permutes 16-byte chunks in a
                     // row, and chunk j ^ (row % 8) keeps 8 rows on distinct banks)
-                    const unsigned char *qrow = sm + s * Lay::kStage + Lay::kStAbig + ptid * 128;
+                    const unsigned char *qrow = sm + s * Tl::stage + Lay::kStAbig + ptid * 128;
                     float ss = 0.f;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
@@ -456,7 +588,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             mbar_arrive(&bs->g_ready[gs]);
         }
-    } else if (warp < 6) {
+    } else if (FA ? warp >= 16 : warp < 6) {
         // ================================================================ w epilogue
         // Rows 0-63 of W (lane quarters 0-1) -> -w, bf16, under q in the stage's
         // stacked operand (that half was last read by BIG(c - 2)).
@@ -474,13 +606,348 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 float v[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = -__uint_as_float(r[e]);
-                unsigned char *base = sm + (c & 1) * Lay::kStage + Lay::kStAbig + (f0 >> 6) * 16384;
+                unsigned char *base = sm + (c & 1) * Tl::stage + Lay::kStAbig + (f0 >> 6) * 16384;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) st_bf16x8(base + sw128(64 + row, (f0 & 63) * 2 + q * 16), v + q * 8);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bs->w_ready);
+        }
+    } else if (FA && warp < 8) {
+        // ================================================================ WY group
+        // Single-kernel form: A = (I + L)^-1 of every chunk, in order, with
+        // L_ij = beta_i (k_i . k_j) exp(g_i - g_j) for i > j; written as
+        // A diag(beta) (U's operand) and A' = A diag(beta exp(g)) (W's). With X
+        // the inverse of the four 16x16 diagonal blocks of I + L (forward
+        // substitution in fp32), N1 its off-diagonal blocks (1,0) and (3,2) and
+        // N2 its bottom-left 32x32 block:
+        //   A0 = X - X N1 X,  A = A0 - A0 N2 A0
+        // ((D + N)^-1 = D^-1 - D^-1 N D^-1 when N D^-1 N = 0), formed from the
+        // Gram matrix in three stacked M = 128 products, each subtraction in the
+        // fp32 accumulator:
+        //   G = k k^T;  [Y1; U] = [N1; N2] X;  [A0; Y2] = [X; U] + [X; U](-Y1);
+        //   A = A0 + A0 (-Y2).
+        // The group loads its own copy of each chunk's k (a chunk ahead), takes
+        // the chunk-local sum of raw decays and the k-row norms when the flags
+        // ask, and hands g, the norms and the A tiles to the other roles.
+        const int wtid = tid - 128, ww = warp - 4;     // ww = this warp's lane quarter
+        const uint32_t lane_off = static_cast<uint32_t>(ww * 32) << 16;
+        const uint32_t tw = tmem + kColWY;
+        float *Ld = reinterpret_cast<float *>(sm + FLay::kWxu + 8192);
+        float *g_s = reinterpret_cast<float *>(sm + FLay::kWmisc);
+        float *b_s = g_s + 64, *eb_s = g_s + 128, *wcf_s = g_s + 192, *rk_s = g_s + 256;
+        float *tot_s = g_s + 320;
+        float *gcum_t = reinterpret_cast<float *>(sm + FLay::kWtab), *rk_t = gcum_t + 256;
+        const uint32_t s_k = s_base + FLay::kWk, s_n = s_base + FLay::kWn;
+        const uint32_t s_xu = s_base + FLay::kWxu, s_y = s_n + 8192;
+        unsigned char *n_t = sm + FLay::kWn, *xu_t = sm + FLay::kWxu, *y_t = n_t + 8192;
+        uint32_t mph = 0;            // next phase of wy_mma
+        int k_loaded = 0;            // chunks whose k tile was requested
+        bool mma_out = false;        // an MMA whose completion was not seen
+        bool ok = true;
+        auto load_k = [&](int j) {   // one thread
+            mbar_arrive_expect_tx(&bs->wyk_full, KB * 8192);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+                tma_load_4d(sm + FLay::kWk + kb * 8192, &tm_k, &bs->wyk_full, kb * 64, h, j * 64, b);
+        };
+        // one MMA group (A K-major; B K-major or rows along N) issued by one thread
+        // (M = 128, N = 64; the first product overwrites, the merges accumulate)
+        auto mma_issue = [&](uint32_t a, uint32_t bop, bool b_mn, int ksteps, bool acc) {
+            if (wtid == 0) {
+                tc_fence_after_sync();
+                const uint32_t id = idesc_bf16(128, 64, false, b_mn);
+                const TileDesc da(a, 16, 1024), db(bop, 8192, 1024);
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint32_t a_off = (ks >> 2) * 8192 + (ks & 3) * 32;
+                    const uint64_t bd = db.at(b_mn ? ks * 2048 : a_off);
+                    if (acc || ks > 0)
+                        mma_bf16_k<true>(tw, da.at(a_off), bd, id);
+                    else
+                        mma_bf16_k<false>(tw, da.at(a_off), bd, id);
+                }
+                mma_commit(&bs->wy_mma);
+            }
+            mma_out = true;
+        };
+        // every thread of the group waits for it; false: give up (abort)
+        // one warp polls, the others wait at the group barrier
+        auto mma_wait = [&]() -> bool {
+            const bool got = ww != 0 || warp_all(spin_bar(&bs->wy_mma, mph, abort, wlim));
+            const bool all = !wy_any(!got);
+            if (all) {
+                mph ^= 1;
+                mma_out = false;
+            }
+            tc_fence_after_sync();
+            return all;
+        };
+        auto load16 = [&](int blk, float *v) {
+            uint32_t t[16];
+            tmem_ld16(tw + lane_off + blk * 16, t);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(t[e]);
+        };
+        if (wtid == 0 && NT > 0) {
+            load_k(0);
+            k_loaded = 1;
+        }
+        for (int j = 0; j < NT && ok; ++j) {
+            const int t0 = j * 64, n = min(64, T - t0), slot = j & 3;
+            const int64_t my_row = (static_cast<int64_t>(b) * T + t0 + wtid) * H + h;
+            float gv = 0.f, bv = 0.f;
+            if (wtid < n) {
+                gv = g[my_row];
+                bv = beta[my_row];
+            }
+            if (raw_g) {
+                // inclusive sum over the chunk: tokens 0-31 in the first warp,
+                // 32-63 in the second, one shared total between them
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gv, off);
+                    if (lane >= off) gv += y;
+                }
+                if (wtid == 31) *tot_s = gv;
+                wy_sync();
+                if (ww == 1) gv += *tot_s;
+                if (wtid >= n) gv = 0.f;
+            }
+            // the previous chunk's readers of these tables are past the barrier
+            // that ended its A tiles
+            if (wtid < 64) {
+                g_s[wtid] = gv;
+                b_s[wtid] = bv;
+                rk_s[wtid] = 1.f;
+            }
+            wy_sync();
+            const float g_last = g_s[n - 1];
+            const float g_ref = 0.5f * g_last;
+            const bool fz = fabsf(g_last) <= 160.f;   // |g_i - g_ref| <= |g_last| / 2 for decays <= 0
+            if (wtid < 64) {
+                eb_s[wtid] = bv * __expf(gv);
+                wcf_s[wtid] = wtid < n ? __expf(g_ref - gv) : 0.f;
+            }
+            // ---- this chunk's k tile, then G = k k^T issued as M = 128 (rows
+            // past the k tile are whatever follows it; their products are unused)
+            if (!(ok = !wy_any(ww == 0 && !warp_all(spin_bar(&bs->wyk_full, j & 1, abort, wlim))))) break;
+            mma_issue(s_k, s_k, false, K / 16, false);
+            if (l2norm && wtid < 64) {
+                // |k_i|^2 from the k tile while the Gram runs (the swizzle only
+                // permutes 16-byte chunks within a row)
+                float ss = 0.f;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(sm + FLay::kWk + kb * 8192 + wtid * 128 +
+                                                                         ((jj ^ (wtid & 7)) * 16));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+                            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                        }
+                    }
+                const float r = rsqrtf(ss + kL2NormEps);
+                rk_s[wtid] = r;
+                wcf_s[wtid] *= r;
+                eb_s[wtid] *= r;
+            }
+            if (!(ok = mma_wait())) break;
+            // the Gram and the norms have read the k tile: the next chunk's may land
+            if (wtid == 0 && j + 1 < NT) {
+                load_k(j + 1);
+                k_loaded = j + 2;
+            }
+            if (ww < 2) {
+                const int r = ww * 32 + lane, rb = r >> 4;
+                const float gr = g_s[r], br = b_s[r] * rk_s[r];
+                const float rf = br * __expf(gr - g_ref);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    float v[16];
+                    load16(blk, v);
+                    if (fz) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float4 c4 = *reinterpret_cast<const float4 *>(wcf_s + blk * 16 + 4 * m);
+                            const float cf[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const int e = 4 * m + e4;
+                                v[e] = (blk * 16 + e < r) ? v[e] * rf * cf[e4] : 0.f;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int jj = blk * 16 + e;
+                            const float d = (jj < r) ? gr - g_s[jj] : -INFINITY;
+                            v[e] = br * v[e] * rk_s[jj] * __expf(d);
+                        }
+                    }
+                    if (blk == rb) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) Ld[(rb * 16 + (r & 15)) * 17 + e] = v[e];
+                    }
+                    // N1: blocks (1,0) and (3,2); N2: rows 32-63 x columns 0-31
+                    const bool in1 = (rb == 1 && blk == 0) || (rb == 3 && blk == 2);
+                    const bool in2 = rb >= 2 && blk < 2;
+                    float n1[16], n2[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        n1[e] = in1 ? v[e] : 0.f;
+                        n2[e] = in2 ? v[e] : 0.f;
+                    }
+                    st_bf16x8(n_t + sw128(r, blk * 32), n1);
+                    st_bf16x8(n_t + sw128(r, blk * 32 + 16), n1 + 8);
+                    st_bf16x8(n_t + 8192 + sw128(r, blk * 32), n2);
+                    st_bf16x8(n_t + 8192 + sw128(r, blk * 32 + 16), n2 + 8);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before_sync();
+            wy_sync();
+            // ---- X: inverse of each 16x16 unit-lower diagonal block, column per thread
+            {
+                float x[16];
+                const int blk = wtid >> 4, col = wtid & 15;
+                float *Lb = Ld + blk * 16 * 17;
+                if (wtid < 64) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 15; ++jj)
+#pragma unroll
+                        for (int i = jj + 1; i < 16; ++i) x[i] = fmaf(-Lb[i * 17 + jj], x[jj], x[i]);
+                }
+                wy_sync();
+                if (wtid < 64) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) Lb[i * 17 + col] = x[i];
+                }
+                wy_sync();
+            }
+            // From here on thread t owns row t of the M = 128 accumulators: rows
+            // 0-63 belong to X / A0 / A, rows 64-127 to U / Y2.
+            const int r = wtid & 63, rb = r >> 4;
+            float xr[16];   // row r of X (threads < 64): its diagonal block
+            if (wtid < 64) {
+                const float z8[8] = {};
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) xr[jj] = Ld[(rb * 16 + (r & 15)) * 17 + jj];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    if ((ch >> 1) == rb)
+                        st_bf16x8(xu_t + sw128(r, ch * 16), xr + (ch & 1) * 8);
+                    else
+                        st_bf16x8(xu_t + sw128(r, ch * 16), z8);
+                }
+            }
+            fence_proxy_async_smem();
+            wy_sync();
+            // ---- [Y1; U] = [N1; N2] X
+            mma_issue(s_n, s_xu, true, 4, false);
+            if (!(ok = mma_wait())) break;
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                load16(blk, v);
+                if (wtid < 64) {
+                    // -Y1, the B operand (rows along N) of the next product
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = -v[e];
+                    st_bf16x8(y_t + sw128(r, blk * 32), v);
+                    st_bf16x8(y_t + sw128(r, blk * 32 + 16), v + 8);
+                } else {
+                    // U, the second half of the A operand [X; U]; its fp32 copy
+                    // stays in the accumulator
+                    st_bf16x8(xu_t + 8192 + sw128(r, blk * 32), v);
+                    st_bf16x8(xu_t + 8192 + sw128(r, blk * 32 + 16), v + 8);
+                }
+            }
+            if (wtid < 64) {
+                // the accumulator's rows 0-63 start the next product from X
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    uint32_t t[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) t[e] = blk == rb ? __float_as_uint(xr[e]) : 0u;
+                    tmem_st16(tw + lane_off + blk * 16, t);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            wy_sync();
+            // ---- [A0; Y2] = [X; U] + [X; U] (-Y1)
+            mma_issue(s_xu, s_y, true, 4, true);
+            if (!(ok = mma_wait())) break;
+            tc_fence_before_sync();
+            wy_sync();   // every MMA operand read before A0 / -Y2 overwrite them
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                load16(blk, v);
+                if (wtid < 64) {
+                    // A0 as the next A operand (its fp32 copy stays in the accumulator)
+                    st_bf16x8(xu_t + sw128(r, blk * 32), v);
+                    st_bf16x8(xu_t + sw128(r, blk * 32 + 16), v + 8);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = -v[e];
+                    st_bf16x8(y_t + sw128(r, blk * 32), v);
+                    st_bf16x8(y_t + sw128(r, blk * 32 + 16), v + 8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            wy_sync();
+            // ---- A = A0 + A0 (-Y2) in rows 0-63 (rows 64-127 of the product are unused)
+            mma_issue(s_xu, s_y, true, 4, true);
+            if (!(ok = mma_wait())) break;
+            // the A tiles are free once W and U of the previous chunk are done
+            if (j >= 1 && !(ok = !wy_any(ww == 0 && !warp_all(spin_bar(&bs->wu_done, (j - 1) & 1, abort, wlim)))))
+                break;
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                load16(blk, v);
+                if (wtid < 64) {
+                    float v2[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float a = v[e];
+                        v[e] = a * b_s[blk * 16 + e];
+                        v2[e] = a * eb_s[blk * 16 + e];
+                    }
+                    st_bf16x8(sm + FLay::kA + sw128(r, blk * 32), v);
+                    st_bf16x8(sm + FLay::kA + sw128(r, blk * 32 + 16), v + 8);
+                    st_bf16x8(sm + FLay::kAp + sw128(r, blk * 32), v2);
+                    st_bf16x8(sm + FLay::kAp + sw128(r, blk * 32 + 16), v2 + 8);
+                }
+            }
+            // tables of this chunk for the prep group: g (summed), k-row factors
+            if (wtid < 64) {
+                gcum_t[slot * 64 + wtid] = g_s[wtid];
+                rk_t[slot * 64 + wtid] = wtid < n ? rk_s[wtid] : 1.f;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->wy_tab[slot]);
+            mbar_arrive(&bs->a_ready);
+            wy_sync();   // every thread is done with this chunk's tables and accumulator
+        }
+        // nothing of the group may still land in shared memory or write tensor
+        // memory when the CTA exits (after an abort)
+        if (wtid == 0) {
+            if (mma_out) mbar_wait(&bs->wy_mma, mph, kWaitNs);
+            // a requested k tile whose wait did not complete: its phase is the
+            // one of chunk k_loaded - 1
+            if (!ok && k_loaded > 0) mbar_wait(&bs->wyk_full, (k_loaded - 1) & 1, kWaitNs);
         }
     } else {
         // ================================================================ chain group
@@ -501,9 +968,15 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             return g[(static_cast<int64_t>(b) * T + min(T, c * 64 + 64) - 1) * H + h];
         };
         // initial state: bf16 h^T under k in the stacked operand; fp32 in TMEM,
-        // pre-decayed by exp(g_last) of chunk 0
+        // pre-decayed by exp(g_last) of chunk 0 (in the single-kernel form the
+        // prep group has it, once the WY group summed the chunk)
         {
-            const float d0 = __expf(g_last_of(0));
+            float d0 = 1.f;
+            if (!FA)
+                d0 = __expf(g_last_of(0));
+            else if (warp_all(wait_bar(&bs->g_ready[0], 0, abort, wlim)))
+                d0 = __expf(tab[0]);   // else the run is aborting and the loop below leaves
+#pragma unroll 1
 #pragma unroll 1
             for (int blk = 0; blk < NF / 16; ++blk) {
                 const int f = f0 + blk * 16;
@@ -601,13 +1074,13 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             return true;
         };
-        float g_last_next = NT > 1 ? g_last_of(1) : 0.f;
+        float g_last_next = (!FA && NT > 1) ? g_last_of(1) : 0.f;
         for (int c = 0; c < NT; ++c) {
             const int t0 = c * 64, n = min(64, T - t0), gs = c & 3;
-            const float d_next = (c + 1 < NT) ? __expf(g_last_next) : 1.f;
-            if (c + 2 < NT) g_last_next = g_last_of(c + 2);   // one chunk ahead
+            float d_next = (!FA && c + 1 < NT) ? __expf(g_last_next) : 1.f;
+            if (!FA && c + 2 < NT) g_last_next = g_last_of(c + 2);   // one chunk ahead
             if (!(ok = warp_all(wait_bar(&bs->g_ready[gs], (c >> 2) & 1, abort, wlim) &&
-                                spin_bar(&bs->big_done, c & 1, abort, wlim))))
+                                nap_bar(&bs->big_done, c & 1, abort, wlim, kNapNs))))
                 break;
             tc_fence_after_sync();
             if (upper) {
@@ -643,8 +1116,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 16; ++e) v[e] = 0.f;
                     }
-                    st_bf16x8(sm + Lay::kP + sw128(row, j0 * 2), v);
-                    st_bf16x8(sm + Lay::kP + sw128(row, j0 * 2 + 16), v + 8);
+                    st_bf16x8(sm + Tl::p(c & 1) + sw128(row, j0 * 2), v);
+                    st_bf16x8(sm + Tl::p(c & 1) + sw128(row, j0 * 2 + 16), v + 8);
                 }
                 {
                     const uint32_t z[16] = {};
@@ -678,16 +1151,22 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tmem_ld16f(tmem + kColX + lane_off + cc, v);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) vg[e] = v[e] * gate;
-                    st_bf16x8(sm + Lay::kVN + sw128(row, cc * 2), v);
-                    st_bf16x8(sm + Lay::kVN + sw128(row, cc * 2 + 16), v + 8);
-                    st_bf16x8(sm + Lay::kVG + sw128(row, cc * 2), vg);
-                    st_bf16x8(sm + Lay::kVG + sw128(row, cc * 2 + 16), vg + 8);
+                    st_bf16x8(sm + Tl::vn(c & 1) + sw128(row, cc * 2), v);
+                    st_bf16x8(sm + Tl::vn(c & 1) + sw128(row, cc * 2 + 16), v + 8);
+                    st_bf16x8(sm + Tl::vg(c & 1) + sw128(row, cc * 2), vg);
+                    st_bf16x8(sm + Tl::vg(c & 1) + sw128(row, cc * 2 + 16), vg + 8);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&bs->vn_ready);
             }
-            if (!(ok = warp_all(spin_bar(&bs->h_done, c & 1, abort, wlim)))) break;
+            if (FA && c + 1 < NT) {
+                // the next chunk's g_last, from the prep group's table of it
+                if (!(ok = warp_all(wait_bar(&bs->g_ready[(c + 1) & 3], ((c + 1) >> 2) & 1, abort, wlim))))
+                    break;
+                d_next = __expf(tab[(c + 1) & 3]);
+            }
+            if (!(ok = warp_all(nap_bar(&bs->h_done, c & 1, abort, wlim, kNapNs)))) break;
             tc_fence_after_sync();
             if (c + 1 < NT) {
 #pragma unroll 1
@@ -703,7 +1182,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         r[e] = __float_as_uint(v[e] * d_next);
                     }
                     tmem_st16(tmem + kColHT + lane_off + f, r);
-                    unsigned char *dst = sm + ((c + 1) & 1) * Lay::kStage + Lay::kStBbig + (f >> 6) * 16384;
+                    unsigned char *dst = sm + ((c + 1) & 1) * Tl::stage + Lay::kStBbig + (f >> 6) * 16384;
                     st_bf16x8(dst + sw128(row, (f & 63) * 2), v);
                     st_bf16x8(dst + sw128(row, (f & 63) * 2 + 16), v + 8);
                 }
@@ -772,16 +1251,23 @@ __global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float
     }
 }
 
+// fa: the single-kernel form (abeta unused); else the second kernel of the
+// two-kernel form, reading A from abeta.
 template <int K>
-cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
+cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool fa) {
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
+        !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B))
+        return cudaErrorInvalidValue;
+    if (fa)
+        ma = mk;   // a valid map the kernel never reads
+    else if (!make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     // the row-sum region at the end is only used (and only allocated) with the output stage
-    const int smem = static_cast<int>((a.gate ? TcLayout<K>::kBytes : TcLayout<K>::kRed) + 1024);
-    const auto kernel = a.gate ? gdn_fused_tc_kernel<K, true> : gdn_fused_tc_kernel<K, false>;
+    const int smem = static_cast<int>(
+        (fa ? FaLayout<K>::kBytes : a.gate ? TcLayout<K>::kBytes : TcLayout<K>::kRed) + 1024);
+    const auto kernel = fa ? gdn_fused_tc_kernel<K, false, true>
+                           : a.gate ? gdn_fused_tc_kernel<K, true, false> : gdn_fused_tc_kernel<K, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -791,7 +1277,7 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     const int nrank = a.gate ? a.V / kTcBV : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.V / kTcBV, a.H, a.B);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(fa ? tc_threads<true>() : tc_threads<false>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -801,7 +1287,7 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     // own setup), which saves about 5 us on B8 H64 T8192. With one wave or
     // less the early start gains nothing and cost 20 us (1.7%) on
     // B1 H32 T32768, so those grids launch after the WY kernel ends.
-    if (ctas > sms) {
+    if (!fa && ctas > sms) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
     }
@@ -814,7 +1300,10 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
     // kernel arguments, in order, for the untyped launch call
-    const float *g_arg = a.g_chunk(), *h0_arg = a.h0, *rk_arg = a.rk, *nw_arg = a.norm_w;
+    // the single-kernel form sums raw decays itself
+    const float *g_arg = fa ? a.g : a.g_chunk(), *h0_arg = a.h0, *rk_arg = a.rk, *nw_arg = a.norm_w;
+    const float *beta_arg = a.beta;
+    int rawg_arg = (fa && (a.flags & GDN_FLAG_RAW_G)) ? 1 : 0;
     float *hf_arg = a.h_final;
     __nv_bfloat16 *o_arg = static_cast<__nv_bfloat16 *>(a.o);
     const __nv_bfloat16 *gate_arg = static_cast<const __nv_bfloat16 *>(a.gate);
@@ -830,7 +1319,7 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s) {
     }
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
                     &scale_arg, &pf_arg, &status_arg, &norm_arg, &rk_arg, &gate_arg, &nw_arg,
-                    &eps_arg, &nrank_arg, &wlim_arg, &stall_arg};
+                    &eps_arg, &nrank_arg, &wlim_arg, &stall_arg, &beta_arg, &rawg_arg};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -846,18 +1335,25 @@ size_t tc_workspace_bytes(int B, int T, int H, int, int) {
     return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
 }
 
-int tc_launches(const char **names, int max_names) {
+int tc_launches(bool single, const char **names, int max_names) {
     static const char *const kNames[2] = {"gdn_wy_tc_kernel", "gdn_fused_tc_kernel"};
-    for (int i = 0; names && i < 2 && i < max_names; ++i) names[i] = kNames[i];
-    return 2;
+    const int n = single ? 1 : 2;
+    for (int i = 0; names && i < n && i < max_names; ++i) names[i] = kNames[2 - n + i];
+    return n;
 }
 
-cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, bool single) {
     cudaError_t e = m.mark(0, s);
     if (e != cudaSuccess) return e;
+    if (single) {
+        // single kernel: the WY matrix is built in the forward kernel itself
+        e = (a.K == 128) ? launch_fused<128>(a, nullptr, s, true) : launch_fused<64>(a, nullptr, s, true);
+        if (e != cudaSuccess) return e;
+        return m.mark(1, s);
+    }
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
-    e = (a.K == 128) ? launch_fused<128>(a, ws, s) : launch_fused<64>(a, ws, s);
+    e = (a.K == 128) ? launch_fused<128>(a, ws, s, false) : launch_fused<64>(a, ws, s, false);
     if (e != cudaSuccess) return e;
     return m.mark(2, s);
 }

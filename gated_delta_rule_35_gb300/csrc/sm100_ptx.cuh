@@ -248,6 +248,36 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same with the accumulate flag fixed at compile time: no flag register is
+// compared per instruction. The MMA-issuing thread shares its sub-partition with
+// epilogue warps, so every instruction it spends between MMAs can leave the
+// tensor pipe waiting.
+template <bool ACC>
+__device__ __forceinline__ void mma_bf16_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+    if constexpr (ACC)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, 1, 1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc)
+            : "memory");
+}
+// A shared-memory descriptor built once for a tile and moved through it by byte
+// offsets (multiples of 16): the start-address field (address / 16, 14 bits)
+// holds every shared-memory address, so adding offset / 16 never carries out
+// of it.
+struct TileDesc {
+    uint64_t d;
+    __device__ __forceinline__ TileDesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+        : d(smem_desc(saddr, lbo_bytes, sbo_bytes, kLayoutSw128)) {}
+    __device__ __forceinline__ uint64_t at(uint32_t off) const { return d + (off >> 4); }
+};
+
 // Arrives on *bar once every previously issued tcgen05.mma of this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(

@@ -71,7 +71,14 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 typedef enum {
     GDN_ALGO_AUTO = 0,   /* fastest built path for the problem */
     GDN_ALGO_SIMT = 1,   /* CUDA-core fp32 pipeline, four kernels, any dtype */
-    GDN_ALGO_TC = 2      /* tensor-core (tcgen05/TMEM, TMA) path, bf16 only */
+    GDN_ALGO_TC = 2,     /* tensor-core (tcgen05/TMEM, TMA) path, bf16 only: a
+                          * kernel building every chunk's WY matrix (in parallel,
+                          * to the workspace), then the forward kernel */
+    GDN_ALGO_TC_SINGLE = 3 /* the same in one kernel: each CTA builds its chunks'
+                          * WY matrices itself, one chunk ahead of their use, so
+                          * A never reaches HBM (slower today: the build is a
+                          * serial chain inside the CTA). Without the output stage
+                          * and without the A export (else GDN_ERR_UNSUPPORTED) */
 } gdn_algo;
 
 /* Input front-end options (gdn_problem.flags), a bit set; 0 = inputs as

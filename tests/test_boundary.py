@@ -135,6 +135,7 @@ def _decode(p, q=FAKE, k=FAKE, v=FAKE, gamma=FAKE, beta=FAKE, s_in=FAKE, s_out=F
     ((1, 1, 1, 64, 24), "auto", native.GDN_ERR_UNSUPPORTED),    # V not a multiple of 16
     ((1, 1, 1, 64, 8192), "auto", native.GDN_ERR_UNSUPPORTED),  # V > 4096
     ((1, 1, 1, 64, 64), "tc", native.GDN_ERR_UNSUPPORTED),      # no tensor-core decode
+    ((1, 1, 1, 64, 64), "tc1", native.GDN_ERR_UNSUPPORTED),
 ])
 def test_decode_rejects_bad_problems(shape, algo, status):
     assert _decode(native.problem(*shape, native.GDN_BF16, algo)) == status
@@ -158,9 +159,38 @@ def test_decode_launches():
     assert native.decode_launches(native.problem(4, 1, 16, 96, 128, native.GDN_BF16)) == []
 
 
+def test_single_kernel_form_sizes_and_limits():
+    """GDN_ALGO_TC_SINGLE keeps A on chip: its workspace holds only the status
+    word and the front-end tables; it launches one kernel; per-channel decay,
+    an output stage and the A export are refused before anything runs."""
+    two = native.problem(4, 2048, 16, 128, 128, native.GDN_BF16, "tc")
+    one = native.problem(4, 2048, 16, 128, 128, native.GDN_BF16, "tc1")
+    rows = 4 * 2048 * 16
+    assert native.workspace_bytes(two) >= rows * 128 * 2
+    assert 0 < native.workspace_bytes(one) < rows * 16
+    assert native.launches(one) == ["gdn_fused_tc_kernel"]
+    assert native.launches(two) == ["gdn_wy_tc_kernel", "gdn_fused_tc_kernel"]
+    assert native.launches(native.problem(4, 2048, 16, 128, 128, native.GDN_BF16)) == native.launches(two)
+    kda = native.problem(1, 64, 1, 128, 128, native.GDN_BF16, "tc1", native.GDN_FLAG_PER_CHANNEL_DECAY)
+    assert native.workspace_bytes(kda) == 0
+    assert native.workspace_bytes(native.problem(1, 64, 1, 128, 128, native.GDN_F32, "tc1")) == 0
+    p = native.problem(1, 64, 1, 64, 64, native.GDN_BF16, "tc1")
+    norm = native.OutputNorm(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1e-6)
+    vp = ctypes.c_void_p
+    st = native.lib().gdn_chunk_fwd_ex(ctypes.byref(p), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                       1.0, None, ctypes.byref(norm), vp(FAKE), None, vp(FAKE),
+                                       native.workspace_bytes(p), None, 0, None)
+    assert st == native.GDN_ERR_UNSUPPORTED
+    ex = native.StageExports(None, None, None, None, None, vp(FAKE))
+    st = native.lib().gdn_chunk_fwd_stages(ctypes.byref(p), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                           vp(FAKE), 1.0, None, vp(FAKE), None, vp(FAKE),
+                                           native.workspace_bytes(p), ctypes.byref(ex), None)
+    assert st == native.GDN_ERR_UNSUPPORTED
+
+
 def test_flags_validated():
     """Known front-end bits are accepted by every path; unknown bits are rejected."""
-    for algo in ("simt", "tc"):
+    for algo in ("simt", "tc", "tc1"):
         for flags in (1, 2, 3):
             p = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo, flags)
             assert native.workspace_bytes(p) > native.workspace_bytes(

@@ -27,16 +27,19 @@ def _inputs():
     return x, {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
 
 
-def test_withheld_loads_report_a_device_timeout_then_recover():
+@pytest.mark.parametrize("algo", ["tc", "tc1"])
+def test_withheld_loads_report_a_device_timeout_then_recover(algo):
+    """Both tensor-core forms; in the single-kernel form the WY group's own
+    waits (on the next chunk's W and U) run out as well."""
     x, d = _inputs()
-    p = native.problem(2, 300, 3, 128, 128, torch.bfloat16, "tc")
+    p = native.problem(2, 300, 3, 128, 128, torch.bfloat16, algo)
     ws = torch.zeros(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
     native.debug_arm_stall(LIMIT_NS)
-    chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tc", workspace=ws)
+    chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=algo, workspace=ws)
     assert check_device_status(ws) == native.GDN_ERR_DEVICE_TIMEOUT
     # the status word was cleared by the read; the context is still usable
     assert check_device_status(ws) == native.GDN_OK
-    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tc",
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=algo,
                       workspace=ws)
     torch.cuda.synchronize()
     assert check_device_status(ws) == native.GDN_OK

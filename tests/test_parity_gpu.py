@@ -40,7 +40,7 @@ def run_oracle(x, scale=1.0):
                               to_f64(x["beta"]), scale, to_f64(x["h0"]))
 
 
-ALGOS = ["simt", "tc"]
+ALGOS = ["simt", "tc", "tc1"]
 
 
 @pytest.mark.parametrize("algo", ALGOS)
