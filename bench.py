@@ -26,6 +26,7 @@ step with per-channel (KDA) decay (--no-per-channel skips it).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -332,7 +333,7 @@ def cpu_baseline(x, w, budget_s):
 def bench_reference(args, w, world, rank):
     if rank != 0:
         return
-    x = make_workload(w.name)
+    x = make_workload(w)
     threads = os.cpu_count() or 1
     n_seq = min(w.B * w.H, max(1, threads))
     samples = oracle_sample(x, n_seq)
@@ -507,7 +508,7 @@ def bench_decode(args, world, dev):
     from gated_delta_rule_35_gb300 import decode_step, native
 
     w = DECODE_WORKLOADS[DECODE_WORKLOAD]
-    x = make_workload(w.name)
+    x = make_workload(w)
     d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
     state = d.pop("h0")
     o = torch.empty((w.B, w.T, w.H, w.V), dtype=d["q"].dtype, device=dev)
@@ -593,7 +594,7 @@ def time_steps(args, w, dev, flush, steps, warmup, per_kernel=True, d=None):
     from gated_delta_rule_35_gb300 import chunk_fwd, native
 
     if d is None:
-        x = make_workload(w.name)
+        x = make_workload(w)
         d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
     p = native.problem(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, args.algo)
     kernels = native.launches(p)
@@ -686,7 +687,7 @@ def bench_ours(args, w, world, rank, local):
 
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
-    x = make_workload(w.name)
+    x = make_workload(w)
     d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     peaks = load_peaks()
@@ -777,7 +778,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
-    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc", "tc1"])
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this many sequences instead of its own B "
+                         "(a slice of the same shape, for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-frontend", action="store_true",
@@ -793,6 +797,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_slice_b{args.batch}")
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         bench_reference(args, w, world, rank)

@@ -142,9 +142,13 @@ def make_output_norm(B: int, T: int, H: int, V: int, *, dtype: str = "bf16", see
     return gate, weight
 
 
-def make_workload(name: str, **overrides) -> dict:
-    """Inputs of a named workload; ``overrides`` may change B/T/H (e.g. a sample)."""
-    w = WORKLOADS[name] if name in WORKLOADS else DECODE_WORKLOADS[name]
+def make_workload(name, **overrides) -> dict:
+    """Inputs of a workload (a name, or a Workload such as a slice of a named
+    one); ``overrides`` may change B/T/H (e.g. a sample)."""
+    if isinstance(name, Workload):
+        w, name = name, name.name
+    else:
+        w = WORKLOADS[name] if name in WORKLOADS else DECODE_WORKLOADS[name]
     p = w.as_dict()
     p.update(overrides)
     return make_inputs(p["B"], p["T"], p["H"], p["K"], p["V"], dtype=p["dtype"], seed=p["seed"],
