@@ -13,7 +13,7 @@
 // Per chunk (C = 64 tokens), with A' = A diag(beta exp(g)) so that
 // w = A diag(beta) (exp(g) k) = A' k. Accumulators live in tensor memory, one
 // row per TMEM lane; "." marks operand rows whose products are never read:
-//   W    [A'; .] k                      W rows 0-63 = w
+//   W    [A diag(beta); A'] k           W rows 64-127 = w
 //   U    [0; A diag(beta)] v            X rows 64-127 = u, X rows 0-63 = 0
 //   BIG  [q; -w] [h^T | k]              X += [q h; -w h]  (rows 64-127: v_new)
 //                                       QK rows 0-63 += q k^T (cleared after each read)
@@ -39,10 +39,14 @@ namespace {
 using namespace ptx;
 
 // Two-kernel form (the WY kernel writes A to the workspace): 16 warps, 0 MMA
-// issuer, 1 TMA producer, 2-3 and 6-7 prep group, 4-5 w epilogue, 8-15 chain
-// group. Single-kernel form (FA: the A build runs in this kernel): 18 warps,
-// 0 MMA issuer, 1 TMA producer, 2-3 prep group, 4-7 WY group, 8-15 chain group,
-// 16-17 w epilogue. A warp reaches the TMEM lanes of quarter warp % 4.
+// issuer, 1 TMA producer, 2-5 prep group, 6-7 w epilogue, 8-15 chain group.
+// Single-kernel form (FA: the A build runs in this kernel): 18 warps, 0 MMA
+// issuer, 1 TMA producer, 2-3 prep group, 4-7 WY group, 8-15 chain group,
+// 16-17 w epilogue. A warp reaches the TMEM lanes of quarter warp % 4 and runs
+// on sub-partition warp % 4: the two-kernel form's w epilogue reads W from
+// lanes 64-127, so that its work shares no sub-partition with the MMA issuer
+// or with the chain warps that turn QK into P (lanes 0-63); on GB300 that
+// placement ran 2.5-3% faster than w in lanes 0-63 with warps 4-5.
 template <bool FA> constexpr int tc_threads() { return FA ? 576 : 512; }
 template <bool FA> constexpr int prep_threads() { return FA ? 64 : 128; }
 constexpr int kWThreads = 64, kChainThreads = 256, kWyThreads = 128;
@@ -61,7 +65,7 @@ struct TcLayout {
     // apart); HT reads the one v_g tile as both halves of its A operand.
     static constexpr uint32_t kStAbig = 0, kStBbig = KB * 16384;
     static constexpr uint32_t kStV = 2 * KB * 16384, kStZ = kStV + 8192, kStA = kStZ + 8192;
-    static constexpr uint32_t kStAp = kStA + 8192;               // A' (W's A operand rows 0-63)
+    static constexpr uint32_t kStAp = kStA + 8192;               // A': [A diag(beta); A'] is W's A operand
     static constexpr uint32_t kStage = kStAp + 8192;
     static constexpr uint32_t kP = 2 * kStage;                   // P
     static constexpr uint32_t kVN = kP + 8192;                   // v_new
@@ -263,10 +267,12 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t idBIG = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idHT = idesc_bf16(128, K, true, true);
             constexpr uint32_t idPV = idesc_bf16(128, 64, false, true);
-            // W = [A'; .] k, k read N-major from the stage's [h^T; k]; the rows under A'
-            // are whatever follows it: their products are unused
+            // W = [A diag(beta); A'] k (w in rows 64-127), k read N-major from the
+            // stage's [h^T; k]; single-kernel form: [A'; .] k (w in rows 0-63, the
+            // rows under A' being whatever follows it). The other half's products
+            // are unused.
             auto issue_w = [&](int s) {
-                const TileDesc da(s_base + Tl::ap(s), 16, 1024);
+                const TileDesc da(s_base + (FA ? Tl::ap(s) : s * Tl::stage + Lay::kStA), 16, 1024);
                 const TileDesc db(s_base + s * Tl::stage + Lay::kStBbig + 8192, 16384, 1024);
                 mma_bf16_k<false>(tmem + kColW, da.at(0), db.at(0), idW);
 #pragma unroll
@@ -416,12 +422,12 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int c = max(stall ? 1 : 0, issued - 2); c < issued; ++c)
                 mbar_wait(&bs->full[c & 1], (c >> 1) & 1, kWaitNs);
         }
-    } else if (FA ? (warp == 2 || warp == 3) : (warp == 2 || warp == 3 || warp == 6 || warp == 7)) {
+    } else if (FA ? (warp == 2 || warp == 3) : (warp >= 2 && warp < 6)) {
         // ================================================================ prep group
         // Per-chunk decay tables (A' = A diag(beta exp(g)) comes with A diag(beta)
         // from the WY kernel or, in the single-kernel form, from the WY group,
         // which also hands over the chunk's cumulative g and k-row factors).
-        const int ptid = warp < 4 ? tid - 64 : tid - 128;
+        const int ptid = tid - 64;
         const float *gcum_t = reinterpret_cast<const float *>(sm + FLay::kWtab);
         const float *rk_t = gcum_t + 256;
         // g of chunk c and of its last valid token, loaded one chunk ahead
@@ -505,10 +511,11 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             mbar_arrive(&bs->g_ready[gs]);
         }
-    } else if (FA ? warp >= 16 : warp < 6) {
+    } else if (FA ? warp >= 16 : (warp == 6 || warp == 7)) {
         // ================================================================ w epilogue
-        // Rows 0-63 of W (lane quarters 0-1) -> -w, bf16, under q in the stage's
-        // stacked operand (that half was last read by BIG(c - 2)).
+        // The w rows of W (lanes 64-127, quarters 2-3; single-kernel form lanes
+        // 0-63, quarters 0-1) -> -w, bf16, under q in the stage's stacked
+        // operand (that half was last read by BIG(c - 2)).
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int row = (warp & 3) * 32 + lane;
         for (int c = 0; c < NT; ++c) {
@@ -525,7 +532,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int e = 0; e < 32; ++e) v[e] = -__uint_as_float(r[e]);
                 unsigned char *base = sm + (c & 1) * Tl::stage + Lay::kStAbig + (f0 >> 6) * 16384;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_bf16x8(base + sw128(64 + row, (f0 & 63) * 2 + q * 16), v + q * 8);
+                for (int q = 0; q < 4; ++q)
+                    st_bf16x8(base + sw128(64 + (row & 63), (f0 & 63) * 2 + q * 16), v + q * 8);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
