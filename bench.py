@@ -88,12 +88,14 @@ def _fused(K, V, d):
 
 KERNEL_MODEL = {
     "gdn_fused_tc_kernel": ("hbm", _fused),
+    "gdn_wide_tc_kernel": ("hbm", _fused),
     "wy_prepare_kernel": ("alu", _simt_prepare),
     "chunk_h_kernel": ("alu", _simt_h),
     "chunk_o_kernel": ("alu", _simt_o),
 }
 KERNEL_SOURCE = {
     "gdn_fused_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc.cu",
+    "gdn_wide_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc_wide.cu",
     "gdn_wy_tc_kernel": "gated_delta_rule_35_gb300/csrc/gdn_tc_wy.cu",
     "gdn_decode_step_kernel": "gated_delta_rule_35_gb300/csrc/gdn_decode.cu",
     "wy_prepare_kernel": "gated_delta_rule_35_gb300/csrc/gdn_simt.cu",

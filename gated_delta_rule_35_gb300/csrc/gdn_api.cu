@@ -22,10 +22,10 @@ gdn_status check_problem(const gdn_problem *p) {
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->K <= 0 || p->V <= 0) return GDN_ERR_INVALID_ARG;
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC &&
-        p->algo != GDN_ALGO_TC_SINGLE)
+        p->algo != GDN_ALGO_TC_SINGLE && p->algo != GDN_ALGO_TC_WIDE)
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
-    const bool tc = p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE;
+    const bool tc = p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE || p->algo == GDN_ALGO_TC_WIDE;
     if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && tc)
         return GDN_ERR_UNSUPPORTED;   // per-channel decay runs on the SIMT pipeline
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
@@ -35,7 +35,12 @@ gdn_status check_problem(const gdn_problem *p) {
     if (p->H > 65535 || p->B > 65535) return GDN_ERR_UNSUPPORTED;
     if (tc && !tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)))
         return GDN_ERR_UNSUPPORTED;
+    if (p->algo == GDN_ALGO_TC_WIDE && p->V % 128 != 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
+}
+
+TcForm tc_form(gdn_algo algo) {
+    return algo == GDN_ALGO_TC_SINGLE ? TcForm::kSingle : algo == GDN_ALGO_TC_WIDE ? TcForm::kWide : TcForm::kTwo;
 }
 
 gdn_algo resolve_algo(const gdn_problem *p) {
@@ -58,7 +63,8 @@ size_t front_bytes(const gdn_problem *p) {
 size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
     if (p->T == 0) return 0;
     const size_t front = front_bytes(p);
-    if (algo == GDN_ALGO_TC) return front + tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+    if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_WIDE)
+        return front + tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
     if (algo == GDN_ALGO_TC_SINGLE) return front;   // A stays in the kernel
     return front + simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
 }
@@ -77,10 +83,12 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
     const gdn_algo algo = resolve_algo(p);
-    if (ex && algo == GDN_ALGO_TC && (ex->A || ex->w || ex->u || ex->v_new || ex->h))
+    if (ex && (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_WIDE) &&
+        (ex->A || ex->w || ex->u || ex->v_new || ex->h))
         return GDN_ERR_UNSUPPORTED;
     // the single-kernel form keeps A on chip and has no output stage
     if (algo == GDN_ALGO_TC_SINGLE && (ex || norm)) return GDN_ERR_UNSUPPORTED;
+    if (algo == GDN_ALGO_TC_WIDE && norm) return GDN_ERR_UNSUPPORTED;   // the stage runs 64 columns per CTA
     if (ex && algo == GDN_ALGO_SIMT && ex->A_beta) return GDN_ERR_UNSUPPORTED;
     const size_t need = kStatusBytes + body_bytes(p, algo);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
@@ -112,8 +120,8 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         e = marks.mark(0, stream);
         if (e == cudaSuccess) e = copy_state(a, stream);
         if (e == cudaSuccess) e = marks.mark(1, stream);
-    } else if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE) {
-        e = tc_forward(a, body, stream, marks, algo == GDN_ALGO_TC_SINGLE);
+    } else if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE || algo == GDN_ALGO_TC_WIDE) {
+        e = tc_forward(a, body, stream, marks, tc_form(algo));
         if (e == cudaSuccess && ex && ex->A_beta) e = tc_export_abeta(a, body, ex->A_beta, stream);
     } else {
         const SimtWorkspace ws = simt_carve(body, a.B, a.T, a.H, a.K, a.V);
@@ -144,8 +152,8 @@ int launches(const gdn_problem *p, const char **names, int max_names) {
         return 1;
     }
     const gdn_algo algo = resolve_algo(p);
-    if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE)
-        return tc_launches(algo == GDN_ALGO_TC_SINGLE, names, max_names);
+    if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE || algo == GDN_ALGO_TC_WIDE)
+        return tc_launches(tc_form(algo), p->B, p->H, p->V, names, max_names);
     for (int i = 0; names && i < kSimtLaunches && i < max_names; ++i) names[i] = kSimtKernelNames[i];
     return kSimtLaunches;
 }

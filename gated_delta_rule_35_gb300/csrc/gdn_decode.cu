@@ -270,11 +270,12 @@ gdn_status check_decode(const gdn_problem *p, const gdn_output_norm *norm) {
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->K <= 0 || p->V <= 0) return GDN_ERR_INVALID_ARG;
     if (p->dtype != GDN_F32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_SIMT && p->algo != GDN_ALGO_TC &&
-        p->algo != GDN_ALGO_TC_SINGLE)
+        p->algo != GDN_ALGO_TC_SINGLE && p->algo != GDN_ALGO_TC_WIDE)
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
     if (norm && (!norm->gate || !norm->weight || !(norm->eps >= 0.f))) return GDN_ERR_INVALID_ARG;
-    if (p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE) return GDN_ERR_UNSUPPORTED;
+    if (p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE || p->algo == GDN_ALGO_TC_WIDE)
+        return GDN_ERR_UNSUPPORTED;
     if (p->K % 64 != 0 || p->K > 256) return GDN_ERR_UNSUPPORTED;
     if (p->V % 16 != 0 || p->V > 4096) return GDN_ERR_UNSUPPORTED;
     if (p->H > 65535 || p->B > 65535) return GDN_ERR_UNSUPPORTED;

@@ -68,8 +68,15 @@ extern const char *const kSimtKernelNames[kSimtLaunches];
 // forward kernel reading it, or (single) one kernel that builds A itself.
 bool tc_supported(int K, int V, gdn_dtype dtype);
 size_t tc_workspace_bytes(int B, int T, int H, int K, int V);
-cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, bool single);
-int tc_launches(bool single, const char **names, int max_names);
+// Tensor-core forms: two kernels (the forward kernel 64 or 128 V columns per CTA,
+// by grid size), one kernel, or two kernels with the 128-column forward kernel.
+enum class TcForm { kTwo, kSingle, kWide };
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, TcForm form);
+int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_names);
+// The 128-column forward kernel (gdn_tc_wide.cu), reading A from abeta, and
+// whether the two-kernel form picks it for this shape.
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s);
+bool tc_wide(int B, int H, int V);
 // WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.
 cudaError_t wy_tc_forward(const Args &a, void *abeta, cudaStream_t s);
 // Converts the workspace's A diag(beta) to fp32 [B, T_pad, H, 64].

@@ -1260,17 +1260,20 @@ size_t tc_workspace_bytes(int B, int T, int H, int, int) {
     return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
 }
 
-int tc_launches(bool single, const char **names, int max_names) {
-    static const char *const kNames[2] = {"gdn_wy_tc_kernel", "gdn_fused_tc_kernel"};
-    const int n = single ? 1 : 2;
-    for (int i = 0; names && i < n && i < max_names; ++i) names[i] = kNames[2 - n + i];
+// Kernel names of the plain call (the output stage always runs on
+// gdn_fused_tc_kernel).
+int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_names) {
+    const bool wide = form == TcForm::kWide || (form == TcForm::kTwo && tc_wide(B, H, V));
+    const char *const two[2] = {"gdn_wy_tc_kernel", wide ? "gdn_wide_tc_kernel" : "gdn_fused_tc_kernel"};
+    const int n = form == TcForm::kSingle ? 1 : 2;
+    for (int i = 0; names && i < n && i < max_names; ++i) names[i] = n == 1 ? "gdn_fused_tc_kernel" : two[i];
     return n;
 }
 
-cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, bool single) {
+cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, TcForm form) {
     cudaError_t e = m.mark(0, s);
     if (e != cudaSuccess) return e;
-    if (single) {
+    if (form == TcForm::kSingle) {
         // single kernel: the WY matrix is built in the forward kernel itself
         e = (a.K == 128) ? launch_fused<128>(a, nullptr, s, true) : launch_fused<64>(a, nullptr, s, true);
         if (e != cudaSuccess) return e;
@@ -1278,7 +1281,10 @@ cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, 
     }
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
-    e = (a.K == 128) ? launch_fused<128>(a, ws, s, false) : launch_fused<64>(a, ws, s, false);
+    if (!a.gate && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V)))
+        e = wide_tc_forward(a, ws, s);
+    else
+        e = (a.K == 128) ? launch_fused<128>(a, ws, s, false) : launch_fused<64>(a, ws, s, false);
     if (e != cudaSuccess) return e;
     return m.mark(2, s);
 }

@@ -18,7 +18,7 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGNMENT = 0, 1, 2, 3
 GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_RAW_G, GDN_FLAG_QK_L2NORM, GDN_FLAG_PER_CHANNEL_DECAY = 1, 2, 4
-ALGOS = {"auto": 0, "simt": 1, "tc": 2, "tc1": 3}
+ALGOS = {"auto": 0, "simt": 1, "tc": 2, "tc1": 3, "tcw": 4}
 DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
 CHUNK = 64
 

@@ -74,11 +74,18 @@ typedef enum {
     GDN_ALGO_TC = 2,     /* tensor-core (tcgen05/TMEM, TMA) path, bf16 only: a
                           * kernel building every chunk's WY matrix (in parallel,
                           * to the workspace), then the forward kernel */
-    GDN_ALGO_TC_SINGLE = 3 /* the same in one kernel: each CTA builds its chunks'
+    GDN_ALGO_TC_SINGLE = 3, /* the same in one kernel: each CTA builds its chunks'
                           * WY matrices itself, one chunk ahead of their use, so
                           * A never reaches HBM (slower today: the build is a
                           * serial chain inside the CTA). Without the output stage
                           * and without the A export (else GDN_ERR_UNSUPPORTED) */
+    GDN_ALGO_TC_WIDE = 4 /* GDN_ALGO_TC with the wide forward kernel: one CTA per
+                          * 128 V columns of a head (W, q k^T and the operand
+                          * loads shared by both 64-column halves). GDN_ALGO_TC
+                          * and GDN_ALGO_AUTO pick it by themselves when the
+                          * 64-column grid would take more than one wave of SMs.
+                          * V a multiple of 128; without the output stage (else
+                          * GDN_ERR_UNSUPPORTED) */
 } gdn_algo;
 
 /* Input front-end options (gdn_problem.flags), a bit set; 0 = inputs as

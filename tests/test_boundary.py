@@ -171,6 +171,14 @@ def test_single_kernel_form_sizes_and_limits():
     assert native.launches(one) == ["gdn_fused_tc_kernel"]
     assert native.launches(two) == ["gdn_wy_tc_kernel", "gdn_fused_tc_kernel"]
     assert native.launches(native.problem(4, 2048, 16, 128, 128, native.GDN_BF16)) == native.launches(two)
+    # more 64-column tiles than SMs: the 128-column forward kernel (without a
+    # visible device the SM count is GB300's 152)
+    wide = native.problem(8, 8192, 64, 128, 128, native.GDN_BF16)
+    assert native.launches(wide) == ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel"]
+    assert native.launches(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tcw")) == native.launches(wide)
+    assert native.workspace_bytes(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tcw")) == \
+        native.workspace_bytes(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tc"))
+    assert native.workspace_bytes(native.problem(1, 64, 1, 128, 192, native.GDN_BF16, "tcw")) == 0
     kda = native.problem(1, 64, 1, 128, 128, native.GDN_BF16, "tc1", native.GDN_FLAG_PER_CHANNEL_DECAY)
     assert native.workspace_bytes(kda) == 0
     assert native.workspace_bytes(native.problem(1, 64, 1, 128, 128, native.GDN_F32, "tc1")) == 0
@@ -186,11 +194,17 @@ def test_single_kernel_form_sizes_and_limits():
                                            vp(FAKE), 1.0, None, vp(FAKE), None, vp(FAKE),
                                            native.workspace_bytes(p), ctypes.byref(ex), None)
     assert st == native.GDN_ERR_UNSUPPORTED
+    # the 128-column forward kernel has no output stage either
+    pw = native.problem(1, 64, 1, 128, 128, native.GDN_BF16, "tcw")
+    st = native.lib().gdn_chunk_fwd_ex(ctypes.byref(pw), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                       1.0, None, ctypes.byref(norm), vp(FAKE), None, vp(FAKE),
+                                       native.workspace_bytes(pw), None, 0, None)
+    assert st == native.GDN_ERR_UNSUPPORTED
 
 
 def test_flags_validated():
     """Known front-end bits are accepted by every path; unknown bits are rejected."""
-    for algo in ("simt", "tc", "tc1"):
+    for algo in ("simt", "tc", "tc1", "tcw"):
         for flags in (1, 2, 3):
             p = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, algo, flags)
             assert native.workspace_bytes(p) > native.workspace_bytes(

@@ -27,7 +27,7 @@ def _inputs():
     return x, {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
 
 
-@pytest.mark.parametrize("algo", ["tc", "tc1"])
+@pytest.mark.parametrize("algo", ["tc", "tc1", "tcw"])
 def test_withheld_loads_report_a_device_timeout_then_recover(algo):
     """Both tensor-core forms; in the single-kernel form the WY group's own
     waits (on the next chunk's W and U) run out as well."""

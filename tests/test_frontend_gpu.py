@@ -44,7 +44,7 @@ def gpu(x):
     return {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
 
 
-@pytest.mark.parametrize("algo", ["simt", "tc", "tc1"])
+@pytest.mark.parametrize("algo", ["simt", "tc", "tc1", "tcw"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 256)])
@@ -66,7 +66,7 @@ def test_frontend_parity(algo, dtype, mode, K, V, T):
     assert rel(hf, hf_ref) < TOL[dtype], rel(hf, hf_ref)
 
 
-@pytest.mark.parametrize("algo", ["simt", "tc", "tc1"])
+@pytest.mark.parametrize("algo", ["simt", "tc", "tc1", "tcw"])
 @pytest.mark.parametrize("g_div", [1.0, 0.25])
 def test_frontend_strong_decay(algo, g_div):
     """Chunk sums of the raw decays near -45 and -180: the second takes the

@@ -40,7 +40,7 @@ def run_oracle(x, scale=1.0):
                               to_f64(x["beta"]), scale, to_f64(x["h0"]))
 
 
-ALGOS = ["simt", "tc", "tc1"]
+ALGOS = ["simt", "tc", "tc1", "tcw"]
 
 
 @pytest.mark.parametrize("algo", ALGOS)
@@ -164,6 +164,20 @@ def test_split_resume(algo):
     oc = torch.cat([o1, o2], 1).float().cpu().numpy()
     assert rel(oc, o.float().cpu().numpy()) < 1e-3
     assert rel(h2.cpu().numpy(), hf.cpu().numpy()) < 1e-3
+
+
+@pytest.mark.parametrize("V", [128, 256])
+def test_wide_kernel_matches_narrow(V):
+    """The 128-column forward kernel against the 64-column one on the same
+    inputs: the same products in the same precision, only grouped differently
+    per CTA, so the two agree far inside the oracle tolerance."""
+    if not have_algo("tcw", 128, V, "bf16"):
+        pytest.skip("not built")
+    x = make_inputs(2, 300, 3, 128, V, dtype="bf16", seed=61 + V, h0_std=0.1)
+    o_w, hf_w = run_gpu(x, "tcw")
+    o_n, hf_n = run_gpu(x, "tc")
+    assert rel(o_w, o_n) < 1e-3, rel(o_w, o_n)
+    assert rel(hf_w, hf_n) < 1e-3, rel(hf_w, hf_n)
 
 
 def test_small_workload_fp32():
