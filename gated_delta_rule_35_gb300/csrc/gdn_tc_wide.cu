@@ -71,7 +71,8 @@ struct WideLayout {
 struct WideBars {
     uint64_t full[2], empty[2];                 // q and k, by chunk parity
     uint64_t ap_full, abv_full;                 // A'; A diag(beta) and v (one buffer each)
-    uint64_t big_done, h_done, o_done, u_done;  // MMA completions
+    uint64_t big_done, h_done, u_done;          // MMA completions
+    uint64_t o_done[2];                         // PV(c), by chunk parity (its readers alternate)
     // W(c) and its epilogue, one barrier per lane half (chunk parity): the aux
     // warps of a half see every phase of their own barrier in order, where
     // one shared barrier's parity would let a half run a chunk ahead
@@ -130,14 +131,15 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bs->w_ready[i], 64);               // the two aux warps on that half
         }
         mbar_init(&bs->h_done, 1);
-        mbar_init(&bs->o_done, 1);
+        mbar_init(&bs->o_done[0], 1);
+        mbar_init(&bs->o_done[1], 1);
         mbar_init(&bs->u_done, 1);
         for (int i = 0; i < 4; ++i) mbar_init(&bs->g_ready[i], kAuxThreads);
         mbar_init(&bs->o_seeded, kChainWarps * 16);       // the eight warps on q's lanes
         mbar_init(&bs->xo_ready, kChainWarps * 16);
         mbar_init(&bs->vn_ready, kChainWarps * 16);       // the eight on v_new's
         mbar_init(&bs->hs_ready, kChainWarps * 32);
-        mbar_init(&bs->o_free, kChainWarps * 16);
+        mbar_init(&bs->o_free, 64);                       // the two aux warps on O's lanes
         mbar_init(&bs->drain, 1);
         bs->abort = 0;
         fence_mbar_init();
@@ -194,7 +196,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const TileDesc db(s_base + Lay::kVN, 8192, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) mma_bf16_k<true>(tmem + kCWO, da.at(ks * 32), db.at(ks * 2048), idPV);
-                mma_commit(&bs->o_done);
+                mma_commit(&bs->o_done[c & 1]);
             };
             // W(c) may go once its k and A' landed, O(c - 1) (the other lane
             // half, which W(c) rewrites unchanged) is seeded, and O(c - 2) (its
@@ -278,6 +280,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tc_fence_after_sync();
                     issue_u(c + 1);
                 }
+                // PV(c) rewrites the other lane half too: O(c - 1) must be out and cleared
+                if (c >= 1 && !(ok = spin_bar(&bs->o_free, (c - 1) & 1, abort, wlim))) break;
                 tc_fence_after_sync();
                 issue_pv(c);
             }
@@ -326,14 +330,43 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     } else if (warp < 6) {
         // ================================================================ aux group
-        // Decay tables of every chunk (threads 0-63, one token each), then the
-        // w epilogue of the chunk on the two warps whose lane quarters hold its
-        // W: W(c) rows -> -w, bf16, into the one -w tile (last read by BIG(c - 1),
-        // done before W(c) was).
+        // Decay tables of every chunk (threads 0-63, one token each), and on the
+        // two warps whose lane quarters hold chunk c's W and O (lane half c % 2):
+        // o(c - 2) out of TMEM, those lanes cleared for W(c), then the w
+        // epilogue, W(c) rows -> -w, bf16, into the one -w tile (last read by
+        // BIG(c - 1), done before W(c) was). The chain warps stay on the chunk
+        // chain.
         const int ptid = tid - 64;
         const int q4 = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int wrow = (q4 & 1) * 32 + lane;
+        // o(cc) from O (these 32 lanes, all 128 columns), then the lanes cleared
+        auto write_o = [&](int cc) -> bool {
+            if (!warp_all(wait_bar(&bs->o_done[cc & 1], (cc >> 1) & 1, abort, wlim))) return false;
+            tc_fence_after_sync();
+            const int64_t oi = ((static_cast<int64_t>(b) * T + cc * 64 + wrow) * H + h) * V + vt * kWideBV;
+            const bool in = wrow < min(64, T - cc * 64);
+#pragma unroll 1
+            for (int bb = 0; bb < kWideBV / 32; ++bb) {
+                uint32_t r[32];
+                tmem_ld32(tmem + kCWO + lane_off + bb * 32, r);
+                tmem_wait_ld();
+                if (in) {
+                    float v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) store_bf16x8_global(o + oi + bb * 32 + q * 8, v + q * 8);
+                }
+            }
+            const uint32_t z[16] = {};
+#pragma unroll
+            for (int bb = 0; bb < kWideBV / 16; ++bb) tmem_st16(tmem + kCWO + lane_off + bb * 16, z);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(&bs->o_free);   // W(cc + 2) and PV(cc + 1) may rewrite these lanes
+            return true;
+        };
         auto load_g = [&](int c) {
             const int t = c * 64 + ptid;
             return (ptid < 64 && c < NT && t < T) ? g[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
@@ -348,16 +381,19 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                            : 1.f;
         };
         float g_next = load_g(0), gl_next = load_gl(0), rk_next = load_rk(0);
+        bool ok = true;
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1, gs = c & 3;
             const int n = min(64, T - c * 64);
+            const bool mine = (q4 >> 1) == (c & 1);   // W(c) and O(c) lie in these lanes
+            if (mine && c >= 2 && !(ok = write_o(c - 2))) break;
             const float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
             g_next = load_g(c + 1);
             gl_next = load_gl(c + 1);
             rk_next = load_rk(c + 1);
             // Slot c % 4's previous reader, chunk c - 4, finished before U(c - 3)
             // was issued, and chunk c's stage landing needs HT(c - 2).
-            if (!wait_bar(&bs->full[s], (c >> 1) & 1, abort, wlim)) break;
+            if (!(ok = wait_bar(&bs->full[s], (c >> 1) & 1, abort, wlim))) break;
             if (ptid < 64) {
                 float rq = 1.f;
                 if (l2norm) {
@@ -397,8 +433,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (ptid == 0) fz_s[gs] = fzc;
             }
             mbar_arrive(&bs->g_ready[gs]);
-            if ((q4 >> 1) != (c & 1)) continue;   // W(c) lies in the other lane half
-            if (!warp_all(wait_bar(&bs->w_done[c & 1], (c >> 1) & 1, abort, wlim))) break;
+            if (!mine) continue;   // W(c) lies in the other lane half
+            if (!(ok = warp_all(wait_bar(&bs->w_done[c & 1], (c >> 1) & 1, abort, wlim)))) break;
             tc_fence_after_sync();
 #pragma unroll 1
             for (int bb = 0; bb < K / 32; ++bb) {
@@ -417,6 +453,9 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before_sync();
             mbar_arrive(&bs->w_ready[c & 1]);
         }
+        // the last two chunks' o
+        for (int cc = max(0, NT - 2); ok && cc < NT; ++cc)
+            if ((q4 >> 1) == (cc & 1)) ok = write_o(cc);
     } else {
         // ================================================================ chain group
         // Chunk c's q rows sit in lane half c % 2: the eight warps there turn QK
@@ -533,7 +572,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 mbar_arrive(&bs->xo_ready);
             } else {
                 // v_new and v_g (v_new tile last read by PV(c - 1))
-                if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort, wlim)))) break;
+                if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort, wlim))))
+                    break;
                 const float gate = gate_s[gs * 64 + row];
                 const int atom = col0 >> 6, cb = (col0 & 63) * 2;
 #pragma unroll 1
@@ -585,27 +625,6 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             tc_fence_before_sync();
             mbar_arrive(&bs->hs_ready);
-            if (qside) {
-                // o(c), then these lanes of the W / O columns back to zero for W(c + 2)
-                if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort, wlim)))) break;
-                tc_fence_after_sync();
-                const int64_t oi = ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V + vt * kWideBV + col0;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float v[16];
-                    tmem_ld16f(tmem + kCWO + lane_off + col0 + half * 16, v);
-                    if (row < n) {
-                        store_bf16x8_global(o + oi + half * 16, v);
-                        store_bf16x8_global(o + oi + half * 16 + 8, v + 8);
-                    }
-                }
-                const uint32_t z[16] = {};
-                tmem_st16(tmem + kCWO + lane_off + col0, z);
-                tmem_st16(tmem + kCWO + lane_off + col0 + 16, z);
-                tmem_wait_st();
-                tc_fence_before_sync();
-                mbar_arrive(&bs->o_free);
-            }
         }
         // final state straight from tensor memory
         if (warp_all(ok) && h_final) {
