@@ -45,12 +45,13 @@ constexpr uint64_t kWyWaitNs = 1000000000ull;
 template <int K>
 struct WyLayout {
     static constexpr int KB = K / 64;
-    // k tile (K-major, KB blocks of 8 KB); after the Gram MMA the first 16 KB
-    // hold the stacked operand [N1; N2], read only by the first merge product
-    static constexpr uint32_t kK = 0;
-    static constexpr uint32_t kKBytes = (KB * 8192 > 16384) ? KB * 8192 : 16384;
+    // k tile twice, [k; k] per 64-feature block (16 KB each), so that the Gram
+    // product's rows land in both TMEM lane halves and all four warps form L.
+    // After the Gram MMA the first 16 KB hold the stacked operand [N1; N2],
+    // read only by the first merge product, and the next 16 KB [X; U].
+    static constexpr uint32_t kK = 0, kKBlk = 16384;
     static constexpr uint32_t kN = 0;
-    static constexpr uint32_t kXU = kKBytes;               // [X; U] stacked, then A0 (bf16)
+    static constexpr uint32_t kXU = 16384;                 // [X; U] stacked, then A0 (bf16)
     // The fp32 diagonal blocks [4][16][17] live in the U half of [X; U] until
     // X is built from them (U is written after the first merge product).
     static constexpr uint32_t kLd = kXU + 8192;
@@ -60,7 +61,7 @@ struct WyLayout {
     static constexpr uint32_t kY = kN + 8192;
     static constexpr uint32_t kOut = kY;
     // g, beta, beta exp(g) r, cf, r (64 floats each), a scan total; barriers
-    static constexpr uint32_t kMisc = kXU + 16384;
+    static constexpr uint32_t kMisc = (KB * kKBlk > kXU + 16384) ? KB * kKBlk : kXU + 16384;
     static constexpr uint32_t kBar = kMisc + 1344;
     static constexpr uint32_t kBytes = kBar + 256;
     static_assert(16 * 17 * 4 * 4 <= 8192, "diagonal blocks fit the U half");
@@ -105,10 +106,13 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_tma, KB * 8192);
+        mbar_arrive_expect_tx(bar_tma, KB * 16384);
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-            tma_load_4d(sm + Lay::kK + kb * 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
+        for (int kb = 0; kb < KB; ++kb) {
+            // the second copy is served from L2
+            tma_load_4d(sm + Lay::kK + kb * Lay::kKBlk, &tm_k, bar_tma, kb * 64, h, t0, b);
+            tma_load_4d(sm + Lay::kK + kb * Lay::kKBlk + 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
+        }
     }
     const bool raw_g = flags & GDN_FLAG_RAW_G, l2norm = flags & GDN_FLAG_QK_L2NORM;
     const int64_t my_row = (static_cast<int64_t>(b) * T + t0 + tid) * H + h;
@@ -186,11 +190,19 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(t[e]);
     };
 
-    // ---- G = k k^T, issued as M = 128 so that row r lands in TMEM lane r: the A
-    // rows past the k tile are whatever follows it (their products are unused),
-    // and two full warps form L instead of four half-empty ones
+    // ---- [G; G] = [k; k] k^T (M = 128): row r of G in TMEM lanes r and 64 + r,
+    // so warps 0-1 form L's columns 0-31 and warps 2-3 its columns 32-63
     if (__syncthreads_or(fail)) goto done;
-    mma_issue(128, s_k, s_k, false, K / 16);
+    if (tid == 0) {
+        tc_fence_after_sync();
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+        for (int ks = 0; ks < K / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * Lay::kKBlk + (ks & 3) * 32;
+            mma_bf16(tmem, smem_desc(s_k + off, 16, 1024, kLayoutSw128), smem_desc(s_k + off, 16, 1024, kLayoutSw128),
+                     id, ks > 0);
+        }
+        mma_commit(bar_mma);
+    }
     if (l2norm && tid < 64) {
         // |k_i|^2 from the k tile while the Gram runs. The 128-byte swizzle
         // permutes the 16-byte chunks within a row, which a sum of squares does
@@ -201,7 +213,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(sm + Lay::kK + kb * 8192 + tid * 128 +
+                const uint4 u = *reinterpret_cast<const uint4 *>(sm + Lay::kK + kb * Lay::kKBlk + tid * 128 +
                                                                  ((j ^ (tid & 7)) * 16));
                 const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -218,12 +230,14 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     mma_wait();
     if (__syncthreads_or(fail)) goto done;
-    if (warp < 2) {
-        const int r = warp * 32 + lane, rb = r >> 4;
+    {
+        // row r (lanes r and 64 + r), column blocks 2 ch and 2 ch + 1
+        const int r = (warp & 1) * 32 + lane, rb = r >> 4, ch = warp >> 1;
         const float gr = g_s[r], br = b_s[r] * rk_s[r];
         const float rf = br * __expf(gr - g_ref);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
+        for (int bi = 0; bi < 2; ++bi) {
+            const int blk = 2 * ch + bi;
             float v[16];
             load16(blk, v);
             if (r >= 0) {
