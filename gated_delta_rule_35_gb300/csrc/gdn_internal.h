@@ -73,10 +73,12 @@ size_t tc_workspace_bytes(int B, int T, int H, int K, int V);
 enum class TcForm { kTwo, kSingle, kWide };
 cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, TcForm form);
 int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_names);
-// The 128-column forward kernel (gdn_tc_wide.cu), reading A from abeta, and
-// whether the two-kernel form picks it for this shape.
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s);
+// The 128-column forward kernel (gdn_tc_wide.cu), reading A from abeta, for the
+// first `heads` of the B * H (b * H + h order); whether the two-kernel form picks
+// it for this shape; the device's SM count (152 when no device is visible).
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads);
 bool tc_wide(int B, int H, int V);
+int tc_sm_count();
 // WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.
 cudaError_t wy_tc_forward(const Args &a, void *abeta, cudaStream_t s);
 // Converts the workspace's A diag(beta) to fp32 [B, T_pad, H, 64].

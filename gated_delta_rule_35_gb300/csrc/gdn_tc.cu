@@ -173,7 +173,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float scale, int l2_prefetch, uint32_t *status, int l2norm,
                     const float *__restrict__ rk, const __nv_bfloat16 *__restrict__ gate,
                     const float *__restrict__ norm_w, float norm_eps, int nrank_arg,
-                    uint64_t wlim, int stall, const float *__restrict__ beta, int raw_g) {
+                    uint64_t wlim, int stall, const float *__restrict__ beta, int raw_g, int head0,
+                    int dep_wait) {
     static_assert(!(GATED && FA), "the output stage runs on the two-kernel form");
     using Lay = TcLayout<K>;
     using FLay = FaLayout<K>;
@@ -202,7 +203,11 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     Bars *bs = reinterpret_cast<Bars *>(sm + Tl::bar);
     volatile uint32_t *abort = &bs->abort;
 
-    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // one-dimensional grid over (head, V tile), heads from head0 on (b * H + h)
+    const int nvt = V / kTcBV;
+    const long long head = head0 + static_cast<long long>(blockIdx.x / nvt);
+    const int vt = static_cast<int>(blockIdx.x % nvt), h = static_cast<int>(head % H),
+              b = static_cast<int>(head / H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (T + 63) / 64;
 
@@ -253,8 +258,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // V tile); its barriers must be initialised before any CTA arrives on them.
     if (nrank) cluster_sync();
     // The setup above overlaps the WY kernel's last CTAs; everything below may
-    // read its output.
-    griddep_wait();
+    // read its output. Launched behind the wide kernel (dep_wait = 0), the WY
+    // kernel had completed before that one let this grid start.
+    if (dep_wait) griddep_wait();
     tc_fence_after_sync();
     const uint32_t tmem = bs->tmem;
     const uint32_t s_base = smem_u32(sm);
@@ -1158,6 +1164,9 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (nrank) cluster_sync();
     if (tid == 0 && *abort) atomicOr(status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    // Launched behind the wide kernel without waiting on it: this grid ends no
+    // sooner than that one, so whatever follows in the stream sees both done.
+    if (!dep_wait) griddep_wait();
 }
 
 // Stage export: A diag(beta), columns 0-63 of the bf16 workspace [B, T, H, 128],
@@ -1178,8 +1187,11 @@ __global__ void export_abeta_kernel(const __nv_bfloat16 *__restrict__ src, float
 
 // fa: the single-kernel form (abeta unused); else the second kernel of the
 // two-kernel form, reading A from abeta.
+// heads [head0, head0 + nheads) of the B * H; after_wide: launched right behind
+// gdn_wide_tc_kernel, which covered the other heads (early start, no wait on it)
 template <int K>
-cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool fa) {
+cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool fa, long long head0,
+                         long long nheads, bool after_wide) {
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B))
@@ -1198,10 +1210,10 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool 
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(a.V / kTcBV) * a.H * a.B;
+    const long long ctas = static_cast<long long>(a.V / kTcBV) * nheads;
     const int nrank = a.gate ? a.V / kTcBV : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.V / kTcBV, a.H, a.B);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(fa ? tc_threads<true>() : tc_threads<false>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -1212,7 +1224,7 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool 
     // own setup), which saves about 5 us on B8 H64 T8192. With one wave or
     // less the early start gains nothing and cost 20 us (1.7%) on
     // B1 H32 T32768, so those grids launch after the WY kernel ends.
-    if (!fa && ctas > sms) {
+    if (!fa && (ctas > sms || after_wide)) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
     }
@@ -1242,9 +1254,10 @@ cudaError_t launch_fused(const Args &a, const void *abeta, cudaStream_t s, bool 
         wlim_arg = armed;
         stall_arg = 1;
     }
+    int head0_arg = static_cast<int>(head0), dep_arg = after_wide ? 0 : 1;
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
                     &scale_arg, &pf_arg, &status_arg, &norm_arg, &rk_arg, &gate_arg, &nw_arg,
-                    &eps_arg, &nrank_arg, &wlim_arg, &stall_arg, &beta_arg, &rawg_arg};
+                    &eps_arg, &nrank_arg, &wlim_arg, &stall_arg, &beta_arg, &rawg_arg, &head0_arg, &dep_arg};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1260,13 +1273,33 @@ size_t tc_workspace_bytes(int B, int T, int H, int, int) {
     return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
 }
 
+// Heads of the two-kernel form's plain call that the wide kernel takes: all
+// of them, or (form kTwo) only whole waves of its CTAs when the rest fit one
+// wave of 64-column CTAs, which finish their chains sooner than a partial
+// wave of wide CTAs would.
+long long tc_wide_heads(TcForm form, int B, int H, int V) {
+    const long long heads = static_cast<long long>(B) * H;
+    if (form != TcForm::kTwo) return heads;
+    const int nvt = V / 128, sms = tc_sm_count();
+    const long long ctas = heads * nvt;
+    if (ctas <= sms) return heads;
+    const long long wide_heads = (ctas / sms) * sms / nvt;
+    return (heads - wide_heads) * (V / 64) <= sms ? wide_heads : heads;
+}
+
 // Kernel names of the plain call (the output stage always runs on
 // gdn_fused_tc_kernel).
 int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_names) {
-    const bool wide = form == TcForm::kWide || (form == TcForm::kTwo && tc_wide(B, H, V));
-    const char *const two[2] = {"gdn_wy_tc_kernel", wide ? "gdn_wide_tc_kernel" : "gdn_fused_tc_kernel"};
-    const int n = form == TcForm::kSingle ? 1 : 2;
-    for (int i = 0; names && i < n && i < max_names; ++i) names[i] = n == 1 ? "gdn_fused_tc_kernel" : two[i];
+    if (form == TcForm::kSingle) {
+        if (names && max_names > 0) names[0] = "gdn_fused_tc_kernel";
+        return 1;
+    }
+    const bool wide = form == TcForm::kWide || tc_wide(B, H, V);
+    const bool split = wide && tc_wide_heads(form, B, H, V) < static_cast<long long>(B) * H;
+    const char *const all[3] = {"gdn_wy_tc_kernel", wide ? "gdn_wide_tc_kernel" : "gdn_fused_tc_kernel",
+                                "gdn_fused_tc_kernel"};
+    const int n = split ? 3 : 2;
+    for (int i = 0; names && i < n && i < max_names; ++i) names[i] = all[i];
     return n;
 }
 
@@ -1275,16 +1308,28 @@ cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, 
     if (e != cudaSuccess) return e;
     if (form == TcForm::kSingle) {
         // single kernel: the WY matrix is built in the forward kernel itself
-        e = (a.K == 128) ? launch_fused<128>(a, nullptr, s, true) : launch_fused<64>(a, nullptr, s, true);
+        const long long heads = static_cast<long long>(a.B) * a.H;
+        e = (a.K == 128) ? launch_fused<128>(a, nullptr, s, true, 0, heads, false)
+                         : launch_fused<64>(a, nullptr, s, true, 0, heads, false);
         if (e != cudaSuccess) return e;
         return m.mark(1, s);
     }
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
-    if (!a.gate && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V)))
-        e = wide_tc_forward(a, ws, s);
-    else
-        e = (a.K == 128) ? launch_fused<128>(a, ws, s, false) : launch_fused<64>(a, ws, s, false);
+    const long long heads = static_cast<long long>(a.B) * a.H;
+    if (!a.gate && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V))) {
+        // whole waves on the wide kernel, the last partial one on the 64-column one
+        const long long wh = tc_wide_heads(form, a.B, a.H, a.V);
+        if ((e = wide_tc_forward(a, ws, s, wh)) != cudaSuccess) return e;
+        if (wh == heads) return m.mark(2, s);
+        if ((e = m.mark(2, s)) != cudaSuccess) return e;
+        e = (a.K == 128) ? launch_fused<128>(a, ws, s, false, wh, heads - wh, m.ev == nullptr)
+                         : launch_fused<64>(a, ws, s, false, wh, heads - wh, m.ev == nullptr);
+        if (e != cudaSuccess) return e;
+        return m.mark(3, s);
+    }
+    e = (a.K == 128) ? launch_fused<128>(a, ws, s, false, 0, heads, false)
+                     : launch_fused<64>(a, ws, s, false, 0, heads, false);
     if (e != cudaSuccess) return e;
     return m.mark(2, s);
 }

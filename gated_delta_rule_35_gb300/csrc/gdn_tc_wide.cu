@@ -104,7 +104,11 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     WideBars *bs = reinterpret_cast<WideBars *>(sm + Lay::kBar);
     volatile uint32_t *abort = &bs->abort;
 
-    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // one-dimensional grid over (head, 128-column V block), head = b * H + h
+    const int nvt = V / kWideBV;
+    const long long head = static_cast<long long>(blockIdx.x / nvt);
+    const int vt = static_cast<int>(blockIdx.x % nvt), h = static_cast<int>(head % H),
+              b = static_cast<int>(head / H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (T + 63) / 64;
 
@@ -151,8 +155,10 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_before_sync();
     __syncthreads();
     // the setup above overlaps the WY kernel's last CTAs; everything below may
-    // read its output
+    // read its output. A 64-column kernel for the remaining heads may start
+    // behind this grid from here on (it reads only the WY kernel's output).
     griddep_wait();
+    griddep_launch_dependents();
     tc_fence_after_sync();
     const uint32_t tmem = bs->tmem;
     const uint32_t s_base = smem_u32(sm);
@@ -646,7 +652,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, kWideTmemCols);
 }
 
-int sm_count() {
+int sm_count_of_device() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
@@ -657,7 +663,7 @@ int sm_count() {
 }
 
 template <int K>
-cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s) {
+cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
@@ -666,16 +672,16 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s) {
     const auto kernel = gdn_wide_tc_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(a.V / kWideBV) * a.H * a.B;
+    const long long ctas = static_cast<long long>(a.V / kWideBV) * heads;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.V / kWideBV, a.H, a.B);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(kWideThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     int nattr = 0;
     // as for gdn_fused_tc_kernel: an early start only pays with more than one wave
-    if (ctas > sm_count()) {
+    if (ctas > sm_count_of_device()) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
     }
@@ -705,11 +711,13 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s) {
 bool tc_wide(int B, int H, int V) {
     // with 64-wide tiles the grid would need more than one wave of SMs; with
     // fewer heads the narrow form keeps more SMs busy
-    return V % kWideBV == 0 && static_cast<long long>(B) * H * (V / 64) > sm_count();
+    return V % kWideBV == 0 && static_cast<long long>(B) * H * (V / 64) > sm_count_of_device();
 }
 
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s) {
-    return a.K == 128 ? launch_wide<128>(a, abeta, s) : launch_wide<64>(a, abeta, s);
+int tc_sm_count() { return sm_count_of_device(); }
+
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
+    return a.K == 128 ? launch_wide<128>(a, abeta, s, heads) : launch_wide<64>(a, abeta, s, heads);
 }
 
 }  // namespace gdn

@@ -172,9 +172,13 @@ def test_single_kernel_form_sizes_and_limits():
     assert native.launches(two) == ["gdn_wy_tc_kernel", "gdn_fused_tc_kernel"]
     assert native.launches(native.problem(4, 2048, 16, 128, 128, native.GDN_BF16)) == native.launches(two)
     # more 64-column tiles than SMs: the 128-column forward kernel (without a
-    # visible device the SM count is GB300's 152)
-    wide = native.problem(8, 8192, 64, 128, 128, native.GDN_BF16)
+    # visible device the SM count is GB300's 152); B8 H64: three whole waves of
+    # it (456 heads), the other 56 heads on the 64-column kernel (112 CTAs)
+    wide = native.problem(2, 8192, 32, 128, 256, native.GDN_BF16)
     assert native.launches(wide) == ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel"]
+    split = native.problem(8, 8192, 64, 128, 128, native.GDN_BF16)
+    assert native.launches(split) == ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel", "gdn_fused_tc_kernel"]
+    assert native.launches(native.problem(8, 8192, 64, 128, 128, native.GDN_BF16, "tcw")) == native.launches(wide)
     assert native.launches(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tcw")) == native.launches(wide)
     assert native.workspace_bytes(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tcw")) == \
         native.workspace_bytes(native.problem(1, 64, 1, 128, 256, native.GDN_BF16, "tc"))

@@ -180,6 +180,26 @@ def test_wide_kernel_matches_narrow(V):
     assert rel(hf_w, hf_n) < 1e-3, rel(hf_w, hf_n)
 
 
+def test_wide_waves_then_narrow_remainder():
+    """B1 H160: 160 wide CTAs on 152 SMs, so 152 heads run on the wide kernel
+    and the other 8 on the 64-column kernel launched right behind it; every
+    head against the oracle."""
+    if not have_algo("tc", 128, 128, "bf16"):
+        pytest.skip("not built")
+    p = native.problem(1, 130, 160, 128, 128, torch.bfloat16, "tc")
+    names = native.launches(p)
+    x = make_inputs(1, 130, 160, 128, 128, dtype="bf16", seed=71, h0_std=0.1)
+    o, hf = run_gpu(x, "tc")
+    o_ref, hf_ref = run_oracle(x)
+    assert rel(o, o_ref) < TOL["bf16"], rel(o, o_ref)
+    assert rel(hf, hf_ref) < TOL["bf16"], rel(hf, hf_ref)
+    # the last heads specifically (the 64-column kernel's share when split)
+    assert rel(o[:, :, 150:], o_ref[:, :, 150:]) < TOL["bf16"]
+    assert rel(hf[:, 150:], hf_ref[:, 150:]) < TOL["bf16"]
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert names == ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel", "gdn_fused_tc_kernel"]
+
+
 def test_small_workload_fp32():
     """The fp32 workload (B1 H1 T256 K=V=64) in full, tolerance 1e-4."""
     x = make_workload("f32_b1_h1_t256_k64_v64")
