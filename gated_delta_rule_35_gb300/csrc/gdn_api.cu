@@ -26,8 +26,9 @@ gdn_status check_problem(const gdn_problem *p) {
         return GDN_ERR_INVALID_ARG;
     if (p->flags & ~kKnownFlags) return GDN_ERR_INVALID_ARG;
     const bool tc = p->algo == GDN_ALGO_TC || p->algo == GDN_ALGO_TC_SINGLE || p->algo == GDN_ALGO_TC_WIDE;
-    if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && tc)
-        return GDN_ERR_UNSUPPORTED;   // per-channel decay runs on the SIMT pipeline
+    // per-channel decay: the CUDA-core pipeline or the two-kernel tensor-core form
+    if ((p->flags & GDN_FLAG_PER_CHANNEL_DECAY) && tc && p->algo != GDN_ALGO_TC)
+        return GDN_ERR_UNSUPPORTED;
     if (p->K != 64 && p->K != 128) return GDN_ERR_UNSUPPORTED;
     if (p->V % 64 != 0 || p->V > 256) return GDN_ERR_UNSUPPORTED;
     // Every index is computed in 64 bits; B*T*H rows must still fit a grid.
@@ -45,10 +46,11 @@ TcForm tc_form(gdn_algo algo) {
 
 gdn_algo resolve_algo(const gdn_problem *p) {
     if (p->algo != GDN_ALGO_AUTO) return static_cast<gdn_algo>(p->algo);
-    if (p->flags & GDN_FLAG_PER_CHANNEL_DECAY) return GDN_ALGO_SIMT;
     return tc_supported(p->K, p->V, static_cast<gdn_dtype>(p->dtype)) ? GDN_ALGO_TC
                                                                        : GDN_ALGO_SIMT;
 }
+
+bool per_channel(const gdn_problem *p) { return p->flags & GDN_FLAG_PER_CHANNEL_DECAY; }
 
 // Front-end region: g_cum (one fp32 per token-head, or per token-head-channel
 // with per-channel decay) and rk (one per token-head).
@@ -63,6 +65,13 @@ size_t front_bytes(const gdn_problem *p) {
 size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
     if (p->T == 0) return 0;
     const size_t front = front_bytes(p);
+    if (algo == GDN_ALGO_TC && per_channel(p)) {
+        // with 'auto' also room for the CUDA-core pipeline, which serves a call
+        // with the output stage (the per-channel tensor-core form has none)
+        const size_t kda = kda_tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+        const size_t simt = simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
+        return front + ((p->algo == GDN_ALGO_AUTO && simt > kda) ? simt : kda);
+    }
     if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_WIDE)
         return front + tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
     if (algo == GDN_ALGO_TC_SINGLE) return front;   // A stays in the kernel
@@ -82,7 +91,16 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
                           norm ? norm->gate : nullptr, norm ? norm->weight : nullptr};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
-    const gdn_algo algo = resolve_algo(p);
+    gdn_algo algo = resolve_algo(p);
+    const bool kda_tc = algo == GDN_ALGO_TC && per_channel(p);
+    // the per-channel tensor-core form has no output stage and exports only
+    // A diag(beta); with 'auto' such calls run on the CUDA-core pipeline, for
+    // which workspace_bytes reserved room
+    const bool simt_only = norm || (ex && (ex->A || ex->w || ex->u || ex->v_new || ex->h));
+    if (kda_tc && simt_only) {
+        if (p->algo != GDN_ALGO_AUTO) return GDN_ERR_UNSUPPORTED;
+        algo = GDN_ALGO_SIMT;
+    }
     if (ex && (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_WIDE) &&
         (ex->A || ex->w || ex->u || ex->v_new || ex->h))
         return GDN_ERR_UNSUPPORTED;
@@ -90,7 +108,7 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
     if (algo == GDN_ALGO_TC_SINGLE && (ex || norm)) return GDN_ERR_UNSUPPORTED;
     if (algo == GDN_ALGO_TC_WIDE && norm) return GDN_ERR_UNSUPPORTED;   // the stage runs 64 columns per CTA
     if (ex && algo == GDN_ALGO_SIMT && ex->A_beta) return GDN_ERR_UNSUPPORTED;
-    const size_t need = kStatusBytes + body_bytes(p, algo);
+    const size_t need = kStatusBytes + body_bytes(p, resolve_algo(p));
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
 
     Args a;
@@ -120,6 +138,9 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         e = marks.mark(0, stream);
         if (e == cudaSuccess) e = copy_state(a, stream);
         if (e == cudaSuccess) e = marks.mark(1, stream);
+    } else if (algo == GDN_ALGO_TC && per_channel(p)) {
+        e = kda_tc_forward(a, body, stream, marks);
+        if (e == cudaSuccess && ex && ex->A_beta) e = tc_export_abeta(a, body, ex->A_beta, stream);
     } else if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE || algo == GDN_ALGO_TC_WIDE) {
         e = tc_forward(a, body, stream, marks, tc_form(algo));
         if (e == cudaSuccess && ex && ex->A_beta) e = tc_export_abeta(a, body, ex->A_beta, stream);
@@ -152,6 +173,10 @@ int launches(const gdn_problem *p, const char **names, int max_names) {
         return 1;
     }
     const gdn_algo algo = resolve_algo(p);
+    if (algo == GDN_ALGO_TC && per_channel(p)) {
+        for (int i = 0; names && i < kKdaTcLaunches && i < max_names; ++i) names[i] = kKdaTcKernelNames[i];
+        return kKdaTcLaunches;
+    }
     if (algo == GDN_ALGO_TC || algo == GDN_ALGO_TC_SINGLE || algo == GDN_ALGO_TC_WIDE)
         return tc_launches(tc_form(algo), p->B, p->H, p->V, names, max_names);
     for (int i = 0; names && i < kSimtLaunches && i < max_names; ++i) names[i] = kSimtKernelNames[i];

@@ -84,6 +84,14 @@ cudaError_t wy_tc_forward(const Args &a, void *abeta, cudaStream_t s);
 // Converts the workspace's A diag(beta) to fp32 [B, T_pad, H, 64].
 cudaError_t tc_export_abeta(const Args &a, const void *ws, float *dst, cudaStream_t s);
 
+// Per-channel decay on the tensor cores (gdn_kda_tc.cu): a prep kernel per
+// chunk, then the forward kernel over the chunks; workspace [A diag(beta) | P A
+// diag(beta)] bf16 [B, T, H, 128] first, as the plain path's.
+size_t kda_tc_workspace_bytes(int B, int T, int H, int K, int V);
+cudaError_t kda_tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m);
+constexpr int kKdaTcLaunches = 2;
+extern const char *const kKdaTcKernelNames[kKdaTcLaunches];
+
 // h_final = h0 (or 0) for T == 0.
 cudaError_t copy_state(const Args &a, cudaStream_t s);
 constexpr const char *kCopyStateName = "copy_state_kernel";

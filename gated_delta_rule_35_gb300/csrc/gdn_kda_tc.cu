@@ -1,0 +1,738 @@
+// Per-channel (KDA) decay on the tensor cores: the chunked form of the
+// "KdaSplit" page's recurrence, in which every token decays each state row d
+// by its own factor exp(gamma_t,d) before the delta-rule read and write.
+//
+// With g the chunk-local cumulative log decay (a K-vector per token) a chunk
+// of 64 tokens entered with state h gives
+//   L_ij = beta_i sum_d k_id k_jd exp(g_id - g_jd)         (j < i)
+//   A    = (I + L)^-1,  Ab = A diag(beta)
+//   w    = Ab (k * exp(g)),  u = Ab v,  v_new = u - w h
+//   P_ij = scale sum_d q_id k_jd exp(g_id - g_jd)           (j <= i)
+//   o    = scale (q * exp(g)) h + P v_new
+//   h'   = diag(exp(g_last)) h + (k * exp(g_last - g))^T v_new
+// Substituting v_new into o gives o = PA v + Q' h with PA = P Ab and
+// Q' = scale (q * exp(g)) - PA (k * exp(g)), so the forward kernel gets v_new
+// and o of a chunk from one stacked M = 128 accumulator,
+//   [v_new; o] = [Ab; PA] v + [-w; Q'] h,
+// and its chain per chunk is that product, the v_new copy, the state-update
+// product and the state update.
+//
+// gdn_kda_prep_tc_kernel (one CTA per chunk and head) builds from q, k, g and
+// beta: X1 = [Ab | PA] (bf16 [B, T, H, 128]), X2 = [-w | Q'] (bf16
+// [B, T, H, 2K]), KH = k * exp(g_last - g) (bf16 [B, T, H, K]) and the chunk's
+// decay exp(g_last) (fp32 [B, NT, H, K]):
+//   operands  kp = k exp(g - r), qp = q exp(g - r), km = k exp(r - g), r = g_last / 2
+//   MMA 1     [G; S] = [kp; qp] km^T    (G_ij = sum_d k_id k_jd exp(g_id - g_jd), S with q_i)
+//   epi       L = diag(beta) G (strictly lower, fp32), P = scale S (lower, bf16)
+//   SIMT      A = (I + L)^-1 by forward substitution, one column per thread (fp32)
+//   MMA 2     [. ; PA] = [Ab; P] Ab
+//   MMA 3     [w; PA ke] = [Ab; PA] ke,  ke = k exp(g)
+//   epi       -w and Q' = q_hat - PA ke, TMA stores
+// With r = g_last / 2 and non-positive log decays every factor lies within
+// exp(+-|g_last| / 2), so the factored products are exact up to rounding while
+// every channel has |g_last| <= 160; a chunk with a stronger decay takes L and P
+// from one exponential per term on the CUDA cores instead (the masked entries
+// of the factored product may overflow; they are replaced, never multiplied).
+//
+// gdn_kda_fwd_tc_kernel (one CTA per 64 V columns of a head) runs the chunk
+// loop: the fp32 state sits in registers, one K row per thread, and its bf16
+// copy in shared memory is the B operand of the next chunk's product.
+#include "gdn_internal.h"
+#include "tc_sync.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kKdaThreads = 128;
+constexpr uint64_t kKdaWaitNs = 1000000000ull;
+constexpr float kFactorLimit = 160.f;   // |g_last| up to which the products are factored
+
+__device__ __forceinline__ void bar_sync_warps23() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+__device__ __forceinline__ void st_bf16(unsigned char *p, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float ld_bf16(const unsigned char *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+
+// ================================================================= prep kernel
+template <int K>
+struct KdaPrepLayout {
+    static constexpr int KB = K / 64;
+    // q and k tiles as loaded (K-major, 8 KB per 64 features); with the
+    // factored products they are overwritten in place by q_hat = scale q exp(g)
+    // and KH, otherwise those two go to the (then unused) [kp; qp] region
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = KB * 8192;
+    static constexpr uint32_t kOpA = 2 * KB * 8192;        // [kp; qp] per feature block, 16 KB each
+    static constexpr uint32_t kOpB = kOpA + KB * 16384;    // km (K-major), later the -w staging
+    static constexpr uint32_t kKe = kOpB + KB * 8192;      // ke (rows = tokens): MMA 3's B
+    static constexpr uint32_t kAP = kKe + KB * 8192;       // [Ab; P], then [Ab; PA]
+    static constexpr uint32_t kLStride = 68;               // L rows, 16-byte aligned (fp32)
+    // g (fp32 [64][K]), then L (fp32 [64][kLStride])
+    static constexpr uint32_t kG = kAP + 16384;
+    static constexpr uint32_t kGBytes = (64 * K > 64 * kLStride) ? 64 * K * 4 : 64 * kLStride * 4;
+    // beta, row factors of q and k (64 each), r (K)
+    static constexpr uint32_t kMisc = kG + kGBytes;
+    static constexpr uint32_t kBar = kMisc + (3 * 64 + K) * 4;
+    static constexpr uint32_t kBytes = kBar + 64;
+};
+
+constexpr uint32_t kPrepColG = 0, kPrepColPA = 64, kPrepColW = 128, kPrepTmemCols = 256;
+
+template <int K>
+__global__ void __launch_bounds__(kKdaThreads, 1)
+gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_x2,
+                       const __grid_constant__ CUtensorMap tm_kh, const float *__restrict__ g,
+                       const float *__restrict__ beta, float *__restrict__ dec_out, float scale, int T,
+                       int H, int NT, uint32_t *status, int flags) {
+    using Lay = KdaPrepLayout<K>;
+    constexpr int KB = K / 64;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float *g_s = reinterpret_cast<float *>(sm + Lay::kG);
+    float *L_s = g_s;
+    float *b_s = reinterpret_cast<float *>(sm + Lay::kMisc);
+    float *fq_s = b_s + 64, *fk_s = b_s + 128, *r_s = b_s + 192;
+    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kBar);
+    uint64_t *bar_mma = bar_tma + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
+
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int t0 = c * 64, n = min(64, T - t0);
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kPrepTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    // the forward kernel may be scheduled as SMs free up
+    griddep_launch_dependents();
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar_tma, 2 * KB * 8192);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+            tma_load_4d(sm + Lay::kQ + kb * 8192, &tm_q, bar_tma, kb * 64, h, t0, b);
+            tma_load_4d(sm + Lay::kK + kb * 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
+        }
+    }
+    const bool raw_g = flags & GDN_FLAG_RAW_G, l2norm = flags & GDN_FLAG_QK_L2NORM;
+    // g tile; rows >= n read as 0 (their q and k rows are zero, so they add nothing)
+    const int64_t row0 = (static_cast<int64_t>(b) * T + t0) * H + h;   // (b, t0, h)
+    for (int e = tid; e < 64 * (K / 4); e += kKdaThreads) {
+        const int i = e / (K / 4), d4 = e % (K / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n) x = *reinterpret_cast<const float4 *>(g + (row0 + static_cast<int64_t>(i) * H) * K + d4 * 4);
+        *reinterpret_cast<float4 *>(g_s + i * K + d4 * 4) = x;
+    }
+    if (tid < 64) b_s[tid] = tid < n ? beta[row0 + static_cast<int64_t>(tid) * H] : 0.f;
+    __syncthreads();
+    if (raw_g && tid < K) {
+        // chunk-local inclusive sum, one channel per thread
+        float acc = 0.f;
+        for (int i = 0; i < 64; ++i) {
+            acc += g_s[i * K + tid];
+            g_s[i * K + tid] = acc;
+        }
+    }
+    __syncthreads();
+    bool fz = true;
+    if (tid < K) {
+        const float gl = g_s[(n - 1) * K + tid];
+        r_s[tid] = 0.5f * gl;
+        fz = fabsf(gl) <= kFactorLimit;
+        dec_out[((static_cast<int64_t>(b) * NT + c) * H + h) * K + tid] = __expf(gl);
+    }
+    fz = __syncthreads_and(fz);
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t qh_off = fz ? Lay::kQ : Lay::kOpA;
+    const uint32_t kh_off = fz ? Lay::kK : Lay::kOpA + KB * 8192;
+    const uint32_t s_ap = smem_u32(sm + Lay::kAP);
+    bool fail = !mbar_wait(bar_tma, 0, kKdaWaitNs);
+    uint32_t phase = 0;
+    auto mma_wait = [&]() {
+        fail |= !mbar_wait(bar_mma, phase, kKdaWaitNs);
+        phase ^= 1;
+        tc_fence_after_sync();
+    };
+
+    do {
+        if (__syncthreads_or(fail)) break;
+        {
+            // row factors: 1, or 1 / sqrt(|x_i|^2 + eps) of the row as loaded
+            const int i = tid & 63;
+            const uint32_t base = tid < 64 ? Lay::kQ : Lay::kK;
+            float f = 1.f;
+            if (l2norm) {
+                float ss = 0.f;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 u = ld_shared_v4(sm + base + kb * 8192 + sw128(i, 16 * j));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 p = unpack_bf16(w4[e]);
+                            ss = fmaf(p.x, p.x, fmaf(p.y, p.y, ss));
+                        }
+                    }
+                f = rsqrtf(ss + kL2NormEps);
+            }
+            (tid < 64 ? fq_s : fk_s)[i] = f;
+        }
+        __syncthreads();
+        // ---- operands, 8 features of one row per item; in place only after
+        // the item has read its own q and k
+        for (int it = tid; it < 64 * KB * 8; it += kKdaThreads) {
+            const int j = it & 7, kb = (it >> 3) % KB, i = it / (8 * KB);
+            const int d0 = kb * 64 + 8 * j;
+            const uint32_t cell = kb * 8192 + sw128(i, 16 * j);
+            const uint4 uq = ld_shared_v4(sm + Lay::kQ + cell), uk = ld_shared_v4(sm + Lay::kK + cell);
+            const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
+            const float fq = fq_s[i], fk = fk_s[i];
+            float qv[8], kv[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = unpack_bf16(wq[e]), bb = unpack_bf16(wk[e]);
+                qv[2 * e] = a.x * fq;
+                qv[2 * e + 1] = a.y * fq;
+                kv[2 * e] = bb.x * fk;
+                kv[2 * e + 1] = bb.y * fk;
+            }
+            float qhat[8], kh[8], ke[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float gv = g_s[i * K + d0 + e];
+                const float eg = __expf(gv);
+                qhat[e] = scale * qv[e] * eg;
+                ke[e] = kv[e] * eg;
+                kh[e] = kv[e] * __expf(2.f * r_s[d0 + e] - gv);
+            }
+            if (fz) {
+                float kp[8], qp[8], km[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float gr = g_s[i * K + d0 + e] - r_s[d0 + e];
+                    const float up = __expf(gr), dn = __expf(-gr);
+                    kp[e] = kv[e] * up;
+                    qp[e] = qv[e] * up;
+                    km[e] = kv[e] * dn;
+                }
+                st_bf16x8(sm + Lay::kOpA + kb * 16384 + sw128(i, 16 * j), kp);
+                st_bf16x8(sm + Lay::kOpA + kb * 16384 + 8192 + sw128(i, 16 * j), qp);
+                st_bf16x8(sm + Lay::kOpB + cell, km);
+            }
+            st_bf16x8(sm + Lay::kKe + cell, ke);
+            st_bf16x8(sm + qh_off + cell, qhat);
+            st_bf16x8(sm + kh_off + cell, kh);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after_sync();
+            if (fz) {
+                // [G; S] = [kp; qp] km^T
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+                const TileDesc da(smem_u32(sm + Lay::kOpA), 16, 1024), db(smem_u32(sm + Lay::kOpB), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_bf16(tmem + kPrepColG, da.at((ks >> 2) * 16384 + (ks & 3) * 32),
+                             db.at((ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
+                mma_commit(bar_mma);
+            }
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) tma_store_4d(&tm_kh, sm + kh_off + kb * 8192, kb * 64, h, t0, b);
+            bulk_commit_group();
+        }
+        if (fz) {
+            mma_wait();
+            if (__syncthreads_or(fail)) break;
+            // rows 0-63 of the accumulator (warps 0-1): G -> L; rows 64-127: S -> P
+            const int i = tid & 63;
+            if (tid < 64) {
+                const float bi = b_s[i];
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    float v[16];
+                    tmem_ld16f(tmem + lane_off + kPrepColG + blk * 16, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) L_s[i * Lay::kLStride + blk * 16 + e] = (blk * 16 + e < i) ? bi * v[e] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    float v[16];
+                    tmem_ld16f(tmem + lane_off + kPrepColG + blk * 16, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = (blk * 16 + e <= i) ? scale * v[e] : 0.f;
+                    st_bf16x8(sm + Lay::kAP + sw128(64 + i, blk * 32), v);
+                    st_bf16x8(sm + Lay::kAP + sw128(64 + i, blk * 32 + 16), v + 8);
+                }
+            }
+        } else {
+            // one exponential per term (exponents <= 0 on the kept entries):
+            // threads 0-63 row i of L, threads 64-127 row i of P
+            const int i = tid & 63;
+            const bool is_p = tid >= 64;
+            const uint32_t xbase = is_p ? Lay::kQ : Lay::kK;
+            const float fi = is_p ? fq_s[i] * scale : fk_s[i] * b_s[i];
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+#pragma unroll 1
+            for (int d = 0; d < K; ++d) {
+                const uint32_t col = (d >> 6) * 8192, byte = 2 * (d & 63);
+                const float xi = ld_bf16(sm + xbase + col + sw128(i, byte));
+                const float gi = g_s[i * K + d];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const bool keep = is_p ? (j <= i) : (j < i);
+                    const float kj = ld_bf16(sm + Lay::kK + col + sw128(j, byte)) * fk_s[j];
+                    const float t = xi * kj * __expf(gi - g_s[j * K + d]);
+                    acc[j] += keep ? t : 0.f;   // a dropped term may overflow; it is never used
+                }
+            }
+            __syncthreads();   // every read of g done before L overwrites it
+            if (!is_p) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) L_s[i * Lay::kLStride + j] = fi * acc[j];
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = fi * acc[ch * 8 + e];
+                    st_bf16x8(sm + Lay::kAP + sw128(64 + i, ch * 16), v);
+                }
+            }
+        }
+        __syncthreads();
+        // ---- A = (I + L)^-1, column j per thread: (I + L) a = e_j top to bottom
+        if (tid < 64) {
+            const int j = tid;
+            float a[64];
+            a[0] = j == 0 ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 1; i < 64; ++i) {
+                const float *Li = L_s + i * Lay::kLStride;
+                float s = i == j ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < (i & ~3); m += 4) {
+                    const float4 l = *reinterpret_cast<const float4 *>(Li + m);
+                    s = fmaf(-l.x, a[m], s);
+                    s = fmaf(-l.y, a[m + 1], s);
+                    s = fmaf(-l.z, a[m + 2], s);
+                    s = fmaf(-l.w, a[m + 3], s);
+                }
+#pragma unroll
+                for (int m = i & ~3; m < i; ++m) s = fmaf(-Li[m], a[m], s);
+                a[i] = s;
+            }
+            // Ab = A diag(beta): column j, rows 0-63 of [Ab; P]
+            const float bj = b_s[j];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) st_bf16(sm + Lay::kAP + sw128(i, 2 * j), a[i] * bj);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // ---- [. ; PA] = [Ab; P] Ab (Ab read again as the B operand, rows along N)
+        if (tid == 0) {
+            tc_fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 64, false, true);
+            const TileDesc da(s_ap, 16, 1024), db(s_ap, 8192, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kPrepColPA, da.at(ks * 32), db.at(ks * 2048), id, ks > 0);
+            mma_commit(bar_mma);
+        }
+        mma_wait();
+        if (__syncthreads_or(fail)) break;
+        if (tid >= 64) {
+            const int i = tid - 64;
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kPrepColPA + blk * 16, v);
+                st_bf16x8(sm + Lay::kAP + sw128(64 + i, blk * 32), v);
+                st_bf16x8(sm + Lay::kAP + sw128(64 + i, blk * 32 + 16), v + 8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // ---- X1 out; [w; PA ke] = [Ab; PA] ke
+        if (tid == 0) {
+            tc_fence_after_sync();
+            tma_store_4d(&tm_x1, sm + Lay::kAP, 0, h, t0, b);
+            tma_store_4d(&tm_x1, sm + Lay::kAP + 8192, 64, h, t0, b);
+            bulk_commit_group();
+            const uint32_t id = idesc_bf16(128, K, false, true);
+            const TileDesc da(s_ap, 16, 1024), db(smem_u32(sm + Lay::kKe), 8192, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kPrepColW, da.at(ks * 32), db.at(ks * 2048), id, ks > 0);
+            mma_commit(bar_mma);
+        }
+        mma_wait();
+        if (__syncthreads_or(fail)) break;
+        {
+            const int i = tid & 63;
+#pragma unroll 1
+            for (int blk = 0; blk < K / 16; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kPrepColW + blk * 16, v);
+                const int kb = blk >> 2;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t cell = kb * 8192 + sw128(i, (blk & 3) * 32 + half * 16);
+                    float x[8];
+                    if (tid < 64) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = -v[half * 8 + e];
+                        st_bf16x8(sm + Lay::kOpB + cell, x);
+                    } else {
+                        const uint4 u = ld_shared_v4(sm + qh_off + cell);
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 p = unpack_bf16(w4[e]);
+                            x[2 * e] = p.x - v[half * 8 + 2 * e];
+                            x[2 * e + 1] = p.y - v[half * 8 + 2 * e + 1];
+                        }
+                        st_bf16x8(sm + qh_off + cell, x);
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+                tma_store_4d(&tm_x2, sm + Lay::kOpB + kb * 8192, kb * 64, h, t0, b);
+                tma_store_4d(&tm_x2, sm + qh_off + kb * 8192, K + kb * 64, h, t0, b);
+            }
+            bulk_commit_group();
+        }
+    } while (false);
+    if (tid == 0) {
+        bulk_wait_group_read0();   // only the shared sources must outlive the CTA
+        if (fail) atomicOr(status, 2u);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// ================================================================= forward kernel
+template <int K>
+struct KdaFwdLayout {
+    static constexpr int KB = K / 64;
+    static constexpr uint32_t kX1 = 0;                   // [Ab; PA] (16 KB)
+    static constexpr uint32_t kX2 = 16384;               // [-w; Q'] per feature block, 16 KB each
+    static constexpr uint32_t kKH = kX2 + KB * 16384;    // KH, rows = tokens, 8 KB per feature block
+    static constexpr uint32_t kV = kKH + KB * 8192;      // v, 64 tokens x 64 columns
+    static constexpr uint32_t kStage = kV + 8192;
+    static constexpr uint32_t kHB = 2 * kStage;           // state, bf16, rows = features (K x 64)
+    static constexpr uint32_t kVN = kHB + KB * 8192;      // v_new, bf16 (64 x 64)
+    static constexpr uint32_t kO = kVN + 8192;            // o staging for the TMA store
+    static constexpr uint32_t kBar = kO + 8192;
+    static constexpr uint32_t kBytes = kBar + 64;
+};
+
+constexpr uint32_t kFwdColD = 0, kFwdColH = 64, kFwdTmemCols = 128;
+
+template <int K>
+__global__ void __launch_bounds__(kKdaThreads, 1)
+gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_x2,
+                      const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ dec,
+                      const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V, int NT,
+                      uint32_t *status) {
+    using Lay = KdaFwdLayout<K>;
+    constexpr int KB = K / 64;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::kBar);   // [2]
+    uint64_t *mma_bar = full + 2, *ht_bar = full + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + 4);
+
+    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t s_base = smem_u32(sm);
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kFwdTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mma_bar, 1);
+        mbar_init(ht_bar, 1);
+        fence_mbar_init();
+    }
+    // the state: row d = tid of the K x 64 block of columns [64 vt, 64 vt + 64)
+    const int d = tid;
+    const int64_t srow = ((static_cast<int64_t>(b) * H + h) * K + d) * V + vt * 64;
+    float hr[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) hr[e] = 0.f;
+    if (h0 && d < K) {
+#pragma unroll
+        for (int e = 0; e < 64; e += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(h0 + srow + e);
+            hr[e] = x.x, hr[e + 1] = x.y, hr[e + 2] = x.z, hr[e + 3] = x.w;
+        }
+    }
+    auto write_state = [&]() {
+        if (d < K) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) st_bf16x8(sm + Lay::kHB + sw128(d, ch * 16), hr + ch * 8);
+        }
+    };
+    write_state();
+    // everything below reads the prep kernel's output
+    griddep_wait();
+    auto load_stage = [&](int c) {
+        unsigned char *st = sm + (c & 1) * Lay::kStage;
+        const int t0 = c * 64;
+        mbar_arrive_expect_tx(&full[c & 1], Lay::kStage);
+        tma_load_4d(st + Lay::kX1, &tm_x1, &full[c & 1], 0, h, t0, b);
+        tma_load_4d(st + Lay::kX1 + 8192, &tm_x1, &full[c & 1], 64, h, t0, b);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+            tma_load_4d(st + Lay::kX2 + kb * 16384, &tm_x2, &full[c & 1], kb * 64, h, t0, b);
+            tma_load_4d(st + Lay::kX2 + kb * 16384 + 8192, &tm_x2, &full[c & 1], K + kb * 64, h, t0, b);
+            tma_load_4d(st + Lay::kKH + kb * 8192, &tm_kh, &full[c & 1], kb * 64, h, t0, b);
+        }
+        tma_load_4d(st + Lay::kV, &tm_v, &full[c & 1], vt * 64, h, t0, b);
+    };
+    if (tid == 0) {
+        load_stage(0);
+        if (NT > 1) load_stage(1);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    // [v_new; o] = [Ab; PA] v (first) + [-w; Q'] h
+    constexpr uint32_t idD = idesc_bf16(128, 64, false, true);
+    constexpr uint32_t idHT = idesc_bf16(128, 64, true, true);
+    auto issue_a = [&](int s) {
+        const uint32_t st = s_base + s * Lay::kStage;
+        const TileDesc da(st + Lay::kX1, 16, 1024), db(st + Lay::kV, 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kFwdColD, da.at(ks * 32), db.at(ks * 2048), idD, ks > 0);
+    };
+    auto issue_b = [&](int s) {
+        const uint32_t st = s_base + s * Lay::kStage;
+        const TileDesc da(st + Lay::kX2, 16, 1024), db(s_base + Lay::kHB, 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < K / 16; ++ks)
+            mma_bf16_k<true>(tmem + kFwdColD, da.at((ks >> 2) * 16384 + (ks & 3) * 32), db.at(ks * 2048), idD);
+    };
+    // dH = KH^T v_new: KH read M-major (features along M; with K = 64 the upper
+    // 64 rows repeat the lower ones and are not read)
+    auto issue_ht = [&](int s) {
+        const uint32_t st = s_base + s * Lay::kStage;
+        const TileDesc da(st + Lay::kKH, K == 128 ? 8192 : 0, 1024), db(s_base + Lay::kVN, 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kFwdColH, da.at(ks * 2048), db.at(ks * 2048), idHT, ks > 0);
+    };
+
+    bool fail = false;   // thread 0: a load wait gave up (then no MMA is issued)
+    bool a_issued = false;
+    for (int c = 0; c < NT; ++c) {
+        const int s = c & 1;
+        if (tid == 0) {
+            if (!fail && !a_issued) {
+                fail = !mbar_wait(&full[s], (c >> 1) & 1, kKdaWaitNs);
+                if (!fail) {
+                    tc_fence_after_sync();
+                    issue_a(s);
+                }
+            }
+            if (!fail) {
+                tc_fence_after_sync();
+                issue_b(s);
+            }
+            mma_commit(mma_bar);   // arrives at once when nothing was issued
+        }
+        const float dv = d < K ? dec[((static_cast<int64_t>(b) * NT + c) * H + h) * K + d] : 0.f;
+        fail |= !mbar_wait(mma_bar, c & 1, kKdaWaitNs);
+        if (__syncthreads_or(fail)) break;
+        tc_fence_after_sync();
+        if (tid < 64) {
+            // v_new row (token) tid -> the B operand of the state update
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kFwdColD + blk * 16, v);
+                st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32), v);
+                st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32 + 16), v + 8);
+            }
+        } else {
+            // o row (token) tid - 64 -> staging; the previous chunk's store has
+            // read it once its issuing thread has waited
+            if (tid == 64) bulk_wait_group_read0();
+            bar_sync_warps23();
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kFwdColD + blk * 16, v);
+                st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32), v);
+                st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32 + 16), v + 8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        a_issued = false;
+        if (tid == 0) {
+            tc_fence_after_sync();
+            issue_ht(s);
+            mma_commit(ht_bar);
+            // the next chunk's [Ab; PA] v behind it: the accumulator was read above
+            if (c + 1 < NT && !fail) {
+                fail = !mbar_wait(&full[s ^ 1], ((c + 1) >> 1) & 1, kKdaWaitNs);
+                if (!fail) {
+                    tc_fence_after_sync();
+                    issue_a(s ^ 1);
+                    a_issued = true;
+                }
+            }
+        }
+        if (tid == 64) {
+            tma_store_4d(&tm_o, sm + Lay::kO, vt * 64, h, c * 64, b);
+            bulk_commit_group();
+        }
+        fail |= !mbar_wait(ht_bar, c & 1, kKdaWaitNs);
+        tc_fence_after_sync();
+        // the stage's last reader (the state update) is done
+        if (tid == 0 && !fail && c + 2 < NT) load_stage(c + 2);
+        if (d < K) {
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kFwdColH + blk * 16, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) hr[blk * 16 + e] = fmaf(dv, hr[blk * 16 + e], v[e]);
+            }
+        }
+        write_state();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        if (__syncthreads_or(fail)) break;
+    }
+    if (!fail && d < K) {
+#pragma unroll
+        for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4 *>(h_final + srow + e) = make_float4(hr[e], hr[e + 1], hr[e + 2], hr[e + 3]);
+    }
+    if (tid == 64) bulk_wait_group0();
+    if (tid == 0 && fail) atomicOr(status, 2u);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kFwdTmemCols);
+}
+
+struct KdaWs {
+    void *x1, *x2, *kh;
+    float *dec;
+};
+
+size_t rows_of(int B, int T, int H) { return static_cast<size_t>(B) * T * H; }
+
+KdaWs kda_carve(void *ws, int B, int T, int H, int K) {
+    char *p = static_cast<char *>(ws);
+    KdaWs w;
+    const size_t rows = rows_of(B, T, H);
+    w.x1 = p;
+    p += align_up(rows * 128 * 2);
+    w.x2 = p;
+    p += align_up(rows * 2 * K * 2);
+    w.kh = p;
+    p += align_up(rows * K * 2);
+    w.dec = reinterpret_cast<float *>(p);
+    return w;
+}
+
+template <int K>
+cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
+    const KdaWs w = kda_carve(ws, a.B, a.T, a.H, K);
+    CUtensorMap mq, mk, mx1, mx2, mkh, mv, mo;
+    if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&mx1, w.x1, 128, a.H, a.T, a.B) || !make_tmap_bthx(&mx2, w.x2, 2 * K, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&mkh, w.kh, K, a.H, a.T, a.B) || !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
+        !make_tmap_bthx(&mo, a.o, a.V, a.H, a.T, a.B))
+        return cudaErrorInvalidValue;
+    const int smem_p = static_cast<int>(KdaPrepLayout<K>::kBytes + 1024);
+    const int smem_f = static_cast<int>(KdaFwdLayout<K>::kBytes + 1024);
+    cudaError_t e = cudaFuncSetAttribute(gdn_kda_prep_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_p);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gdn_kda_fwd_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f);
+    if (e != cudaSuccess) return e;
+    if ((e = m.mark(0, s)) != cudaSuccess) return e;
+    gdn_kda_prep_tc_kernel<K><<<dim3(a.NT, a.H, a.B), kKdaThreads, smem_p, s>>>(
+        mq, mk, mx1, mx2, mkh, a.g, a.beta, w.dec, a.scale, a.T, a.H, a.NT, a.status, a.flags);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = m.mark(1, s)) != cudaSuccess) return e;
+    // The forward grid may start while the prep kernel's last CTAs run (its
+    // setup and state load overlap them); it waits for their output before
+    // its first load. Only with more than one wave: otherwise its CTAs would
+    // hold SMs the prep kernel still needs.
+    const long long ctas = static_cast<long long>(a.V / 64) * a.H * a.B;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.V / 64, a.H, a.B);
+    cfg.blockDim = dim3(kKdaThreads);
+    cfg.dynamicSmemBytes = smem_f;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (ctas > tc_sm_count()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const float *dec = w.dec;
+    const float *h0 = a.h0;
+    float *hf = a.h_final;
+    int T = a.T, H = a.H, V = a.V, NT = a.NT;
+    uint32_t *status = a.status;
+    void *args[] = {&mx1, &mx2, &mkh, &mv, &mo, &dec, &h0, &hf, &T, &H, &V, &NT, &status};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(gdn_kda_fwd_tc_kernel<K>), args);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return m.mark(2, s);
+}
+
+}  // namespace
+
+const char *const kKdaTcKernelNames[kKdaTcLaunches] = {"gdn_kda_prep_tc_kernel", "gdn_kda_fwd_tc_kernel"};
+
+size_t kda_tc_workspace_bytes(int B, int T, int H, int K, int) {
+    const size_t rows = rows_of(B, T, H);
+    return align_up(rows * 128 * 2) + align_up(rows * 2 * K * 2) + align_up(rows * K * 2) +
+           align_up(static_cast<size_t>(B) * num_chunks(T) * H * K * sizeof(float));
+}
+
+cudaError_t kda_tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
+    return a.K == 128 ? launch_kda<128>(a, ws, s, m) : launch_kda<64>(a, ws, s, m);
+}
+
+}  // namespace gdn

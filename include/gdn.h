@@ -106,8 +106,14 @@ typedef enum {
  *    S[i, :] <- exp(gamma_t[i]) S[i, :]; in the chunked form every
  *    exp(g_i - g_j) becomes a per-channel factor inside the k and q products.
  *    It combines with the other flags (the cumulative sum is then per
- *    channel). The chunked forward runs it on the CUDA-core pipeline only:
- *    GDN_ALGO_TC gives GDN_ERR_UNSUPPORTED and GDN_ALGO_AUTO picks SIMT.
+ *    channel). The chunked forward runs it on the CUDA-core pipeline or, for
+ *    bf16, on a tensor-core form of its own under GDN_ALGO_TC (a prep kernel
+ *    per chunk building the decay-weighted WY and attention products, then
+ *    the forward kernel over the chunks); GDN_ALGO_TC_SINGLE and
+ *    GDN_ALGO_TC_WIDE give GDN_ERR_UNSUPPORTED. That form has no output stage
+ *    and exports only A_beta: with GDN_ALGO_TC such calls give
+ *    GDN_ERR_UNSUPPORTED, with GDN_ALGO_AUTO they run on the CUDA-core
+ *    pipeline, and the workspace size for GDN_ALGO_AUTO covers both.
  * gdn_decode_step always takes raw gamma and accepts either g flag; it
  * honours GDN_FLAG_QK_L2NORM and GDN_FLAG_PER_CHANNEL_DECAY (gamma [B,T,H,K]). */
 enum {

@@ -247,18 +247,29 @@ def test_output_norm_validated():
     assert dec(128, 128, native.OutputNorm(None, FAKE, 1e-6)) == native.GDN_ERR_INVALID_ARG
 
 
-def test_per_channel_flag_routes_to_simt():
+def test_per_channel_flag_routes():
+    """Per-channel decay: bf16 on the tensor-core form of its own (two kernels),
+    fp32 on the CUDA-core pipeline; 'auto' reserves room for both, since a call
+    with the output stage or the stage exports runs on the CUDA-core pipeline."""
     flags = native.GDN_FLAG_PER_CHANNEL_DECAY
     p_tc = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "tc", flags)
-    assert native.workspace_bytes(p_tc) == 0
-    assert _call(p_tc) == native.GDN_ERR_UNSUPPORTED
     p_auto = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "auto", flags)
     p_simt = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "simt", flags)
-    assert native.workspace_bytes(p_auto) == native.workspace_bytes(p_simt) > 0
+    assert 0 < native.workspace_bytes(p_tc) <= native.workspace_bytes(p_auto)
+    assert native.workspace_bytes(p_auto) == max(native.workspace_bytes(p_tc), native.workspace_bytes(p_simt))
+    kda = ["gdn_kda_prep_tc_kernel", "gdn_kda_fwd_tc_kernel"]
+    assert native.launches(p_tc) == kda and native.launches(p_auto) == kda
+    for form in ("tc1", "tcw"):
+        assert native.workspace_bytes(native.problem(2, 100, 3, 128, 128, native.GDN_BF16, form, flags)) == 0
+    p32 = native.problem(2, 100, 3, 128, 128, native.GDN_F32, "auto", flags)
+    assert native.launches(p32) == ["wy_prepare_kernel", "chunk_h_kernel", "chunk_o_kernel"]
     # the front-end's g region holds one value per channel with this flag
     plain = native.problem(2, 100, 3, 128, 128, native.GDN_BF16, "simt")
     assert native.workspace_bytes(p_simt) - native.workspace_bytes(plain) >= 2 * 100 * 3 * 127 * 4 - 256
-    assert native.launches(p_auto) == ["wy_prepare_kernel", "chunk_h_kernel", "chunk_o_kernel"]
+    # tensor-core workspace: [A diag(beta) | P A diag(beta)], [-w | Q'], KH (bf16), decays
+    rows = 2 * 100 * 3
+    body = native.workspace_bytes(p_tc) - native.workspace_bytes(native.problem(2, 0, 3, 128, 128, native.GDN_BF16, "tc", flags))
+    assert body >= rows * (128 + 256 + 128) * 2 + 2 * 2 * 3 * 128 * 4
 
 
 def test_host_binding_output_validation():
