@@ -62,29 +62,29 @@ __device__ __forceinline__ float ld_bf16(const unsigned char *p) {
 template <int K>
 struct KdaPrepLayout {
     static constexpr int KB = K / 64;
-    // q and k tiles as loaded (K-major, 8 KB per 64 features); with the
-    // factored products they are overwritten in place by q_hat = scale q exp(g)
-    // and KH, otherwise those two go to the (then unused) [kp; qp] region
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = KB * 8192;
-    static constexpr uint32_t kOpA = 2 * KB * 8192;        // [kp; qp] per feature block, 16 KB each
-    static constexpr uint32_t kOpB = kOpA + KB * 16384;    // km (K-major), later the -w staging
-    static constexpr uint32_t kKe = kOpB + KB * 8192;      // ke (rows = tokens): MMA 3's B
-    static constexpr uint32_t kAP = kKe + KB * 8192;       // [Ab; P], then [Ab; PA]
+    // Per 64-feature block (16 KB): rows 0-63 the k tile, rows 64-127 the q
+    // tile, as loaded. With the factored products they become [kp; qp] in
+    // place (MMA 1's A), then [ke; qp] (ke: MMA 3's B) and [ke; Q'] (Q' staged
+    // for its store); otherwise [ke; q_hat], then [ke; Q'].
+    static constexpr uint32_t kKQ = 0;
+    // km (K-major, MMA 1's B), then KH in place (staged for its store), then -w
+    static constexpr uint32_t kM = KB * 16384;
+    static constexpr uint32_t kAP = kM + KB * 8192;        // [Ab; P], then [Ab; PA]
     static constexpr uint32_t kLStride = 68;               // L rows, 16-byte aligned (fp32)
     // g (fp32 [64][K]), then L (fp32 [64][kLStride])
     static constexpr uint32_t kG = kAP + 16384;
     static constexpr uint32_t kGBytes = (64 * K > 64 * kLStride) ? 64 * K * 4 : 64 * kLStride * 4;
-    // beta, row factors of q and k (64 each), r (K)
+    // beta, row factors of q and k (64 each), r and exp(r) (K each)
     static constexpr uint32_t kMisc = kG + kGBytes;
-    static constexpr uint32_t kBar = kMisc + (3 * 64 + K) * 4;
+    static constexpr uint32_t kBar = kMisc + (3 * 64 + 2 * K) * 4;
     static constexpr uint32_t kBytes = kBar + 64;
 };
 
 constexpr uint32_t kPrepColG = 0, kPrepColPA = 64, kPrepColW = 128, kPrepTmemCols = 256;
 
 template <int K>
-__global__ void __launch_bounds__(kKdaThreads, 1)
+// Two CTAs per SM (98.8 KB of shared memory and 256 TMEM columns each at K = 128).
+__global__ void __launch_bounds__(kKdaThreads, 2)
 gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_x2,
                        const __grid_constant__ CUtensorMap tm_kh, const float *__restrict__ g,
@@ -97,7 +97,7 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     float *g_s = reinterpret_cast<float *>(sm + Lay::kG);
     float *L_s = g_s;
     float *b_s = reinterpret_cast<float *>(sm + Lay::kMisc);
-    float *fq_s = b_s + 64, *fk_s = b_s + 128, *r_s = b_s + 192;
+    float *fq_s = b_s + 64, *fk_s = b_s + 128, *r_s = b_s + 192, *er_s = r_s + K;
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + Lay::kBar);
     uint64_t *bar_mma = bar_tma + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_tma + 2);
@@ -121,18 +121,28 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         mbar_arrive_expect_tx(bar_tma, 2 * KB * 8192);
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) {
-            tma_load_4d(sm + Lay::kQ + kb * 8192, &tm_q, bar_tma, kb * 64, h, t0, b);
-            tma_load_4d(sm + Lay::kK + kb * 8192, &tm_k, bar_tma, kb * 64, h, t0, b);
+            tma_load_4d(sm + Lay::kKQ + kb * 16384, &tm_k, bar_tma, kb * 64, h, t0, b);
+            tma_load_4d(sm + Lay::kKQ + kb * 16384 + 8192, &tm_q, bar_tma, kb * 64, h, t0, b);
         }
     }
     const bool raw_g = flags & GDN_FLAG_RAW_G, l2norm = flags & GDN_FLAG_QK_L2NORM;
-    // g tile; rows >= n read as 0 (their q and k rows are zero, so they add nothing)
     const int64_t row0 = (static_cast<int64_t>(b) * T + t0) * H + h;   // (b, t0, h)
-    for (int e = tid; e < 64 * (K / 4); e += kKdaThreads) {
-        const int i = e / (K / 4), d4 = e % (K / 4);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n) x = *reinterpret_cast<const float4 *>(g + (row0 + static_cast<int64_t>(i) * H) * K + d4 * 4);
-        *reinterpret_cast<float4 *>(g_s + i * K + d4 * 4) = x;
+    {
+        // g tile, every load issued before the first store; rows >= n read as 0
+        // (their q and k rows are zero too, so they add nothing)
+        constexpr int kPer = 64 * (K / 4) / kKdaThreads;
+        float4 x[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = tid + u * kKdaThreads, i = e / (K / 4), d4 = e % (K / 4);
+            x[u] = i < n ? *reinterpret_cast<const float4 *>(g + (row0 + static_cast<int64_t>(i) * H) * K + d4 * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = tid + u * kKdaThreads, i = e / (K / 4), d4 = e % (K / 4);
+            *reinterpret_cast<float4 *>(g_s + i * K + d4 * 4) = x[u];
+        }
     }
     if (tid < 64) b_s[tid] = tid < n ? beta[row0 + static_cast<int64_t>(tid) * H] : 0.f;
     __syncthreads();
@@ -149,15 +159,15 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     if (tid < K) {
         const float gl = g_s[(n - 1) * K + tid];
         r_s[tid] = 0.5f * gl;
+        er_s[tid] = __expf(0.5f * gl);
         fz = fabsf(gl) <= kFactorLimit;
         dec_out[((static_cast<int64_t>(b) * NT + c) * H + h) * K + tid] = __expf(gl);
     }
     fz = __syncthreads_and(fz);
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t qh_off = fz ? Lay::kQ : Lay::kOpA;
-    const uint32_t kh_off = fz ? Lay::kK : Lay::kOpA + KB * 8192;
     const uint32_t s_ap = smem_u32(sm + Lay::kAP);
+    // (the barriers were initialised before the block-wide barriers above)
     bool fail = !mbar_wait(bar_tma, 0, kKdaWaitNs);
     uint32_t phase = 0;
     auto mma_wait = [&]() {
@@ -165,13 +175,32 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         phase ^= 1;
         tc_fence_after_sync();
     };
+    // item it of the 64 x K / 8 chunks of 8 features: row, block, chunk
+    auto item = [](int it, int &i, int &kb, int &j) {
+        j = it & 7;
+        kb = (it >> 3) % KB;
+        i = it / (8 * KB);
+    };
+    auto unpack8 = [](const uint4 u, float f, float (&x)[8]) {
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 p = unpack_bf16(w4[e]);
+            x[2 * e] = p.x * f;
+            x[2 * e + 1] = p.y * f;
+        }
+    };
+    auto load8 = [](const float *p, float (&x)[8]) {
+        const float4 a = *reinterpret_cast<const float4 *>(p), bb = *reinterpret_cast<const float4 *>(p + 4);
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = bb.x, x[5] = bb.y, x[6] = bb.z, x[7] = bb.w;
+    };
 
     do {
         if (__syncthreads_or(fail)) break;
         {
             // row factors: 1, or 1 / sqrt(|x_i|^2 + eps) of the row as loaded
             const int i = tid & 63;
-            const uint32_t base = tid < 64 ? Lay::kQ : Lay::kK;
+            const uint32_t base = Lay::kKQ + (tid < 64 ? 8192 : 0);
             float f = 1.f;
             if (l2norm) {
                 float ss = 0.f;
@@ -179,84 +208,55 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint4 u = ld_shared_v4(sm + base + kb * 8192 + sw128(i, 16 * j));
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                        float x[8];
+                        unpack8(ld_shared_v4(sm + base + kb * 16384 + sw128(i, 16 * j)), 1.f, x);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 p = unpack_bf16(w4[e]);
-                            ss = fmaf(p.x, p.x, fmaf(p.y, p.y, ss));
-                        }
+                        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
                     }
                 f = rsqrtf(ss + kL2NormEps);
             }
             (tid < 64 ? fq_s : fk_s)[i] = f;
         }
         __syncthreads();
-        // ---- operands, 8 features of one row per item; in place only after
-        // the item has read its own q and k
-        for (int it = tid; it < 64 * KB * 8; it += kKdaThreads) {
-            const int j = it & 7, kb = (it >> 3) % KB, i = it / (8 * KB);
-            const int d0 = kb * 64 + 8 * j;
-            const uint32_t cell = kb * 8192 + sw128(i, 16 * j);
-            const uint4 uq = ld_shared_v4(sm + Lay::kQ + cell), uk = ld_shared_v4(sm + Lay::kK + cell);
-            const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
-            const float fq = fq_s[i], fk = fk_s[i];
-            float qv[8], kv[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 a = unpack_bf16(wq[e]), bb = unpack_bf16(wk[e]);
-                qv[2 * e] = a.x * fq;
-                qv[2 * e + 1] = a.y * fq;
-                kv[2 * e] = bb.x * fk;
-                kv[2 * e + 1] = bb.y * fk;
-            }
-            float qhat[8], kh[8], ke[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float gv = g_s[i * K + d0 + e];
-                const float eg = __expf(gv);
-                qhat[e] = scale * qv[e] * eg;
-                ke[e] = kv[e] * eg;
-                kh[e] = kv[e] * __expf(2.f * r_s[d0 + e] - gv);
-            }
-            if (fz) {
+        if (fz) {
+            // ---- kp, qp in place, km beside them
+            for (int it = tid; it < 64 * KB * 8; it += kKdaThreads) {
+                int i, kb, j;
+                item(it, i, kb, j);
+                const int d0 = kb * 64 + 8 * j;
+                const uint32_t ck = Lay::kKQ + kb * 16384 + sw128(i, 16 * j);
+                float kv[8], qv[8], gv[8], rv[8];
+                unpack8(ld_shared_v4(sm + ck), fk_s[i], kv);
+                unpack8(ld_shared_v4(sm + ck + 8192), fq_s[i], qv);
+                load8(g_s + i * K + d0, gv);
+                load8(r_s + d0, rv);
                 float kp[8], qp[8], km[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float gr = g_s[i * K + d0 + e] - r_s[d0 + e];
-                    const float up = __expf(gr), dn = __expf(-gr);
+                    const float x = gv[e] - rv[e];
+                    const float up = __expf(x), dn = __expf(-x);
                     kp[e] = kv[e] * up;
                     qp[e] = qv[e] * up;
                     km[e] = kv[e] * dn;
                 }
-                st_bf16x8(sm + Lay::kOpA + kb * 16384 + sw128(i, 16 * j), kp);
-                st_bf16x8(sm + Lay::kOpA + kb * 16384 + 8192 + sw128(i, 16 * j), qp);
-                st_bf16x8(sm + Lay::kOpB + cell, km);
+                st_bf16x8(sm + ck, kp);
+                st_bf16x8(sm + ck + 8192, qp);
+                st_bf16x8(sm + Lay::kM + kb * 8192 + sw128(i, 16 * j), km);
             }
-            st_bf16x8(sm + Lay::kKe + cell, ke);
-            st_bf16x8(sm + qh_off + cell, qhat);
-            st_bf16x8(sm + kh_off + cell, kh);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after_sync();
-            if (fz) {
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
                 // [G; S] = [kp; qp] km^T
+                tc_fence_after_sync();
                 const uint32_t id = idesc_bf16(128, 64, false, false);
-                const TileDesc da(smem_u32(sm + Lay::kOpA), 16, 1024), db(smem_u32(sm + Lay::kOpB), 16, 1024);
+                const TileDesc da(smem_u32(sm + Lay::kKQ), 16, 1024), db(smem_u32(sm + Lay::kM), 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
                     mma_bf16(tmem + kPrepColG, da.at((ks >> 2) * 16384 + (ks & 3) * 32),
                              db.at((ks >> 2) * 8192 + (ks & 3) * 32), id, ks > 0);
                 mma_commit(bar_mma);
             }
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb) tma_store_4d(&tm_kh, sm + kh_off + kb * 8192, kb * 64, h, t0, b);
-            bulk_commit_group();
-        }
-        if (fz) {
             mma_wait();
             if (__syncthreads_or(fail)) break;
             // rows 0-63 of the accumulator (warps 0-1): G -> L; rows 64-127: S -> P
@@ -268,7 +268,8 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     float v[16];
                     tmem_ld16f(tmem + lane_off + kPrepColG + blk * 16, v);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) L_s[i * Lay::kLStride + blk * 16 + e] = (blk * 16 + e < i) ? bi * v[e] : 0.f;
+                    for (int e = 0; e < 16; ++e)
+                        L_s[i * Lay::kLStride + blk * 16 + e] = (blk * 16 + e < i) ? bi * v[e] : 0.f;
                 }
             } else {
 #pragma unroll
@@ -281,34 +282,48 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     st_bf16x8(sm + Lay::kAP + sw128(64 + i, blk * 32 + 16), v + 8);
                 }
             }
+            // MMA 1 has read kp and km: ke = kp exp(r) = k exp(g) and
+            // KH = km exp(r) = k exp(g_last - g), both in place
+            for (int it = tid; it < 64 * KB * 8; it += kKdaThreads) {
+                int ii, kb, j;
+                item(it, ii, kb, j);
+                const int d0 = kb * 64 + 8 * j;
+                float ev[8], x[8];
+                load8(er_s + d0, ev);
+                const uint32_t ck = Lay::kKQ + kb * 16384 + sw128(ii, 16 * j);
+                const uint32_t cm = Lay::kM + kb * 8192 + sw128(ii, 16 * j);
+                unpack8(ld_shared_v4(sm + ck), 1.f, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] *= ev[e];
+                st_bf16x8(sm + ck, x);
+                unpack8(ld_shared_v4(sm + cm), 1.f, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] *= ev[e];
+                st_bf16x8(sm + cm, x);
+            }
         } else {
             // one exponential per term (exponents <= 0 on the kept entries):
             // threads 0-63 row i of L, threads 64-127 row i of P
             const int i = tid & 63;
             const bool is_p = tid >= 64;
-            const uint32_t xbase = is_p ? Lay::kQ : Lay::kK;
             const float fi = is_p ? fq_s[i] * scale : fk_s[i] * b_s[i];
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.f;
 #pragma unroll 1
             for (int d = 0; d < K; ++d) {
-                const uint32_t col = (d >> 6) * 8192, byte = 2 * (d & 63);
-                const float xi = ld_bf16(sm + xbase + col + sw128(i, byte));
+                const uint32_t col = Lay::kKQ + (d >> 6) * 16384, byte = 2 * (d & 63);
+                const float xi = ld_bf16(sm + col + (is_p ? 8192 : 0) + sw128(i, byte));
                 const float gi = g_s[i * K + d];
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     const bool keep = is_p ? (j <= i) : (j < i);
-                    const float kj = ld_bf16(sm + Lay::kK + col + sw128(j, byte)) * fk_s[j];
+                    const float kj = ld_bf16(sm + col + sw128(j, byte)) * fk_s[j];
                     const float t = xi * kj * __expf(gi - g_s[j * K + d]);
                     acc[j] += keep ? t : 0.f;   // a dropped term may overflow; it is never used
                 }
             }
-            __syncthreads();   // every read of g done before L overwrites it
-            if (!is_p) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) L_s[i * Lay::kLStride + j] = fi * acc[j];
-            } else {
+            if (is_p) {
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     float v[8];
@@ -317,9 +332,45 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     st_bf16x8(sm + Lay::kAP + sw128(64 + i, ch * 16), v);
                 }
             }
+            __syncthreads();   // every read of the raw tiles done
+            // ke = k exp(g) and q_hat = scale q exp(g) in place, KH beside them
+            for (int it = tid; it < 64 * KB * 8; it += kKdaThreads) {
+                int ii, kb, j;
+                item(it, ii, kb, j);
+                const int d0 = kb * 64 + 8 * j;
+                const uint32_t ck = Lay::kKQ + kb * 16384 + sw128(ii, 16 * j);
+                float kv[8], qv[8], gv[8], rv[8];
+                unpack8(ld_shared_v4(sm + ck), fk_s[ii], kv);
+                unpack8(ld_shared_v4(sm + ck + 8192), fq_s[ii] * scale, qv);
+                load8(g_s + ii * K + d0, gv);
+                load8(r_s + d0, rv);
+                float kh[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float eg = __expf(gv[e]);
+                    kh[e] = kv[e] * __expf(2.f * rv[e] - gv[e]);
+                    kv[e] *= eg;
+                    qv[e] *= eg;
+                }
+                st_bf16x8(sm + ck, kv);
+                st_bf16x8(sm + ck + 8192, qv);
+                st_bf16x8(sm + Lay::kM + kb * 8192 + sw128(ii, 16 * j), kh);
+            }
+            __syncthreads();   // every read of g done before L overwrites it
+            if (!is_p) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) L_s[i * Lay::kLStride + j] = fi * acc[j];
+            }
         }
+        fence_proxy_async_smem();
         __syncthreads();
-        // ---- A = (I + L)^-1, column j per thread: (I + L) a = e_j top to bottom
+        if (tid == 0) {
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) tma_store_4d(&tm_kh, sm + Lay::kM + kb * 8192, kb * 64, h, t0, b);
+            bulk_commit_group();
+        }
+        // ---- A = (I + L)^-1, column j per thread: (I + L) a = e_j top to bottom,
+        // each row's sum in four interleaved partial sums
         if (tid < 64) {
             const int j = tid;
             float a[64];
@@ -327,18 +378,18 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 #pragma unroll
             for (int i = 1; i < 64; ++i) {
                 const float *Li = L_s + i * Lay::kLStride;
-                float s = i == j ? 1.f : 0.f;
+                float s0 = i == j ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                 for (int m = 0; m < (i & ~3); m += 4) {
                     const float4 l = *reinterpret_cast<const float4 *>(Li + m);
-                    s = fmaf(-l.x, a[m], s);
-                    s = fmaf(-l.y, a[m + 1], s);
-                    s = fmaf(-l.z, a[m + 2], s);
-                    s = fmaf(-l.w, a[m + 3], s);
+                    s0 = fmaf(-l.x, a[m], s0);
+                    s1 = fmaf(-l.y, a[m + 1], s1);
+                    s2 = fmaf(-l.z, a[m + 2], s2);
+                    s3 = fmaf(-l.w, a[m + 3], s3);
                 }
 #pragma unroll
-                for (int m = i & ~3; m < i; ++m) s = fmaf(-Li[m], a[m], s);
-                a[i] = s;
+                for (int m = i & ~3; m < i; ++m) s0 = fmaf(-Li[m], a[m], s0);
+                a[i] = (s0 + s1) + (s2 + s3);
             }
             // Ab = A diag(beta): column j, rows 0-63 of [Ab; P]
             const float bj = b_s[j];
@@ -372,21 +423,24 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        // ---- X1 out; [w; PA ke] = [Ab; PA] ke
+        // ---- X1 out; [w; PA ke] = [Ab; PA] ke (ke: rows 0-63 of each feature block)
         if (tid == 0) {
             tc_fence_after_sync();
             tma_store_4d(&tm_x1, sm + Lay::kAP, 0, h, t0, b);
             tma_store_4d(&tm_x1, sm + Lay::kAP + 8192, 64, h, t0, b);
             bulk_commit_group();
             const uint32_t id = idesc_bf16(128, K, false, true);
-            const TileDesc da(s_ap, 16, 1024), db(smem_u32(sm + Lay::kKe), 8192, 1024);
+            const TileDesc da(s_ap, 16, 1024), db(smem_u32(sm + Lay::kKQ), 16384, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kPrepColW, da.at(ks * 32), db.at(ks * 2048), id, ks > 0);
             mma_commit(bar_mma);
         }
         mma_wait();
+        if (tid == 0) bulk_wait_group_read0();   // KH's staging is read before -w replaces it
         if (__syncthreads_or(fail)) break;
         {
+            // -w (rows 0-63) and Q' = q_hat - PA ke (rows 64-127; q_hat = scale
+            // exp(r) qp with the factored operands)
             const int i = tid & 63;
 #pragma unroll 1
             for (int blk = 0; blk < K / 16; ++blk) {
@@ -395,22 +449,27 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 const int kb = blk >> 2;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const uint32_t cell = kb * 8192 + sw128(i, (blk & 3) * 32 + half * 16);
+                    const uint32_t byte = (blk & 3) * 32 + half * 16;
                     float x[8];
                     if (tid < 64) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x[e] = -v[half * 8 + e];
-                        st_bf16x8(sm + Lay::kOpB + cell, x);
+                        st_bf16x8(sm + Lay::kM + kb * 8192 + sw128(i, byte), x);
                     } else {
-                        const uint4 u = ld_shared_v4(sm + qh_off + cell);
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                        const uint32_t cq = Lay::kKQ + kb * 16384 + 8192 + sw128(i, byte);
+                        float qf[8];
+                        if (fz) {
+                            load8(er_s + blk * 16 + half * 8, qf);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 p = unpack_bf16(w4[e]);
-                            x[2 * e] = p.x - v[half * 8 + 2 * e];
-                            x[2 * e + 1] = p.y - v[half * 8 + 2 * e + 1];
+                            for (int e = 0; e < 8; ++e) qf[e] *= scale;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) qf[e] = 1.f;
                         }
-                        st_bf16x8(sm + qh_off + cell, x);
+                        unpack8(ld_shared_v4(sm + cq), 1.f, x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = fmaf(qf[e], x[e], -v[half * 8 + e]);
+                        st_bf16x8(sm + cq, x);
                     }
                 }
             }
@@ -420,8 +479,8 @@ gdn_kda_prep_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (tid == 0) {
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
-                tma_store_4d(&tm_x2, sm + Lay::kOpB + kb * 8192, kb * 64, h, t0, b);
-                tma_store_4d(&tm_x2, sm + qh_off + kb * 8192, K + kb * 64, h, t0, b);
+                tma_store_4d(&tm_x2, sm + Lay::kM + kb * 8192, kb * 64, h, t0, b);
+                tma_store_4d(&tm_x2, sm + Lay::kKQ + kb * 16384 + 8192, K + kb * 64, h, t0, b);
             }
             bulk_commit_group();
         }
