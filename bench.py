@@ -454,8 +454,9 @@ def bench_output_norm(args, w, world, dev, flush, d):
 
 def bench_per_channel(args, w, world, dev, flush):
     """Per-channel (KDA) decay: the chunked step on the same shape (one decay per
-    key channel, CUDA-core pipeline) and the decode step on the decode workload
-    with a per-channel gamma [B,T,H,K]."""
+    key channel; 'auto' runs bf16 on the tensor-core form, the CUDA-core
+    pipeline timed beside it) and the decode step on the decode workload with a
+    per-channel gamma [B,T,H,K]."""
     from gated_delta_rule_35_gb300 import chunk_fwd, decode_step, native
 
     x = make_inputs(w.B, w.T, w.H, w.K, w.V, dtype=w.dtype, seed=w.seed, h0_std=w.h0_std,
@@ -486,6 +487,14 @@ def bench_per_channel(args, w, world, dev, flush):
     t_chunk = timed(lambda: chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"],
                                       workspace=ws, stream=stream, per_channel_decay=True),
                     max(5, min(args.steps, 20)), True)
+    t_simt = timed(lambda: chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="simt",
+                                     workspace=ws, stream=stream, per_channel_decay=True),
+                   5, True)
+    # algorithmic bytes: q, k, v in, o out, g (fp32 per channel) and beta in,
+    # h0 in and h_final out
+    es_c = DSIZE[w.dtype]
+    chunk_bytes = (w.B * w.T * w.H * ((2 * w.K + 2 * w.V) * es_c + 4 * w.K + 4)
+                   + w.B * w.H * w.K * w.V * 4 * (2 if w.h0_std else 1))
     wd = DECODE_WORKLOADS[DECODE_WORKLOAD]
     y = make_inputs(wd.B, wd.T, wd.H, wd.K, wd.V, dtype=wd.dtype, seed=wd.seed, h0_std=wd.h0_std,
                     chunk=1, per_channel=True)
@@ -499,7 +508,12 @@ def bench_per_channel(args, w, world, dev, flush):
     nbytes = heads * wd.K * wd.V * 8 + heads * wd.T * ((2 * wd.K + 2 * wd.V) * es + 4 * wd.K + 4)
     peaks = load_peaks()
     return {"chunked": {"workload": w.name + "_per_channel", "ms_per_step": 1e3 * t_chunk,
-                        "tokens_per_s": w.B * w.T * world / t_chunk, "kernels": native.launches(p)},
+                        "tokens_per_s": w.B * w.T * world / t_chunk, "kernels": native.launches(p),
+                        "cuda_core_ms_per_step": 1e3 * t_simt,
+                        "algorithmic_bytes_per_step": chunk_bytes,
+                        "pipeline_roofline": {"bound": "hbm", "achieved": chunk_bytes / t_chunk / 1e9,
+                                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                              "frac": chunk_bytes / t_chunk / 1e9 / peaks["hbm_gbs"]}},
             "decode": {"workload": wd.name + "_per_channel", "ms_per_call": 1e3 * t_dec,
                        "algorithmic_bytes_per_call": nbytes,
                        "roofline": {"bound": "hbm", "achieved": nbytes / t_dec / 1e9,
