@@ -72,7 +72,7 @@ struct TcLayout {
     static constexpr uint32_t kVG = kVN + 8192;                  // v_g
     static constexpr uint32_t kG = kVG + 8192;                   // decay tables, 4 chunk slots
     static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
-    // output stage: row sums of squares, [2 chunk slots][4 ranks x 2 halves][64 rows]
+    // output stage: row sums of squares, [2 chunk slots][4 ranks][64 rows]
     static constexpr uint32_t kRed = kBar + 256;
     static constexpr uint32_t kBytes = kRed + 2 * 8 * 64 * 4;
 };
@@ -137,6 +137,8 @@ struct Bars {
     uint64_t xo_ready, vn_ready, hs_ready;          // chain group
     uint64_t drain;                                 // every MMA issued is done
     uint64_t norm_bar[2];                           // output stage: row sums of the cluster
+    uint64_t o_done2[2];                            // output stage: PV of chunk slot c % 2 done
+    uint64_t o_free[2];                             // output stage: O of chunk slot c % 2 read
     // single-kernel form
     uint64_t a_ready;                               // WY group: A tiles of the next chunk
     uint64_t wu_done;                               // W and U of a chunk are done (A tiles free)
@@ -144,6 +146,7 @@ struct Bars {
     uint64_t wy_tab[4];                             // WY group: tables of chunk slot c % 4
     uint32_t abort, tmem;
 };
+static_assert(sizeof(Bars) <= 256, "the barrier block has 256 bytes in both layouts");
 
 // Named barrier 1 over the WY group's four warps (128 threads), and the same
 // barrier reducing a predicate with OR over them.
@@ -157,6 +160,16 @@ __device__ __forceinline__ bool wy_any(bool x) {
         : "r"(static_cast<uint32_t>(x))
         : "memory");
     return r != 0;
+}
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh: one special-function
+// instruction instead of an exponential and a reciprocal. Those units are shared
+// with the chain warps of the same sub-partitions, and with two per element they
+// set the output stage's pace. Absolute error below 3e-4, far inside the bf16
+// rounding of o.
+__device__ __forceinline__ float sigmoid_tanh(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
 }
 // GATED: the output stage (gated RMSNorm over V) with the V tiles of a head as
 // one cluster of nrank_arg CTAs; without it the cluster code is compiled out.
@@ -180,7 +193,8 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     using FLay = FaLayout<K>;
     using Tl = Tiles<K, FA>;
     constexpr int kThreads = tc_threads<FA>();
-    constexpr int kPrepThreads = prep_threads<FA>();
+    // with the output stage, the prep group's warps 4-5 run it instead
+    constexpr int kPrepThreads = GATED ? 64 : prep_threads<FA>();
     const int nrank = GATED ? nrank_arg : 0;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -237,7 +251,11 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // output stage: one local arrival (with the expected bytes) per chunk;
         // the row sums of every CTA of the cluster arrive as transactions
         if (nrank)
-            for (int i = 0; i < 2; ++i) mbar_init(&bs->norm_bar[i], 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&bs->norm_bar[i], 1);
+                mbar_init(&bs->o_done2[i], 1);
+                mbar_init(&bs->o_free[i], 64);
+            }
         if (FA) {
             mbar_init(&bs->a_ready, kWyThreads);
             mbar_init(&bs->wu_done, 1);
@@ -301,6 +319,7 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) mma_bf16_k<true>(tmem + ocol, da.at(ks * 32), db.at(ks * 2048), idPV);
                 mma_commit(&bs->o_done);
+                if (GATED) mma_commit(&bs->o_done2[cp & 1]);
             };
             // single-kernel form: chunk c's A tiles are in (WY group) once a_ready
             // completes its phase c
@@ -427,6 +446,84 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // (after an abort the last loads may have no consumer)
             for (int c = max(stall ? 1 : 0, issued - 2); c < issued; ++c)
                 mbar_wait(&bs->full[c & 1], (c >> 1) & 1, kWaitNs);
+        }
+    } else if (GATED && (warp == 4 || warp == 5)) {
+        // ================================================================ output stage
+        // Gated RMSNorm over the head's V columns, off the chunk chain. Warps
+        // 4-5 sit on TMEM lane quarters 0-1, where O lives: one token row per
+        // thread, all 64 of this CTA's columns. Per chunk c:
+        //  - load the row's gate (in flight while O(c) is produced);
+        //  - once PV(c) is done, send the row's sum of squares to every CTA of
+        //    the cluster (slot c % 2, entry = rank) as asynchronous stores that
+        //    complete bytes of the receiver's norm_bar;
+        //  - with every sum in, normalise, gate and store the row, and hand
+        //    O(c)'s columns back (o_free) for the O seed of chunk c + 2.
+        // A slot is next written for chunk c + 2. That send follows the
+        // sender's own finish of chunk c + 1, which waits for this CTA's sums
+        // of chunk c + 1, which are sent only after this CTA has read its slot
+        // for chunk c: neither the sums nor the barrier phase can be overtaken.
+        const int orow = tid - 128;
+        const uint32_t olane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float *wv = norm_w + vt * kTcBV;
+        for (int c = 0; c < NT; ++c) {
+            const int slot = c & 1, t0 = c * 64;
+            const bool valid = orow < min(64, T - t0);
+            const int64_t oi = ((static_cast<int64_t>(b) * T + t0 + orow) * H + h) * V + vt * kTcBV;
+            uint4 zr[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                zr[i] = valid ? reinterpret_cast<const uint4 *>(gate + oi)[i] : make_uint4(0u, 0u, 0u, 0u);
+            // and the next chunk's row into L2
+            if (orow < min(64, T - t0 - 64)) prefetch_l2(gate + oi + static_cast<int64_t>(64) * H * V);
+            if (!warp_all(wait_bar(&bs->o_done2[slot], (c >> 1) & 1, abort, wlim))) break;
+            tc_fence_after_sync();
+            const uint32_t ob = slot ? kColO2 : kColO;
+            float ss = 0.f;
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + ob + olane + blk * 16, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+            const uint32_t red = s_base + Lay::kRed + ((slot * 4 + vt) * 64 + orow) * 4;
+            const uint32_t nb = smem_u32(&bs->norm_bar[slot]);
+            // this CTA expects one sum per row from each CTA of the cluster
+            if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bs->norm_bar[slot], nrank * 64 * 4);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
+            if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (c >> 1) & 1, abort, wlim))) break;
+            const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 256;
+            float tot = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < nrank) tot += sums[r * 64 + orow];
+            const float rstd = rsqrtf(tot / V + norm_eps);
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16], y[16];
+                tmem_ld16f(tmem + ob + olane + blk * 16, v);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint4 z4 = zr[blk * 2 + i];
+                    const uint32_t w4[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = i * 8 + 2 * e;
+                        const float z0 = __uint_as_float(w4[e] << 16);
+                        const float z1 = __uint_as_float(w4[e] & 0xffff0000u);
+                        y[j] = v[j] * rstd * wv[blk * 16 + j] * sigmoid_tanh(z0);
+                        y[j + 1] = v[j + 1] * rstd * wv[blk * 16 + j + 1] * sigmoid_tanh(z1);
+                    }
+                }
+                if (valid) {
+                    store_bf16x8_global(o + oi + blk * 16, y);
+                    store_bf16x8_global(o + oi + blk * 16 + 8, y + 8);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bs->o_free[slot]);
         }
     } else if (FA ? (warp == 2 || warp == 3) : (warp >= 2 && warp < 6)) {
         // ================================================================ prep group
@@ -934,77 +1031,6 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tc_fence_before_sync();
         mbar_arrive(&bs->hs_ready);
         bool ok = true;
-        // Output stage (gated RMSNorm over the head's V columns), in two parts
-        // per chunk so that the cluster exchange overlaps the next chunk:
-        // part 1, after o_done(c), sends this thread's sum of squares over its
-        // 32 columns to every CTA of the cluster (slot c % 2, entry rank * 2 +
-        // half) and prefetches the gate; part 2, after the next chunk's O seed,
-        // waits for all sums, reads O(c) again and writes the output. A slot is
-        // next written for chunk c + 2, which needs every thread of the
-        // cluster to have arrived for chunk c + 1, i.e. to have finished part 2
-        // of chunk c: neither the sums nor the barrier phase can be overtaken.
-        // The sums travel as asynchronous stores that complete bytes of the
-        // receiving CTA's barrier, so the sender needs no memory fence.
-        auto gated_send = [&](int c) {
-            const uint32_t ob = (c & 1) ? kColO2 : kColO;
-            float v0[16], v1[16];
-            tmem_ld16f(tmem + ob + lane_off + col0, v0);
-            tmem_ld16f(tmem + ob + lane_off + col0 + 16, v1);
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ss = fmaf(v0[e], v0[e], fmaf(v1[e], v1[e], ss));
-            const int tc0 = c * 64;
-            if (row < min(64, T - tc0))
-                prefetch_l2(gate + ((static_cast<int64_t>(b) * T + tc0 + row) * H + h) * V +
-                            vt * kTcBV + col0);
-            const int slot = c & 1;
-            const uint32_t red = s_base + Lay::kRed + ((slot * 8 + vt * 2 + hf) * 64 + row) * 4;
-            const uint32_t nb = smem_u32(&bs->norm_bar[slot]);
-            // this CTA expects one sum from each of the cluster's o-epilogue threads
-            if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&bs->norm_bar[slot], nrank * 128 * 4);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
-        };
-        auto gated_finish = [&](int c) -> bool {
-            const int slot = c & 1;
-            if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (c >> 1) & 1, abort, wlim))) return false;
-            const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 512;
-            float tot = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < 2 * nrank) tot += sums[i * 64 + row];
-            const float rstd = rsqrtf(tot / V + norm_eps);
-            const uint32_t ob = (c & 1) ? kColO2 : kColO;
-            float v0[16], v1[16];
-            tmem_ld16f(tmem + ob + lane_off + col0, v0);
-            tmem_ld16f(tmem + ob + lane_off + col0 + 16, v1);
-            const int tc0 = c * 64;
-            if (row < min(64, T - tc0)) {
-                const int64_t oi = ((static_cast<int64_t>(b) * T + tc0 + row) * H + h) * V +
-                                   vt * kTcBV + col0;
-                const float *wv = norm_w + vt * kTcBV + col0;
-                float y[32];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 zr = reinterpret_cast<const uint4 *>(gate + oi)[i];
-                    const uint32_t w4[4] = {zr.x, zr.y, zr.z, zr.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = i * 8 + 2 * e;
-                        const float z0 = __uint_as_float(w4[e] << 16);
-                        const float z1 = __uint_as_float(w4[e] & 0xffff0000u);
-                        const float o0 = j < 16 ? v0[j] : v1[j - 16];
-                        const float o1 = j + 1 < 16 ? v0[j + 1] : v1[j - 15];
-                        y[j] = o0 * rstd * wv[j] * __fdividef(1.f, 1.f + __expf(-z0));
-                        y[j + 1] = o1 * rstd * wv[j + 1] * __fdividef(1.f, 1.f + __expf(-z1));
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) store_bf16x8_global(o + oi + i * 8, y + i * 8);
-            }
-            return true;
-        };
         float g_last_next = (!FA && NT > 1) ? g_last_of(1) : 0.f;
         for (int c = 0; c < NT; ++c) {
             const int t0 = c * 64, n = min(64, T - t0), gs = c & 3;
@@ -1055,6 +1081,11 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tmem_st16(tmem + kColQK + lane_off + col0, z);
                     tmem_st16(tmem + kColQK + lane_off + col0 + 16, z);
                 }
+                // with the output stage, O(c - 2) (same columns) must have been read
+                if (GATED && c >= 2 &&
+                    !(ok = warp_all(wait_bar(&bs->o_free[c & 1], ((c >> 1) + 1) & 1, abort, wlim))))
+                    break;
+                tc_fence_after_sync();
                 const float so = scale * eg_s[gs * 64 + row];
                 const uint32_t ocol = (GATED && (c & 1)) ? kColO2 : kColO;
 #pragma unroll 1
@@ -1070,8 +1101,6 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&bs->xo_ready);
-                // previous chunk's output stage, part 2, while this chunk's MMAs run
-                if (GATED && c >= 1 && !(ok = gated_finish(c - 1))) break;
             } else {
                 if (c >= 1 && !(ok = warp_all(wait_bar(&bs->o_done, (c - 1) & 1, abort, wlim)))) break;
                 const float gate = gate_s[gs * 64 + row];
@@ -1122,28 +1151,22 @@ gdn_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             tc_fence_before_sync();
             mbar_arrive(&bs->hs_ready);
-            if (upper) {
+            if (upper && !GATED) {
                 if (!(ok = warp_all(wait_bar(&bs->o_done, c & 1, abort, wlim)))) break;
                 tc_fence_after_sync();
                 const int64_t oi = ((static_cast<int64_t>(b) * T + t0 + row) * H + h) * V +
                                    vt * kTcBV + col0;
-                if (!nrank) {
 #pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        float v[16];
-                        tmem_ld16f(tmem + kColO + lane_off + col0 + half * 16, v);
-                        if (row < n) {
-                            store_bf16x8_global(o + oi + half * 16, v);
-                            store_bf16x8_global(o + oi + half * 16 + 8, v + 8);
-                        }
+                for (int half = 0; half < 2; ++half) {
+                    float v[16];
+                    tmem_ld16f(tmem + kColO + lane_off + col0 + half * 16, v);
+                    if (row < n) {
+                        store_bf16x8_global(o + oi + half * 16, v);
+                        store_bf16x8_global(o + oi + half * 16 + 8, v + 8);
                     }
-                } else {
-                    gated_send(c);   // output stage, part 1
                 }
             }
         }
-        // output stage, part 2 of the last chunk
-        if (GATED && upper && warp_all(ok)) ok = gated_finish(NT - 1);
         // final state straight from tensor memory
         if (warp_all(ok) && h_final) {
             tc_fence_after_sync();
