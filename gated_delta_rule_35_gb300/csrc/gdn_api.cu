@@ -67,7 +67,8 @@ size_t body_bytes(const gdn_problem *p, gdn_algo algo) {
     const size_t front = front_bytes(p);
     if (algo == GDN_ALGO_TC && per_channel(p)) {
         // with 'auto' also room for the CUDA-core pipeline, which serves a call
-        // with the output stage (the per-channel tensor-core form has none)
+        // asking for the stage exports (the per-channel tensor-core form has
+        // only A diag(beta))
         const size_t kda = kda_tc_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
         const size_t simt = simt_workspace_bytes(p->B, p->T, p->H, p->K, p->V);
         return front + ((p->algo == GDN_ALGO_AUTO && simt > kda) ? simt : kda);
@@ -93,10 +94,10 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         if (ptr && !aligned16(ptr)) return GDN_ERR_ALIGNMENT;
     gdn_algo algo = resolve_algo(p);
     const bool kda_tc = algo == GDN_ALGO_TC && per_channel(p);
-    // the per-channel tensor-core form has no output stage and exports only
-    // A diag(beta); with 'auto' such calls run on the CUDA-core pipeline, for
-    // which workspace_bytes reserved room
-    const bool simt_only = norm || (ex && (ex->A || ex->w || ex->u || ex->v_new || ex->h));
+    // the per-channel tensor-core form exports only A diag(beta); with 'auto'
+    // a call asking for more runs on the CUDA-core pipeline, for which
+    // workspace_bytes reserved room
+    const bool simt_only = ex && (ex->A || ex->w || ex->u || ex->v_new || ex->h);
     if (kda_tc && simt_only) {
         if (p->algo != GDN_ALGO_AUTO) return GDN_ERR_UNSUPPORTED;
         algo = GDN_ALGO_SIMT;

@@ -506,26 +506,43 @@ struct KdaFwdLayout {
     static constexpr uint32_t kHB = 2 * kStage;           // state, bf16, rows = features (K x 64)
     static constexpr uint32_t kVN = kHB + KB * 8192;      // v_new, bf16 (64 x 64)
     static constexpr uint32_t kO = kVN + 8192;            // o staging for the TMA store
+    // barriers: full[2], mma, ht, norm[2] (output stage), then the TMEM address
     static constexpr uint32_t kBar = kO + 8192;
-    static constexpr uint32_t kBytes = kBar + 64;
+    // output stage: row sums of squares, [2 chunk slots][4 ranks][64 rows]
+    static constexpr uint32_t kRed = kBar + 64;
+    static constexpr uint32_t kBytes = kRed;
+    static constexpr uint32_t kBytesGated = kRed + 2 * 4 * 64 * 4;
 };
 
 constexpr uint32_t kFwdColD = 0, kFwdColH = 64, kFwdTmemCols = 128;
 
-template <int K>
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh (one special-function
+// instruction; absolute error below 3e-4, far inside the bf16 rounding of o).
+__device__ __forceinline__ float kda_sigmoid(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
+}
+
+// GATED: the output stage (gated RMSNorm over the head's V columns), the V
+// tiles of a head running as one cluster of V / 64 CTAs that exchange each
+// row's sum of squares.
+template <int K, bool GATED>
 __global__ void __launch_bounds__(kKdaThreads, 1)
 gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_x2,
                       const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ dec,
                       const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V, int NT,
-                      uint32_t *status) {
+                      uint32_t *status, const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w,
+                      float norm_eps) {
     using Lay = KdaFwdLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::kBar);   // [2]
-    uint64_t *mma_bar = full + 2, *ht_bar = full + 3;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + 4);
+    uint64_t *mma_bar = full + 2, *ht_bar = full + 3, *norm_bar = full + 4;   // norm_bar[2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + 6);
+    const int nrank = GATED ? V / 64 : 0;
 
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -541,6 +558,12 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
         mbar_init(&full[1], 1);
         mbar_init(mma_bar, 1);
         mbar_init(ht_bar, 1);
+        // output stage: one local arrival (with the expected bytes) per chunk;
+        // the row sums of every CTA of the cluster arrive as transactions
+        if (GATED) {
+            mbar_init(&norm_bar[0], 1);
+            mbar_init(&norm_bar[1], 1);
+        }
         fence_mbar_init();
     }
     // the state: row d = tid of the K x 64 block of columns [64 vt, 64 vt + 64)
@@ -586,6 +609,8 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
+    // the cluster's barriers are initialised before any CTA sends to them
+    if (GATED) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -645,7 +670,7 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
                 st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32), v);
                 st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32 + 16), v + 8);
             }
-        } else {
+        } else if (!GATED) {
             // o row (token) tid - 64 -> staging; the previous chunk's store has
             // read it once its issuing thread has waited
             if (tid == 64) bulk_wait_group_read0();
@@ -656,6 +681,65 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
                 tmem_ld16f(tmem + lane_off + kFwdColD + blk * 16, v);
                 st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32), v);
                 st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32 + 16), v + 8);
+            }
+        } else {
+            // o row i = tid - 64 with the output stage: its sum of squares goes
+            // to every CTA of the cluster (slot c % 2, entry = rank) as
+            // asynchronous stores that complete bytes of the receiver's
+            // norm_bar; with every sum in, the row is normalised and gated. A
+            // slot is next written for chunk c + 2, after the sender has waited
+            // for this CTA's sums of chunk c + 1, which are sent only after
+            // this CTA has read its slot for chunk c.
+            const int i = tid - 64, slot = c & 1;
+            float ov[64];
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float v[16];
+                tmem_ld16f(tmem + lane_off + kFwdColD + blk * 16, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[blk * 16 + e] = v[e];
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) ss = fmaf(ov[e], ov[e], ss);
+            const uint32_t red = s_base + Lay::kRed + ((slot * 4 + vt) * 64 + i) * 4;
+            const uint32_t nb = smem_u32(&norm_bar[slot]);
+            if (tid == 64) mbar_arrive_expect_tx(&norm_bar[slot], nrank * 64 * 4);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
+            bool got = mbar_try_wait_cluster(&norm_bar[slot], (c >> 1) & 1);
+            if (!got) {
+                const uint64_t tw = globaltimer_ns();
+                while (!(got = mbar_try_wait_cluster(&norm_bar[slot], (c >> 1) & 1)))
+                    if (globaltimer_ns() - tw > kKdaWaitNs) break;
+            }
+            fail |= !got;
+            const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 256;
+            float tot = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < nrank) tot += sums[r * 64 + i];
+            const float rstd = rsqrtf(tot / V + norm_eps);
+            const float *wv = norm_w + vt * 64;
+            const int t = c * 64 + i;
+            const uint4 *zrow = reinterpret_cast<const uint4 *>(
+                gate + ((static_cast<int64_t>(b) * T + min(t, T - 1)) * H + h) * V + vt * 64);
+            if (tid == 64) bulk_wait_group_read0();
+            bar_sync_warps23();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 z4 = zrow[q];
+                const uint32_t w4[4] = {z4.x, z4.y, z4.z, z4.w};
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 z = unpack_bf16(w4[e]);
+                    const int j = q * 8 + 2 * e;
+                    y[2 * e] = ov[j] * rstd * wv[j] * kda_sigmoid(z.x);
+                    y[2 * e + 1] = ov[j + 1] * rstd * wv[j + 1] * kda_sigmoid(z.y);
+                }
+                st_bf16x8(sm + Lay::kO + sw128(i, q * 16), y);
             }
         }
         fence_proxy_async_smem();
@@ -704,9 +788,11 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
             *reinterpret_cast<float4 *>(h_final + srow + e) = make_float4(hr[e], hr[e + 1], hr[e + 2], hr[e + 3]);
     }
     if (tid == 64) bulk_wait_group0();
-    if (tid == 0 && fail) atomicOr(status, 2u);
+    if (fail) atomicOr(status, 2u);
     tc_fence_before_sync();
     __syncthreads();
+    // no CTA of a cluster leaves while another may still write its shared memory
+    if (GATED) cluster_sync();
     if (warp == 0) tmem_dealloc(tmem, kFwdTmemCols);
 }
 
@@ -741,10 +827,13 @@ cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) 
         !make_tmap_bthx(&mo, a.o, a.V, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem_p = static_cast<int>(KdaPrepLayout<K>::kBytes + 1024);
-    const int smem_f = static_cast<int>(KdaFwdLayout<K>::kBytes + 1024);
+    const bool gated = a.gate != nullptr;
+    const auto fwd = gated ? gdn_kda_fwd_tc_kernel<K, true> : gdn_kda_fwd_tc_kernel<K, false>;
+    const int smem_f =
+        static_cast<int>((gated ? KdaFwdLayout<K>::kBytesGated : KdaFwdLayout<K>::kBytes) + 1024);
     cudaError_t e = cudaFuncSetAttribute(gdn_kda_prep_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_p);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gdn_kda_fwd_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f);
+    e = cudaFuncSetAttribute(fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f);
     if (e != cudaSuccess) return e;
     if ((e = m.mark(0, s)) != cudaSuccess) return e;
     gdn_kda_prep_tc_kernel<K><<<dim3(a.NT, a.H, a.B), kKdaThreads, smem_p, s>>>(
@@ -761,20 +850,31 @@ cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) 
     cfg.blockDim = dim3(kKdaThreads);
     cfg.dynamicSmemBytes = smem_f;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
     if (ctas > tc_sm_count()) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
     }
+    if (gated) {
+        // a head's V tiles form one cluster for the output stage's exchange
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = a.V / 64;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr++].val.clusterDim.z = 1;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
     const float *dec = w.dec;
     const float *h0 = a.h0;
     float *hf = a.h_final;
     int T = a.T, H = a.H, V = a.V, NT = a.NT;
     uint32_t *status = a.status;
-    void *args[] = {&mx1, &mx2, &mkh, &mv, &mo, &dec, &h0, &hf, &T, &H, &V, &NT, &status};
-    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(gdn_kda_fwd_tc_kernel<K>), args);
+    const __nv_bfloat16 *gate = static_cast<const __nv_bfloat16 *>(a.gate);
+    const float *norm_w = a.norm_w;
+    float norm_eps = a.norm_eps;
+    void *args[] = {&mx1, &mx2, &mkh, &mv, &mo, &dec, &h0, &hf, &T, &H, &V, &NT, &status, &gate, &norm_w, &norm_eps};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), args);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return m.mark(2, s);

@@ -110,10 +110,11 @@ typedef enum {
  *    bf16, on a tensor-core form of its own under GDN_ALGO_TC (a prep kernel
  *    per chunk building the decay-weighted WY and attention products, then
  *    the forward kernel over the chunks); GDN_ALGO_TC_SINGLE and
- *    GDN_ALGO_TC_WIDE give GDN_ERR_UNSUPPORTED. That form has no output stage
- *    and exports only A_beta: with GDN_ALGO_TC such calls give
- *    GDN_ERR_UNSUPPORTED, with GDN_ALGO_AUTO they run on the CUDA-core
- *    pipeline, and the workspace size for GDN_ALGO_AUTO covers both.
+ *    GDN_ALGO_TC_WIDE give GDN_ERR_UNSUPPORTED. That form runs the output
+ *    stage too, but of the stage exports it has only A_beta: with GDN_ALGO_TC
+ *    a call asking for the others gives GDN_ERR_UNSUPPORTED, with
+ *    GDN_ALGO_AUTO it runs on the CUDA-core pipeline, and the workspace size
+ *    for GDN_ALGO_AUTO covers both.
  * gdn_decode_step always takes raw gamma and accepts either g flag; it
  * honours GDN_FLAG_QK_L2NORM and GDN_FLAG_PER_CHANNEL_DECAY (gamma [B,T,H,K]). */
 enum {

@@ -163,6 +163,25 @@ def test_kda_tensor_core_a_export():
     assert np.all(a[:, T:] == 0)
 
 
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 256), (64, 192)])
+@pytest.mark.parametrize("T", [1, 65, 200])
+def test_kda_tensor_core_output_stage(K, V, T):
+    """The per-channel tensor-core form with the gated RMSNorm output stage
+    (a head's V tiles as one cluster), against the oracle's recurrence and
+    epilogue."""
+    B, H = 2, 3
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=950 + T + V, h0_std=0.1, per_channel=True)
+    gate, weight = make_output_norm(B, T, H, V, seed=950 + T + V)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 0.5, d["h0"], algo="tc", gate=gate.cuda(),
+                      norm_weight=weight.cuda(), per_channel_decay=True)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, 0.5)
+    o_ref = epilogue.gated_rmsnorm(o_ref, to_f64(gate), to_f64(weight), 1e-6)
+    assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"], rel(o.float().cpu().numpy(), o_ref)
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+
+
 def test_kda_tensor_core_limits():
     x = gpu(make_inputs(1, 64, 1, 64, 64, dtype="bf16", seed=74, per_channel=True))
     for algo in ("tc1", "tcw"):
@@ -170,10 +189,9 @@ def test_kda_tensor_core_limits():
             chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None, algo=algo,
                       per_channel_decay=True)
         assert e.value.status == native.GDN_ERR_UNSUPPORTED
-    gate, weight = make_output_norm(1, 64, 1, 64, seed=74)
     with pytest.raises(GdnError) as e:
-        chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None, algo="tc", gate=gate.cuda(),
-                  norm_weight=weight.cuda(), per_channel_decay=True)
+        chunk_fwd_stages(x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None, algo="tc",
+                         stages=("A", "w"), per_channel_decay=True)
     assert e.value.status == native.GDN_ERR_UNSUPPORTED
     p = native.problem(4, 2048, 16, 128, 128, torch.bfloat16, "auto",
                        native.flags_of(per_channel=True))

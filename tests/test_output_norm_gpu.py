@@ -76,6 +76,22 @@ def test_front_end_and_output_stage_together(algo):
     assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
 
 
+def test_output_norm_clusters_over_several_waves():
+    """Four-CTA clusters (V = 256), 160 CTAs on 152 SMs and 16 chunks with a
+    ragged last one: every slot of the output stage's hand-offs cycles eight
+    times, and some clusters start only as others finish."""
+    B, T, H, K, V = 2, 1000, 20, 128, 256
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=17, h0_std=0.1)
+    gate, weight = make_output_norm(B, T, H, V, seed=17)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 0.5, d["h0"], algo="tc", gate=gate.cuda(),
+                      norm_weight=weight.cuda(), norm_eps=EPS)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, gate, weight, scale=0.5)
+    assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+
+
 def test_output_norm_full_size_whole():
     """The default workload's shape with the output stage through 'auto' (the
     tensor-core path with two-CTA clusters), against the oracle over the whole
