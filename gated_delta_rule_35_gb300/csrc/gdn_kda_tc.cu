@@ -49,7 +49,6 @@ constexpr int kKdaThreads = 128;
 constexpr uint64_t kKdaWaitNs = 1000000000ull;
 constexpr float kFactorLimit = 160.f;   // |g_last| up to which the products are factored
 
-__device__ __forceinline__ void bar_sync_warps23() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 __device__ __forceinline__ void st_bf16(unsigned char *p, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
@@ -505,11 +504,11 @@ struct KdaFwdLayout {
     static constexpr uint32_t kStage = kV + 8192;
     static constexpr uint32_t kHB = 2 * kStage;           // state, bf16, rows = features (K x 64)
     static constexpr uint32_t kVN = kHB + KB * 8192;      // v_new, bf16 (64 x 64)
-    static constexpr uint32_t kO = kVN + 8192;            // o staging for the TMA store
-    // barriers: full[2], mma, ht, norm[2] (output stage), then the TMEM address
-    static constexpr uint32_t kBar = kO + 8192;
+    // barriers: full[2], mma, ht, norm[2] (output stage), vn_ready, o_taken,
+    // h_ready, drain; then the TMEM address and the abort flag
+    static constexpr uint32_t kBar = kVN + 8192;
     // output stage: row sums of squares, [2 chunk slots][4 ranks][64 rows]
-    static constexpr uint32_t kRed = kBar + 64;
+    static constexpr uint32_t kRed = kBar + 128;
     static constexpr uint32_t kBytes = kRed;
     static constexpr uint32_t kBytesGated = kRed + 2 * 4 * 64 * 4;
 };
@@ -531,7 +530,7 @@ template <int K, bool GATED>
 __global__ void __launch_bounds__(kKdaThreads, 1)
 gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_x2,
                       const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ dec,
+                      __nv_bfloat16 *__restrict__ o, const float *__restrict__ dec,
                       const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V, int NT,
                       uint32_t *status, const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w,
                       float norm_eps) {
@@ -541,7 +540,12 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::kBar);   // [2]
     uint64_t *mma_bar = full + 2, *ht_bar = full + 3, *norm_bar = full + 4;   // norm_bar[2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + 6);
+    // v_new rows in shared memory (warps 0-1), o rows out of the accumulator
+    // (warps 2-3), the state's bf16 copy written (its K rows)
+    uint64_t *vn_ready = full + 6, *o_taken = full + 7, *h_ready = full + 8;
+    uint64_t *drain = full + 9;   // every MMA issued is done (before TMEM is freed)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + 10);
+    volatile uint32_t *abort = tmem_slot + 1;
     const int nrank = GATED ? V / 64 : 0;
 
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -564,6 +568,11 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
             mbar_init(&norm_bar[0], 1);
             mbar_init(&norm_bar[1], 1);
         }
+        mbar_init(vn_ready, 64);
+        mbar_init(o_taken, 64);
+        mbar_init(h_ready, K);
+        mbar_init(drain, 1);
+        *abort = 0;
         fence_mbar_init();
     }
     // the state: row d = tid of the K x 64 block of columns [64 vt, 64 vt + 64)
@@ -602,9 +611,12 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
         }
         tma_load_4d(st + Lay::kV, &tm_v, &full[c & 1], vt * 64, h, t0, b);
     };
+    // thread 0: chunks whose loads were issued, and whose landing was waited for
+    int loaded = 0, landed = 0;
     if (tid == 0) {
         load_stage(0);
         if (NT > 1) load_stage(1);
+        loaded = NT > 1 ? 2 : 1;
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -639,28 +651,47 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tmem + kFwdColH, da.at(ks * 2048), db.at(ks * 2048), idHT, ks > 0);
     };
 
-    bool fail = false;   // thread 0: a load wait gave up (then no MMA is issued)
+    // The chunk loop runs on barrier hand-offs rather than block-wide
+    // barriers, so that the o rows (and the output stage) stay off the chain:
+    //   thread 0   h_ready(c) -> [Ab; PA] v (unless issued already) + [-w; Q'] h
+    //              -> commit mma; vn_ready(c) -> KH^T v_new -> commit ht;
+    //              o_taken(c) -> the next chunk's [Ab; PA] v
+    //   warps 0-1  mma(c) -> v_new rows to shared memory -> vn_ready
+    //   warps 2-3  mma(c) -> o rows into registers -> o_taken
+    //   rows < K   ht(c) -> state update -> bf16 copy -> h_ready(c + 1)
+    //   warps 2-3  then the o rows' output stage and store
+    // No waiter can fall two phases behind its barrier: each barrier's next
+    // phase needs, through this chain, the waiter's own earlier arrival. Every
+    // wait is bounded and gives up once any role has given up (abort flag).
+    const uint64_t lim = kKdaWaitNs;
+    if (d < K) {
+        // the entering state's copy (written above) for the first product
+        fence_proxy_async_smem();
+        mbar_arrive(h_ready);
+    }
+    bool ok = true;
     bool a_issued = false;
     for (int c = 0; c < NT; ++c) {
         const int s = c & 1;
         if (tid == 0) {
-            if (!fail && !a_issued) {
-                fail = !mbar_wait(&full[s], (c >> 1) & 1, kKdaWaitNs);
-                if (!fail) {
-                    tc_fence_after_sync();
-                    issue_a(s);
-                }
-            }
-            if (!fail) {
+            ok = wait_bar(h_ready, c & 1, abort, lim) &&
+                 (a_issued || wait_bar(&full[s], (c >> 1) & 1, abort, lim));
+            if (ok) landed = c + 1;
+            if (ok) {
                 tc_fence_after_sync();
+                if (!a_issued) issue_a(s);
                 issue_b(s);
+                mma_commit(mma_bar);
             }
-            mma_commit(mma_bar);   // arrives at once when nothing was issued
+            a_issued = false;
         }
         const float dv = d < K ? dec[((static_cast<int64_t>(b) * NT + c) * H + h) * K + d] : 0.f;
-        fail |= !mbar_wait(mma_bar, c & 1, kKdaWaitNs);
-        if (__syncthreads_or(fail)) break;
+        if (!warp_all(ok && wait_bar(mma_bar, c & 1, abort, lim))) {
+            ok = false;
+            break;
+        }
         tc_fence_after_sync();
+        float ov[64];   // warps 2-3: this thread's o row
         if (tid < 64) {
             // v_new row (token) tid -> the B operand of the state update
 #pragma unroll
@@ -670,28 +701,10 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
                 st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32), v);
                 st_bf16x8(sm + Lay::kVN + sw128(tid, blk * 32 + 16), v + 8);
             }
-        } else if (!GATED) {
-            // o row (token) tid - 64 -> staging; the previous chunk's store has
-            // read it once its issuing thread has waited
-            if (tid == 64) bulk_wait_group_read0();
-            bar_sync_warps23();
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                float v[16];
-                tmem_ld16f(tmem + lane_off + kFwdColD + blk * 16, v);
-                st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32), v);
-                st_bf16x8(sm + Lay::kO + sw128(tid - 64, blk * 32 + 16), v + 8);
-            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(vn_ready);
         } else {
-            // o row i = tid - 64 with the output stage: its sum of squares goes
-            // to every CTA of the cluster (slot c % 2, entry = rank) as
-            // asynchronous stores that complete bytes of the receiver's
-            // norm_bar; with every sum in, the row is normalised and gated. A
-            // slot is next written for chunk c + 2, after the sender has waited
-            // for this CTA's sums of chunk c + 1, which are sent only after
-            // this CTA has read its slot for chunk c.
-            const int i = tid - 64, slot = c & 1;
-            float ov[64];
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 float v[16];
@@ -699,76 +712,40 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
 #pragma unroll
                 for (int e = 0; e < 16; ++e) ov[blk * 16 + e] = v[e];
             }
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 64; ++e) ss = fmaf(ov[e], ov[e], ss);
-            const uint32_t red = s_base + Lay::kRed + ((slot * 4 + vt) * 64 + i) * 4;
-            const uint32_t nb = smem_u32(&norm_bar[slot]);
-            if (tid == 64) mbar_arrive_expect_tx(&norm_bar[slot], nrank * 64 * 4);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
-            bool got = mbar_try_wait_cluster(&norm_bar[slot], (c >> 1) & 1);
-            if (!got) {
-                const uint64_t tw = globaltimer_ns();
-                while (!(got = mbar_try_wait_cluster(&norm_bar[slot], (c >> 1) & 1)))
-                    if (globaltimer_ns() - tw > kKdaWaitNs) break;
-            }
-            fail |= !got;
-            const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 256;
-            float tot = 0.f;
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (r < nrank) tot += sums[r * 64 + i];
-            const float rstd = rsqrtf(tot / V + norm_eps);
-            const float *wv = norm_w + vt * 64;
-            const int t = c * 64 + i;
-            const uint4 *zrow = reinterpret_cast<const uint4 *>(
-                gate + ((static_cast<int64_t>(b) * T + min(t, T - 1)) * H + h) * V + vt * 64);
-            if (tid == 64) bulk_wait_group_read0();
-            bar_sync_warps23();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 z4 = zrow[q];
-                const uint32_t w4[4] = {z4.x, z4.y, z4.z, z4.w};
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 z = unpack_bf16(w4[e]);
-                    const int j = q * 8 + 2 * e;
-                    y[2 * e] = ov[j] * rstd * wv[j] * kda_sigmoid(z.x);
-                    y[2 * e + 1] = ov[j + 1] * rstd * wv[j + 1] * kda_sigmoid(z.y);
-                }
-                st_bf16x8(sm + Lay::kO + sw128(i, q * 16), y);
-            }
+            tc_fence_before_sync();
+            mbar_arrive(o_taken);
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        a_issued = false;
         if (tid == 0) {
-            tc_fence_after_sync();
-            issue_ht(s);
-            mma_commit(ht_bar);
-            // the next chunk's [Ab; PA] v behind it: the accumulator was read above
-            if (c + 1 < NT && !fail) {
-                fail = !mbar_wait(&full[s ^ 1], ((c + 1) >> 1) & 1, kKdaWaitNs);
-                if (!fail) {
+            ok = wait_bar(vn_ready, c & 1, abort, lim);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_ht(s);
+                mma_commit(ht_bar);
+            }
+            // the next chunk's [Ab; PA] v once this chunk's o rows are out of
+            // the accumulator
+            if (ok && c + 1 < NT) {
+                ok = wait_bar(o_taken, c & 1, abort, lim) &&
+                     wait_bar(&full[s ^ 1], ((c + 1) >> 1) & 1, abort, lim);
+                if (ok) landed = c + 2;
+                if (ok) {
                     tc_fence_after_sync();
                     issue_a(s ^ 1);
                     a_issued = true;
                 }
             }
         }
-        if (tid == 64) {
-            tma_store_4d(&tm_o, sm + Lay::kO, vt * 64, h, c * 64, b);
-            bulk_commit_group();
-        }
-        fail |= !mbar_wait(ht_bar, c & 1, kKdaWaitNs);
-        tc_fence_after_sync();
-        // the stage's last reader (the state update) is done
-        if (tid == 0 && !fail && c + 2 < NT) load_stage(c + 2);
         if (d < K) {
+            if (!warp_all(ok && wait_bar(ht_bar, c & 1, abort, lim))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            // the stage's last reader (the state update) is done
+            if (tid == 0 && c + 2 < NT) {
+                load_stage(c + 2);
+                loaded = c + 3;
+            }
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 float v[16];
@@ -776,19 +753,82 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
 #pragma unroll
                 for (int e = 0; e < 16; ++e) hr[blk * 16 + e] = fmaf(dv, hr[blk * 16 + e], v[e]);
             }
+            write_state();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(h_ready);
         }
-        write_state();
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (__syncthreads_or(fail)) break;
+        if (tid >= 64) {
+            const int i = tid - 64;
+            if (GATED) {
+                // Output stage: the row's sum of squares goes to every CTA of
+                // the cluster (slot c % 2, entry = rank) as asynchronous stores
+                // that complete bytes of the receiver's norm_bar; with every
+                // sum in, the row is normalised and gated. A slot is next
+                // written for chunk c + 2, after the sender has waited for this
+                // CTA's sums of chunk c + 1, which are sent only after this CTA
+                // has read its slot for chunk c.
+                const int slot = c & 1;
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) ss = fmaf(ov[e], ov[e], ss);
+                const uint32_t red = s_base + Lay::kRed + ((slot * 4 + vt) * 64 + i) * 4;
+                const uint32_t nb = smem_u32(&norm_bar[slot]);
+                if (tid == 64) mbar_arrive_expect_tx(&norm_bar[slot], nrank * 64 * 4);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (r < nrank) st_async_cluster_f32(mapa_shared(red, r), ss, mapa_shared(nb, r));
+                if (!warp_all(wait_bar_cluster(&norm_bar[slot], (c >> 1) & 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                const float *sums = reinterpret_cast<const float *>(sm + Lay::kRed) + slot * 256;
+                float tot = 0.f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (r < nrank) tot += sums[r * 64 + i];
+                const float rstd = rsqrtf(tot / V + norm_eps);
+                const float *wv = norm_w + vt * 64;
+                const int t = c * 64 + i;
+                const uint4 *zrow = reinterpret_cast<const uint4 *>(
+                    gate + ((static_cast<int64_t>(b) * T + min(t, T - 1)) * H + h) * V + vt * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 z4 = zrow[q];
+                    const uint32_t w4[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 z = unpack_bf16(w4[e]);
+                        const int j = q * 8 + 2 * e;
+                        ov[j] *= rstd * wv[j] * kda_sigmoid(z.x);
+                        ov[j + 1] *= rstd * wv[j + 1] * kda_sigmoid(z.y);
+                    }
+                }
+            }
+            // o row (token) i: the thread's own 128 bytes of the row
+            if (c * 64 + i < T) {
+                __nv_bfloat16 *dst = o + ((static_cast<int64_t>(b) * T + c * 64 + i) * H + h) * V + vt * 64;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) store_bf16x8_global(dst + q * 8, ov + q * 8);
+            }
+        }
     }
+    const bool fail = !ok || *abort;
     if (!fail && d < K) {
 #pragma unroll
         for (int e = 0; e < 64; e += 4)
             *reinterpret_cast<float4 *>(h_final + srow + e) = make_float4(hr[e], hr[e + 1], hr[e + 2], hr[e + 3]);
     }
-    if (tid == 64) bulk_wait_group0();
-    if (fail) atomicOr(status, 2u);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        if (!ok || *abort) atomicOr(status, 2u);
+        // after a failure: the loads still in flight land and every MMA issued
+        // completes (bounded) before the CTA's shared and tensor memory go
+        for (int k = landed; k < loaded; ++k) mbar_wait(&full[k & 1], (k >> 1) & 1, kKdaWaitNs);
+        mma_commit(drain);
+        mbar_wait(drain, 0, kKdaWaitNs);
+    }
     tc_fence_before_sync();
     __syncthreads();
     // no CTA of a cluster leaves while another may still write its shared memory
@@ -820,11 +860,10 @@ KdaWs kda_carve(void *ws, int B, int T, int H, int K) {
 template <int K>
 cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) {
     const KdaWs w = kda_carve(ws, a.B, a.T, a.H, K);
-    CUtensorMap mq, mk, mx1, mx2, mkh, mv, mo;
+    CUtensorMap mq, mk, mx1, mx2, mkh, mv;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mx1, w.x1, 128, a.H, a.T, a.B) || !make_tmap_bthx(&mx2, w.x2, 2 * K, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&mkh, w.kh, K, a.H, a.T, a.B) || !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) ||
-        !make_tmap_bthx(&mo, a.o, a.V, a.H, a.T, a.B))
+        !make_tmap_bthx(&mkh, w.kh, K, a.H, a.T, a.B) || !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem_p = static_cast<int>(KdaPrepLayout<K>::kBytes + 1024);
     const bool gated = a.gate != nullptr;
@@ -873,7 +912,8 @@ cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) 
     const __nv_bfloat16 *gate = static_cast<const __nv_bfloat16 *>(a.gate);
     const float *norm_w = a.norm_w;
     float norm_eps = a.norm_eps;
-    void *args[] = {&mx1, &mx2, &mkh, &mv, &mo, &dec, &h0, &hf, &T, &H, &V, &NT, &status, &gate, &norm_w, &norm_eps};
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
+    void *args[] = {&mx1, &mx2, &mkh, &mv, &o, &dec, &h0, &hf, &T, &H, &V, &NT, &status, &gate, &norm_w, &norm_eps};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), args);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
