@@ -533,7 +533,7 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
                       __nv_bfloat16 *__restrict__ o, const float *__restrict__ dec,
                       const float *__restrict__ h0, float *__restrict__ h_final, int T, int H, int V, int NT,
                       uint32_t *status, const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w,
-                      float norm_eps) {
+                      float norm_eps, uint64_t wlim, int stall) {
     using Lay = KdaFwdLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -612,9 +612,11 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
         tma_load_4d(st + Lay::kV, &tm_v, &full[c & 1], vt * 64, h, t0, b);
     };
     // thread 0: chunks whose loads were issued, and whose landing was waited for
-    int loaded = 0, landed = 0;
+    // (test hook: with `stall` chunk 0's loads are withheld, so the first wait
+    // on them runs out after wlim and every role leaves its loop)
+    int loaded = 0, landed = stall ? 1 : 0;
     if (tid == 0) {
-        load_stage(0);
+        if (!stall) load_stage(0);
         if (NT > 1) load_stage(1);
         loaded = NT > 1 ? 2 : 1;
     }
@@ -663,7 +665,7 @@ gdn_kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x1, const __grid_co
     // No waiter can fall two phases behind its barrier: each barrier's next
     // phase needs, through this chain, the waiter's own earlier arrival. Every
     // wait is bounded and gives up once any role has given up (abort flag).
-    const uint64_t lim = kKdaWaitNs;
+    const uint64_t lim = wlim;
     if (d < K) {
         // the entering state's copy (written above) for the first product
         fence_proxy_async_smem();
@@ -913,7 +915,14 @@ cudaError_t launch_kda(const Args &a, void *ws, cudaStream_t s, const Marks &m) 
     const float *norm_w = a.norm_w;
     float norm_eps = a.norm_eps;
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
-    void *args[] = {&mx1, &mx2, &mkh, &mv, &o, &dec, &h0, &hf, &T, &H, &V, &NT, &status, &gate, &norm_w, &norm_eps};
+    uint64_t wlim = kKdaWaitNs;
+    int stall = 0;
+    if (const uint64_t armed = take_armed_stall()) {
+        wlim = armed;
+        stall = 1;
+    }
+    void *args[] = {&mx1, &mx2, &mkh, &mv, &o,       &dec,  &h0,       &hf,   &T,     &H, &V,
+                    &NT,  &status, &gate, &norm_w, &norm_eps, &wlim, &stall};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), args);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

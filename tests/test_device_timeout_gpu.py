@@ -49,6 +49,40 @@ def test_withheld_loads_report_a_device_timeout_then_recover(algo):
     assert rel(hf.cpu().numpy(), hf_ref) < 2e-2
 
 
+@pytest.mark.parametrize("gated", [False, True])
+def test_per_channel_form_reports_a_device_timeout_then_recovers(gated):
+    """The per-channel tensor-core form's forward kernel: its first load
+    withheld, every role's bounded wait runs out (with the output stage, in
+    every CTA of each cluster), the status word records it, and the next call
+    on the same context is correct."""
+    from oracle import epilogue
+    from gated_delta_rule_35_gb300.inputs import make_output_norm
+    B, T, H, K, V = 2, 200, 3, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=89, h0_std=0.1, per_channel=True)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    kw = {}
+    if gated:
+        gate, weight = make_output_norm(B, T, H, V, seed=89)
+        kw = dict(gate=gate.cuda(), norm_weight=weight.cuda(), norm_eps=1e-6)
+    p = native.problem(B, T, H, K, V, torch.bfloat16, "tc", native.flags_of(per_channel=True))
+    ws = torch.zeros(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    native.debug_arm_stall(LIMIT_NS)
+    chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tc", workspace=ws,
+              per_channel_decay=True, **kw)
+    assert check_device_status(ws) == native.GDN_ERR_DEVICE_TIMEOUT
+    assert check_device_status(ws) == native.GDN_OK
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tc", workspace=ws,
+                      per_channel_decay=True, **kw)
+    torch.cuda.synchronize()
+    assert check_device_status(ws) == native.GDN_OK
+    o_ref, hf_ref = recurrence.forward(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), to_f64(x["g"]),
+                                       to_f64(x["beta"]), 1.0, to_f64(x["h0"]))
+    if gated:
+        o_ref = epilogue.gated_rmsnorm(o_ref, to_f64(gate), to_f64(weight), 1e-6)
+    assert rel(o.float().cpu().numpy(), o_ref) < 2e-2
+    assert rel(hf.cpu().numpy(), hf_ref) < 2e-2
+
+
 def test_host_entry_returns_a_device_timeout():
     x, _ = _inputs()
     hx = {n: (t.pin_memory() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
