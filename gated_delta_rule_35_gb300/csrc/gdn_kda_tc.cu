@@ -36,7 +36,9 @@
 //
 // gdn_kda_fwd_tc_kernel (one CTA per 64 V columns of a head) runs the chunk
 // loop: the fp32 state sits in registers, one K row per thread, and its bf16
-// copy in shared memory is the B operand of the next chunk's product.
+// copy in shared memory is the B operand of the next chunk's product. With
+// the gated RMSNorm output stage a head's V tiles run as one cluster that
+// exchanges each o row's sum of squares.
 #include "gdn_internal.h"
 #include "tc_sync.cuh"
 
