@@ -54,3 +54,22 @@ def test_step_statistics_and_roofline_arithmetic():
     nbytes = 1032 * units + w.B * w.H * w.K * w.V * 4
     assert r["bytes"] == nbytes and r["bound"] == "hbm"
     assert abs(r["frac"] - nbytes / 6800e9 / 2e-3) < 1e-12
+
+
+def test_dominant_kernel_of_a_split_forward():
+    """With the forward split over the wide and the 64-column kernel, the two
+    count as one launch; given the unmarked steps' total, the pair's time is
+    that total minus the other kernels' marked time when that is the smaller
+    (the marker between the pair removes their overlap)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    kernels = ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel", "gdn_fused_tc_kernel"]
+    name, t = bench.dominant(kernels, [6.0, 10.5, 2.4])
+    assert name == "gdn_wide_tc_kernel+gdn_fused_tc_kernel" and abs(t - 12.9) < 1e-12
+    name, t = bench.dominant(kernels, [6.0, 10.5, 2.4], 18.7)
+    assert abs(t - 12.7) < 1e-12
+    # never longer than the marked sum
+    assert abs(bench.dominant(kernels, [6.0, 10.5, 2.4], 20.0)[1] - 12.9) < 1e-12
+    # an unsplit step: the longest kernel, untouched by the total
+    assert bench.dominant(["gdn_wy_tc_kernel", "gdn_fused_tc_kernel"], [3.0, 7.0], 9.0) == ("gdn_fused_tc_kernel", 7.0)
