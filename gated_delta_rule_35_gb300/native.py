@@ -214,7 +214,8 @@ def chunk_fwd(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state:
     rows pass through the gated RMSNorm o * rsqrt(mean o^2 + norm_eps) *
     norm_weight * sigmoid(gate) before their rounding.
     ``per_channel_decay``: g is [B,T,H,K], one decay per key channel (the KDA
-    variant; CUDA-core pipeline)."""
+    variant; bf16 runs on its own tensor-core form, fp32 on the CUDA-core
+    pipeline)."""
     B, T, H, K, V = _check_inputs(q, k, v, g, beta, h0, per_channel_decay)
     norm = _output_norm(gate, norm_weight, norm_eps, (B, T, H, V), q)
     p = problem(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm, per_channel_decay))
