@@ -399,7 +399,7 @@ def _host_out(t, shape, dtype, name):
 
 def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_state: bool = True,
                    algo: str = "auto", device=None, raw_g: bool = False, qk_l2norm: bool = False,
-                   pieces: int = 0, out=None, final_state=None):
+                   pieces: int = 0, out=None, final_state=None, per_channel_decay: bool = False):
     """Host-tensor front end (gdn_chunk_fwd_host): host inputs in, host outputs
     out; returns when o (and h_final) are in host tensors. Pinned inputs let the
     library overlap the copies of one span of T (up to ``pieces`` 64-aligned
@@ -408,7 +408,8 @@ def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_s
     host tensors [B, T, H, V] / [B, H, K, V] fp32 to write into (pinned ones
     allocated when None). torch supplies the device buffer and the two side
     streams, both kept per device for later calls; a lock serialises callers,
-    and the work waits for what the caller's current stream has queued."""
+    and the work waits for what the caller's current stream has queued.
+    ``per_channel_decay``: g is [B,T,H,K] (as for chunk_fwd)."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     if dev.index is None:
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -421,7 +422,10 @@ def chunk_fwd_host(q, k, v, g, beta, scale: float = 1.0, h0=None, output_final_s
         raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
-    p, need = _host_plan(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm), pieces)
+    g_shape = (B, T, H, K) if per_channel_decay else (B, T, H)
+    if tuple(g.shape) != g_shape or tuple(beta.shape) != (B, T, H):
+        raise ValueError(f"g must be {g_shape} and beta {(B, T, H)}")
+    p, need = _host_plan(B, T, H, K, V, q.dtype, algo, flags_of(raw_g, qk_l2norm, per_channel_decay), pieces)
     ho = _host_out(out, (B, T, H, V), q.dtype, "out")
     hhf = _host_out(final_state, (B, H, K, V), torch.float32, "final_state") \
         if output_final_state else None

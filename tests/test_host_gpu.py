@@ -45,6 +45,26 @@ def test_host_entry_spans(algo, B, T, pieces):
     assert rel(hhf.numpy(), hf.cpu().numpy()) < 1e-3
 
 
+@pytest.mark.parametrize("algo", ["simt", "tc"])
+@pytest.mark.parametrize("pieces", [1, 4])
+def test_host_entry_per_channel_decay(algo, pieces):
+    """Per-channel decay through the host entry (g [B,T,H,K] cut into the same
+    spans): bit for bit with one span, within 1e-3 with several."""
+    x = make_inputs(2, 300, 3, 128, 128, dtype="bf16", seed=97, h0_std=0.1, per_channel=True)
+    h = pinned(x)
+    ho, hhf = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], 1.0, h["h0"], algo=algo,
+                             pieces=pieces, per_channel_decay=True)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo=algo,
+                      per_channel_decay=True)
+    torch.cuda.synchronize()
+    if pieces == 1:
+        assert torch.equal(ho, o.cpu()) and torch.equal(hhf, hf.cpu())
+    else:
+        assert rel(ho.float().numpy(), o.float().cpu().numpy()) < 1e-3
+        assert rel(hhf.numpy(), hf.cpu().numpy()) < 1e-3
+
+
 def test_host_entry_without_final_state_and_empty():
     x = pinned(make_inputs(2, 100, 2, 64, 64, dtype="bf16", seed=95))
     ho, hhf = chunk_fwd_host(x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, None,
