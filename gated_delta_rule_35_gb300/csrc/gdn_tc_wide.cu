@@ -656,7 +656,7 @@ int sm_count_of_device() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-        cudaGetLastError();   // no device visible: the machine's GB300 count
+        cudaGetLastError();   // no device visible: GB300's SM count
         return 152;
     }
     return sms;
