@@ -573,17 +573,27 @@ def step_stats(ms):
             "p10_ms": pick(0.1), "p90_ms": pick(0.9), "min_ms": xs[0], "max_ms": xs[-1]}
 
 
-def pipeline_roofline(w, t_step_s, peaks, has_h0):
-    """The whole step against max(flops / bf16 peak, compulsory bytes / HBM)."""
+def pipeline_roofline(w, t_step_s, peaks, has_h0, kernels=None):
+    """The whole step against max(flops / bf16 peak, compulsory bytes / HBM).
+    With the step's kernels: the DRAM bytes the design actually moves per step
+    (the committed ncu records of every kernel, when all are current), against
+    the compulsory bytes and as a rate against HBM."""
     units = w.B * w.T * w.H
     hbytes = (2 if has_h0 else 1) * w.B * w.H * w.K * w.V * 4
     F = flops_per_token_head(w.K, w.V) * units
     Bt = bytes_per_token_head(w.K, w.V, DSIZE[w.dtype]) * units + hbytes
     t_f, t_b = F / (peaks["bf16_tflops"] * 1e12), Bt / (peaks["hbm_gbs"] * 1e9)
     t_roof = max(t_f, t_b)
-    return {"t_roof_us": 1e6 * t_roof, "t_meas_us": 1e6 * t_step_s, "frac": t_roof / t_step_s,
-            "flops": F, "bytes": Bt, "bound": "hbm" if t_b >= t_f else "tensor",
-            "peak_source": peaks["_source"]}
+    out = {"t_roof_us": 1e6 * t_roof, "t_meas_us": 1e6 * t_step_s, "frac": t_roof / t_step_s,
+           "flops": F, "bytes": Bt, "bound": "hbm" if t_b >= t_f else "tensor",
+           "peak_source": peaks["_source"]}
+    if kernels:
+        parts = [ncu_traffic(k, w.name) for k in kernels]
+        moved = None if any(x is None for x in parts) else sum(parts)
+        out["design_traffic"] = moved
+        out["design_traffic_over_compulsory"] = None if moved is None else moved / Bt
+        out["design_traffic_frac_of_hbm"] = None if moved is None else moved / t_step_s / 1e9 / peaks["hbm_gbs"]
+    return out
 
 
 PAIR_TIMING = ("the 64-column grid runs beside the wide grid's last wave, which a marker between them "
@@ -715,7 +725,7 @@ def bench_other_workloads(args, main_w, dev, flush, peaks, world):
         out[name] = {
             "tokens_per_s": w.B * w.T * world / t_step, "ms_per_step": 1e3 * t_step,
             "timing": st,
-            "pipeline_roofline": pipeline_roofline(w, t_step, peaks, has_h0),
+            "pipeline_roofline": pipeline_roofline(w, t_step, peaks, has_h0, kernels),
             "roofline": kernel_roofline(dom_name, w, dom_t / len(step_ms) / 1e3, peaks, has_h0),
             "per_kernel_ms": {k: per_kernel[j] / len(step_ms) for j, k in enumerate(kernels)},
             "kernels": kernels, "gpu_launches": nk * len(step_ms),
@@ -757,7 +767,7 @@ def bench_ours(args, w, world, rank, local):
     roofline["share"] = dom_t / max(sum(per_kernel), 1e-12)
     if "+" in dom_name:
         roofline["kernel_ms_how"] = PAIR_TIMING
-    pipeline = pipeline_roofline(w, t_step, peaks, has_h0)
+    pipeline = pipeline_roofline(w, t_step, peaks, has_h0, kernels)
 
     # end to end through the public host-tensor API: H2D inputs, forward, D2H o and h_final
     hx = {n: (t_.pin_memory() if isinstance(t_, torch.Tensor) else t_) for n, t_ in x.items()}

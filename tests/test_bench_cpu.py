@@ -73,3 +73,26 @@ def test_dominant_kernel_of_a_split_forward():
     assert abs(bench.dominant(kernels, [6.0, 10.5, 2.4], 20.0)[1] - 12.9) < 1e-12
     # an unsplit step: the longest kernel, untouched by the total
     assert bench.dominant(["gdn_wy_tc_kernel", "gdn_fused_tc_kernel"], [3.0, 7.0], 9.0) == ("gdn_fused_tc_kernel", 7.0)
+
+
+def test_design_traffic_from_the_committed_records():
+    """The pipeline line adds the bytes the design moves per step (the ncu
+    records of every kernel of the step, when all are current) to the
+    compulsory bytes; a kernel without a current record leaves it null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from gated_delta_rule_35_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS["bf16_b8_h64_t8192_k128_v128"]
+    peaks = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "_source": "test"}
+    ks = ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel", "gdn_fused_tc_kernel"]
+    r = bench.pipeline_roofline(w, 2e-3, peaks, False, ks)
+    recs = [bench.ncu_traffic(k, w.name) for k in ks]
+    if any(x is None for x in recs):
+        assert r["design_traffic"] is None
+    else:
+        assert r["design_traffic"] == sum(recs)
+        assert abs(r["design_traffic_over_compulsory"] - sum(recs) / r["bytes"]) < 1e-12
+        assert abs(r["design_traffic_frac_of_hbm"] - sum(recs) / 2e-3 / 6800e9) < 1e-12
+    assert bench.pipeline_roofline(w, 2e-3, peaks, False, ["no_such_kernel"])["design_traffic"] is None
+    assert "design_traffic" not in bench.pipeline_roofline(w, 2e-3, peaks, False)
