@@ -76,3 +76,31 @@ def test_chunk_fwd_replays_from_a_graph(algo, gated):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o, o_e) and torch.equal(hf, hf_e)
+
+
+@pytest.mark.parametrize("shape,per_channel", [((1, 130, 160, 128, 128), False), ((2, 200, 3, 128, 128), True)])
+def test_split_forward_and_per_channel_form_replay_from_a_graph(shape, per_channel):
+    """The split forward (the wide kernel on a whole wave of heads, the
+    64-column kernel started right behind it for the rest: B1 H160 gives 152 +
+    8 heads on 152 SMs) and the per-channel tensor-core form, captured and
+    replayed: bit for bit the eager result."""
+    B, T, H, K, V = shape
+    x = gpu(make_inputs(B, T, H, K, V, dtype="bf16", seed=53, h0_std=0.1, per_channel=per_channel))
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, x["h0"])
+    kw = dict(algo="tc", per_channel_decay=per_channel)
+    p = native.problem(B, T, H, K, V, torch.bfloat16, "tc", native.flags_of(per_channel=per_channel))
+    o_e, hf_e = chunk_fwd(*args, **kw)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(o_e)
+    hf = torch.empty_like(hf_e)
+    chunk_fwd(*args, workspace=ws, out=o, final_state=hf, **kw)   # warm-up
+    torch.cuda.synchronize()
+    o.fill_(float("nan"))
+    hf.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chunk_fwd(*args, workspace=ws, out=o, final_state=hf, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(hf, hf_e)
+    assert native.check_device_status(ws) == native.GDN_OK
