@@ -107,7 +107,6 @@ gdn_status run(const gdn_problem *p, const void *q, const void *k, const void *v
         return GDN_ERR_UNSUPPORTED;
     // the single-kernel form keeps A on chip and has no output stage
     if (algo == GDN_ALGO_TC_SINGLE && (ex || norm)) return GDN_ERR_UNSUPPORTED;
-    if (algo == GDN_ALGO_TC_WIDE && norm) return GDN_ERR_UNSUPPORTED;   // the stage runs 64 columns per CTA
     if (ex && algo == GDN_ALGO_SIMT && ex->A_beta) return GDN_ERR_UNSUPPORTED;
     const size_t need = kStatusBytes + body_bytes(p, resolve_algo(p));
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;

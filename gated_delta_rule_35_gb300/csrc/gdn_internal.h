@@ -76,7 +76,11 @@ int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_na
 // The 128-column forward kernel (gdn_tc_wide.cu), reading A from abeta, for the
 // first `heads` of the B * H (b * H + h order); whether the two-kernel form picks
 // it for this shape; the device's SM count (152 when no device is visible).
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads);
+// With row_ss it also writes each o row's fp32 sum of squares over its 128
+// columns ([B, T, H, V / 128]) for wide_out_norm, the output stage that follows.
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads,
+                            float *row_ss = nullptr);
+cudaError_t wide_out_norm(const Args &a, const float *row_ss, cudaStream_t s);
 bool tc_wide(int B, int H, int V);
 int tc_sm_count();
 // WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.

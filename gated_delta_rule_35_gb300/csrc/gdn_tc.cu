@@ -1292,8 +1292,14 @@ bool tc_supported(int K, int V, gdn_dtype dtype) {
     return dtype == GDN_BF16 && (K == 64 || K == 128) && V % kTcBV == 0 && V >= kTcBV;
 }
 
-size_t tc_workspace_bytes(int B, int T, int H, int, int) {
+// A diag(beta) | A' (bf16 [B, T, H, 128]), then, where the 128-column kernel
+// may run, its rows' sums of squares for the output stage (fp32 [B, T, H, V / 128]).
+size_t tc_abeta_bytes(int B, int T, int H) {
     return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
+}
+size_t tc_workspace_bytes(int B, int T, int H, int, int V) {
+    const size_t ss = V % 128 == 0 ? align_up(static_cast<size_t>(B) * T * H * (V / 128) * sizeof(float)) : 0;
+    return tc_abeta_bytes(B, T, H) + ss;
 }
 
 // Heads of the two-kernel form's plain call that the wide kernel takes: all
@@ -1340,6 +1346,17 @@ cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, 
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
     const long long heads = static_cast<long long>(a.B) * a.H;
+    if (a.gate && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V))) {
+        // The output stage on a grid that takes the 128-column kernel: that
+        // kernel (every head) also writes each row's fp32 sum of squares, then
+        // the stage rewrites o in place. The 64-column kernel's cluster form
+        // of the stage cannot use the wide kernel and costs 1.8-1.9x there.
+        float *row_ss = reinterpret_cast<float *>(static_cast<char *>(ws) + tc_abeta_bytes(a.B, a.T, a.H));
+        if ((e = wide_tc_forward(a, ws, s, heads, row_ss)) != cudaSuccess) return e;
+        if ((e = m.mark(2, s)) != cudaSuccess) return e;
+        if ((e = wide_out_norm(a, row_ss, s)) != cudaSuccess) return e;
+        return m.mark(3, s);
+    }
     if (!a.gate && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V))) {
         // whole waves on the wide kernel, the last partial one on the 64-column one
         const long long wh = tc_wide_heads(form, a.B, a.H, a.V);

@@ -83,14 +83,16 @@ struct WideBars {
     uint32_t abort, tmem;
 };
 
-template <int K>
+// SS: with the output stage after it, also each o row's fp32 sum of squares
+// over the CTA's columns (row_ss); the plain instance has none of that code.
+template <int K, bool SS>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                    const float *__restrict__ g, const float *__restrict__ h0,
                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
                    float scale, uint32_t *status, int l2norm, const float *__restrict__ rk,
-                   uint64_t wlim, int stall) {
+                   uint64_t wlim, int stall, float *__restrict__ row_ss) {
     using Lay = WideLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -350,21 +352,30 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto write_o = [&](int cc) -> bool {
             if (!warp_all(wait_bar(&bs->o_done[cc & 1], (cc >> 1) & 1, abort, wlim))) return false;
             tc_fence_after_sync();
-            const int64_t oi = ((static_cast<int64_t>(b) * T + cc * 64 + wrow) * H + h) * V + vt * kWideBV;
+            const int64_t row = (static_cast<int64_t>(b) * T + cc * 64 + wrow) * H + h;
+            const int64_t oi = row * V + vt * kWideBV;
             const bool in = wrow < min(64, T - cc * 64);
+            // with the output stage: the row's sum of squares over these columns,
+            // before rounding (four partial sums; none without the stage)
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
             for (int bb = 0; bb < kWideBV / 32; ++bb) {
                 uint32_t r[32];
                 tmem_ld32(tmem + kCWO + lane_off + bb * 32, r);
                 tmem_wait_ld();
-                if (in) {
-                    float v[32];
+                float v[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+                if constexpr (SS) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ss[e & 3] = fmaf(v[e], v[e], ss[e & 3]);
+                }
+                if (in) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) store_bf16x8_global(o + oi + bb * 32 + q * 8, v + q * 8);
                 }
             }
+            if (SS && in) row_ss[row * nvt + vt] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
             const uint32_t z[16] = {};
 #pragma unroll
             for (int bb = 0; bb < kWideBV / 16; ++bb) tmem_st16(tmem + kCWO + lane_off + bb * 16, z);
@@ -663,13 +674,13 @@ int sm_count_of_device() {
 }
 
 template <int K>
-cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
+cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads, float *row_ss) {
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(WideLayout<K>::kBytes + 1024);
-    const auto kernel = gdn_wide_tc_kernel<K>;
+    const auto kernel = row_ss ? gdn_wide_tc_kernel<K, true> : gdn_wide_tc_kernel<K, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(a.V / kWideBV) * heads;
@@ -700,13 +711,63 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long l
         stall_arg = 1;
     }
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
-                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg};
+                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg, &row_ss};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// Gated RMSNorm of the rows written by the 128-column kernel: one warp per
+// (token, head) row, 8 columns per lane and step. The row's mean square comes
+// from the fp32 sums of squares that kernel took before rounding o (one per
+// 128-column tile); gate and weight apply to the rounded o, which is
+// rewritten in place.
+__device__ __forceinline__ float sigmoid_tanh_w(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
+}
+
+__global__ void __launch_bounds__(256)
+gdn_out_norm_kernel(__nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ gate,
+                    const float *__restrict__ w, const float *__restrict__ row_ss, long long rows, int V,
+                    float eps) {
+    const int lane = threadIdx.x & 31, nvt = V / kWideBV;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        float ss = 0.f;
+        for (int p = 0; p < nvt; ++p) ss += row_ss[r * nvt + p];
+        const float rstd = rsqrtf(ss / V + eps);
+        for (int j = lane; j < V / 8; j += 32) {
+            uint4 *op = reinterpret_cast<uint4 *>(o + r * V) + j;
+            const uint4 ov = *op, zv = reinterpret_cast<const uint4 *>(gate + r * V)[j];
+            const float4 w0 = reinterpret_cast<const float4 *>(w)[2 * j], w1 = reinterpret_cast<const float4 *>(w)[2 * j + 1];
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const uint32_t o4[4] = {ov.x, ov.y, ov.z, ov.w}, z4[4] = {zv.x, zv.y, zv.z, zv.w};
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = unpack_bf16(o4[e]), z = unpack_bf16(z4[e]);
+                y[2 * e] = a.x * rstd * wv[2 * e] * sigmoid_tanh_w(z.x);
+                y[2 * e + 1] = a.y * rstd * wv[2 * e + 1] * sigmoid_tanh_w(z.y);
+            }
+            *op = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t wide_out_norm(const Args &a, const float *row_ss, cudaStream_t s) {
+    const long long rows = static_cast<long long>(a.B) * a.T * a.H;
+    const long long blocks = (rows + 7) / 8;
+    const int grid = static_cast<int>(blocks < 16LL * sm_count_of_device() ? blocks : 16LL * sm_count_of_device());
+    gdn_out_norm_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(a.o),
+                                             static_cast<const __nv_bfloat16 *>(a.gate), a.norm_w, row_ss, rows,
+                                             a.V, a.norm_eps);
+    return cudaGetLastError();
+}
 
 bool tc_wide(int B, int H, int V) {
     // with 64-wide tiles the grid would need more than one wave of SMs; with
@@ -716,8 +777,8 @@ bool tc_wide(int B, int H, int V) {
 
 int tc_sm_count() { return sm_count_of_device(); }
 
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
-    return a.K == 128 ? launch_wide<128>(a, abeta, s, heads) : launch_wide<64>(a, abeta, s, heads);
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads, float *row_ss) {
+    return a.K == 128 ? launch_wide<128>(a, abeta, s, heads, row_ss) : launch_wide<64>(a, abeta, s, heads, row_ss);
 }
 
 }  // namespace gdn

@@ -311,7 +311,11 @@ GDN_API int32_t gdn_decode_step_launches(const gdn_problem *p, const char **name
  * the token's gate through a sigmoid). Each row o_t of one token and head
  * (V values) becomes
  *     o_t[v] * rsqrt(mean_u o_t[u]^2 + eps) * weight[v] * sigmoid(gate_t[v]),
- * formed from the fp32 o before its one rounding to the output dtype. */
+ * formed from the fp32 o before its one rounding to the output dtype. On the
+ * tensor-core path with the 128-column forward kernel (GDN_ALGO_TC_WIDE, or
+ * GDN_ALGO_TC / AUTO on grids that take it) the mean square still comes from
+ * the fp32 o, but weight and gate are applied by a second pass to the o that
+ * kernel rounded: one more rounding, at most one unit in the last place. */
 typedef struct {
     const void *gate;      /* [B,T,H,V] in p->dtype, required, 16-byte aligned */
     const float *weight;   /* [V] fp32, required, 16-byte aligned */

@@ -36,7 +36,7 @@ def oracle(x, gate, weight, scale=1.0, raw_g=False, l2norm=False, chunk=64):
     return epilogue.gated_rmsnorm(o, to_f64(gate), to_f64(weight), EPS), hf
 
 
-@pytest.mark.parametrize("algo", ["simt", "tc"])
+@pytest.mark.parametrize("algo", ["simt", "tc", "tcw"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 256), (64, 192)])
 @pytest.mark.parametrize("T", [1, 64, 65, 200])
@@ -90,6 +90,24 @@ def test_output_norm_clusters_over_several_waves():
     o_ref, hf_ref = oracle(x, gate, weight, scale=0.5)
     assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
     assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+
+
+def test_output_norm_on_the_wide_kernel_grid():
+    """A grid that takes the 128-column kernel (B3 H64: 384 64-column tiles on
+    152 SMs) with the output stage through 'auto': that kernel writes o and its
+    rows' fp32 sums of squares, then the stage rewrites o; against the oracle."""
+    B, T, H, K, V = 3, 200, 64, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=19, h0_std=0.1)
+    gate, weight = make_output_norm(B, T, H, V, seed=19)
+    d = gpu(x)
+    kw = dict(gate=gate.cuda(), norm_weight=weight.cuda(), norm_eps=EPS)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], **kw)
+    torch.cuda.synchronize()
+    o_ref, hf_ref = oracle(x, gate, weight)
+    assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
+    assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+    p = native.problem(B, T, H, K, V, torch.bfloat16, "tc")
+    assert native.launches(p)[1] == "gdn_wide_tc_kernel"
 
 
 def test_output_norm_full_size_whole():
