@@ -325,8 +325,10 @@ typedef struct {
 /* gdn_chunk_fwd with the optional output stage (norm == NULL: the plain o of
  * gdn_chunk_fwd) and optional timing markers as in gdn_chunk_fwd_profiled
  * (events == NULL: none). The tensor-core path runs the CTAs of one head's V
- * tiles as a thread-block cluster to share the row sums; every other contract
- * is gdn_chunk_fwd's. */
+ * tiles as a thread-block cluster to share the row sums, except on grids that
+ * take the 128-column kernel: there the stage is a second kernel after it (one
+ * more than gdn_chunk_fwd_launches counts; its marker is recorded when
+ * n_events allows). Every other contract is gdn_chunk_fwd's. */
 GDN_API gdn_status gdn_chunk_fwd_ex(const gdn_problem *p,
                                     const void *q, const void *k, const void *v,
                                     const float *g, const float *beta, float scale,
