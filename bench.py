@@ -19,9 +19,12 @@ workload (256 sequences x 16 heads, one token, K = V = 128, bf16) against the
 HBM roofline of reading and writing the fp32 state once (--no-decode skips it);
 "frontend": the same step on raw inputs with the chunk-local cumsum of g
 and the q/k L2 norm done in the kernels (--no-frontend skips it); and
-"output_norm": the same step with the gated RMSNorm output stage
-(--no-output-norm skips it); "per_channel": the chunked step and the decode
-step with per-channel (KDA) decay (--no-per-channel skips it).
+"output_norm": the same step with the gated RMSNorm output stage, and
+"output_norm_headline": the stage on the headline workload, each with its ratio
+to the plain step (--no-output-norm skips both); "per_channel": the chunked
+step and the decode step with per-channel (KDA) decay (--no-per-channel skips
+it). "pipeline_roofline.design_traffic" is the DRAM bytes the step's kernels
+move (the committed ncu records, where current), beside the compulsory bytes.
 """
 from __future__ import annotations
 
