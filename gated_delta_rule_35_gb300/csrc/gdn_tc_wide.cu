@@ -43,6 +43,10 @@ constexpr int kAuxThreads = 128, kChainWarps = 16;
 constexpr uint32_t kWideTmemCols = 512;
 // TMEM columns: BIG's accumulator [X | QK] or [QK | X] (192), HT (K), W / O (128).
 constexpr uint32_t kCBig = 0, kCHT = 192, kCWO = 320;
+// With the output stage in the kernel (V = 128): a lane's o row, rounded to
+// bf16 and packed in pairs, between its write and its normalisation.
+constexpr uint32_t kCStash = 448;
+static_assert(kCWO + kWideBV <= kCStash && kCStash + kWideBV / 2 <= kWideTmemCols, "the stash fits");
 
 // Shared-memory map (bytes from a 1024-aligned base); every tile is 64 rows of
 // 128 bytes (h^T: 128 rows) with the 128-byte swizzle, as TMA writes it.
@@ -60,7 +64,8 @@ struct WideLayout {
     static constexpr uint32_t kVG = kVN + 16384;          // v_g
     static constexpr uint32_t kG = kVG + 16384;           // decay tables, 4 chunk slots
     static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
-    static constexpr uint32_t kBytes = kBar + 256;
+    static constexpr uint32_t kNw = kBar + 256;           // output stage: norm weight (128 floats)
+    static constexpr uint32_t kBytes = kNw + kWideBV * 4;
     static_assert(kBytes + 1024 <= 232448, "fits the 227 KB of shared memory a CTA may use");
     // q / k tile of chunk parity p within a block; -w and h^T sit between them
     __host__ __device__ static constexpr uint32_t qslot(int p) { return p ? 16384 : 0; }
@@ -83,16 +88,33 @@ struct WideBars {
     uint32_t abort, tmem;
 };
 
-// SS: with the output stage after it, also each o row's fp32 sum of squares
-// over the CTA's columns (row_ss); the plain instance has none of that code.
-template <int K, bool SS>
+// Output stage (gated RMSNorm over V), by instance; the plain instance has
+// none of its code:
+//   kOsSums  each o row's fp32 sum of squares over the CTA's 128 columns goes to
+//            row_ss, for a second kernel (a row spans several CTAs);
+//   kOsNorm  V = 128, so a row lies in one thread's TMEM lane: the aux warp
+//            takes the row's sum of squares from the fp32 accumulator O(c),
+//            parks the row rounded to bf16 in spare TMEM columns and frees O;
+//            one chunk later, in the chunk whose W and O lie in the other lane
+//            half (its idle turn), it applies norm, weight and gate and stores
+//            o. The chain never waits for the stage's element work.
+constexpr int kOsNone = 0, kOsSums = 1, kOsNorm = 2;
+
+__device__ __forceinline__ float sigmoid_tanh_w(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
+}
+
+template <int K, int OS>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a,
                    const float *__restrict__ g, const float *__restrict__ h0,
                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
                    float scale, uint32_t *status, int l2norm, const float *__restrict__ rk,
-                   uint64_t wlim, int stall, float *__restrict__ row_ss) {
+                   uint64_t wlim, int stall, float *__restrict__ row_ss,
+                   const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w, float norm_eps) {
     using Lay = WideLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -119,6 +141,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                   "the zero tiles are every other tile of the row");
     for (int i = tid; i < 4 * 512; i += kWideThreads)
         st_shared_v4(sm + Lay::kZx + (i >> 9) * 16384 + (i & 511) * 16, 0u, 0u, 0u, 0u);
+    if (OS == kOsNorm && tid < kWideBV) reinterpret_cast<float *>(sm + Lay::kNw)[tid] = norm_w[tid];
     fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(&bs->tmem, kWideTmemCols);
@@ -348,6 +371,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int q4 = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int wrow = (q4 & 1) * 32 + lane;
+        // kOsNorm: the row's 1 / rms, kept from write_o(cc) to finish_o(cc)
+        float rstd_pend = 0.f;
         // o(cc) from O (these 32 lanes, all 128 columns), then the lanes cleared
         auto write_o = [&](int cc) -> bool {
             if (!warp_all(wait_bar(&bs->o_done[cc & 1], (cc >> 1) & 1, abort, wlim))) return false;
@@ -358,6 +383,12 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // with the output stage: the row's sum of squares over these columns,
             // before rounding (four partial sums; none without the stage)
             float ss[4] = {0.f, 0.f, 0.f, 0.f};
+            if (OS == kOsNorm && in) {
+                // the gate row (256 B) is read in this warp's next idle turn
+                const __nv_bfloat16 *zr = gate + row * V;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(zr));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(zr + 64));
+            }
 #pragma unroll 1
             for (int bb = 0; bb < kWideBV / 32; ++bb) {
                 uint32_t r[32];
@@ -366,16 +397,23 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 float v[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-                if constexpr (SS) {
+                if constexpr (OS != kOsNone) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ss[e & 3] = fmaf(v[e], v[e], ss[e & 3]);
                 }
-                if (in) {
+                if constexpr (OS == kOsNorm) {
+                    // the same rounding as the plain store
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                    tmem_st16(tmem + kCStash + lane_off + bb * 16, pk);
+                } else if (in) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) store_bf16x8_global(o + oi + bb * 32 + q * 8, v + q * 8);
                 }
             }
-            if (SS && in) row_ss[row * nvt + vt] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+            if (OS == kOsSums && in) row_ss[row * nvt + vt] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+            if (OS == kOsNorm) rstd_pend = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / V + norm_eps);
             const uint32_t z[16] = {};
 #pragma unroll
             for (int bb = 0; bb < kWideBV / 16; ++bb) tmem_st16(tmem + kCWO + lane_off + bb * 16, z);
@@ -383,6 +421,50 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before_sync();
             mbar_arrive(&bs->o_free);   // W(cc + 2) and PV(cc + 1) may rewrite these lanes
             return true;
+        };
+        // kOsNorm: o(cc) <- o * rstd * weight * sigmoid(gate) for this lane's row,
+        // 32 columns a step from the TMEM stash (the tcgen05.ld is warp-wide, so
+        // every lane takes part), with the gate's next 64 bytes loaded while the
+        // current ones are used.
+        auto finish_o = [&](int cc) {
+            const bool in = wrow < min(64, T - cc * 64);
+            const int64_t row = in ? (static_cast<int64_t>(b) * T + cc * 64 + wrow) * H + h : 0;
+            const uint4 *zp = reinterpret_cast<const uint4 *>(gate + row * V);
+            uint4 *op = reinterpret_cast<uint4 *>(o + row * V);
+            const float4 *nw4 = reinterpret_cast<const float4 *>(sm + Lay::kNw);
+            const float rs = rstd_pend;
+            uint4 zn[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) zn[q] = in ? __ldg(zp + q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+            for (int p = 0; p < kWideBV / 32; ++p) {
+                uint4 z[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) z[q] = zn[q];
+                if (p + 1 < kWideBV / 32) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) zn[q] = in ? __ldg(zp + 4 * (p + 1) + q) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint32_t pk[16];
+                tmem_ld16(tmem + kCStash + lane_off + p * 16, pk);
+                tmem_wait_ld();
+                if (!in) continue;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 w0 = nw4[8 * p + 2 * q], w1 = nw4[8 * p + 2 * q + 1];
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    const uint32_t z4[4] = {z[q].x, z[q].y, z[q].z, z[q].w};
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = unpack_bf16(pk[4 * q + e]), zz = unpack_bf16(z4[e]);
+                        y[2 * e] = a.x * rs * wv[2 * e] * sigmoid_tanh_w(zz.x);
+                        y[2 * e + 1] = a.y * rs * wv[2 * e + 1] * sigmoid_tanh_w(zz.y);
+                    }
+                    op[4 * p + q] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                                               pack_bf16(y[6], y[7]));
+                }
+            }
         };
         auto load_g = [&](int c) {
             const int t = c * 64 + ptid;
@@ -399,11 +481,15 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         };
         float g_next = load_g(0), gl_next = load_gl(0), rk_next = load_rk(0);
         bool ok = true;
+        int pend = -1;   // kOsNorm: the chunk whose rows wait for finish_o
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1, gs = c & 3;
             const int n = min(64, T - c * 64);
             const bool mine = (q4 >> 1) == (c & 1);   // W(c) and O(c) lie in these lanes
-            if (mine && c >= 2 && !(ok = write_o(c - 2))) break;
+            if (mine && c >= 2) {
+                if (!(ok = write_o(c - 2))) break;
+                if (OS == kOsNorm) pend = c - 2;
+            }
             const float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
             g_next = load_g(c + 1);
             gl_next = load_gl(c + 1);
@@ -450,7 +536,14 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (ptid == 0) fz_s[gs] = fzc;
             }
             mbar_arrive(&bs->g_ready[gs]);
-            if (!mine) continue;   // W(c) lies in the other lane half
+            if (!mine) {
+                // W(c) lies in the other lane half: this warp's idle turn
+                if (OS == kOsNorm && pend >= 0) {
+                    finish_o(pend);
+                    pend = -1;
+                }
+                continue;
+            }
             if (!(ok = warp_all(wait_bar(&bs->w_done[c & 1], (c >> 1) & 1, abort, wlim)))) break;
             tc_fence_after_sync();
 #pragma unroll 1
@@ -471,8 +564,12 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_arrive(&bs->w_ready[c & 1]);
         }
         // the last two chunks' o
+        if (OS == kOsNorm && ok && pend >= 0) finish_o(pend);
         for (int cc = max(0, NT - 2); ok && cc < NT; ++cc)
-            if ((q4 >> 1) == (cc & 1)) ok = write_o(cc);
+            if ((q4 >> 1) == (cc & 1)) {
+                ok = write_o(cc);
+                if (OS == kOsNorm && ok) finish_o(cc);
+            }
     } else {
         // ================================================================ chain group
         // Chunk c's q rows sit in lane half c % 2: the eight warps there turn QK
@@ -675,12 +772,17 @@ int sm_count_of_device() {
 
 template <int K>
 cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads, float *row_ss) {
+    // the output stage: in the kernel when a row is one CTA's, else row sums
+    const int os = !a.gate ? kOsNone : a.V == kWideBV ? kOsNorm : kOsSums;
+    if (os == kOsSums && !row_ss) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(WideLayout<K>::kBytes + 1024);
-    const auto kernel = row_ss ? gdn_wide_tc_kernel<K, true> : gdn_wide_tc_kernel<K, false>;
+    const auto kernel = os == kOsNorm   ? gdn_wide_tc_kernel<K, kOsNorm>
+                        : os == kOsSums ? gdn_wide_tc_kernel<K, kOsSums>
+                                        : gdn_wide_tc_kernel<K, kOsNone>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(a.V / kWideBV) * heads;
@@ -710,8 +812,13 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long l
         wlim_arg = armed;
         stall_arg = 1;
     }
+    float *ss_arg = os == kOsSums ? row_ss : nullptr;
+    const __nv_bfloat16 *gate_arg = static_cast<const __nv_bfloat16 *>(a.gate);
+    const float *nw_arg = a.norm_w;
+    float eps_arg = a.norm_eps;
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
-                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg, &row_ss};
+                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg, &ss_arg,
+                    &gate_arg, &nw_arg, &eps_arg};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -722,11 +829,6 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long l
 // from the fp32 sums of squares that kernel took before rounding o (one per
 // 128-column tile); gate and weight apply to the rounded o, which is
 // rewritten in place.
-__device__ __forceinline__ float sigmoid_tanh_w(float z) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
-    return fmaf(0.5f, t, 0.5f);
-}
 
 __global__ void __launch_bounds__(256)
 gdn_out_norm_kernel(__nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ gate,

@@ -94,20 +94,48 @@ def test_output_norm_clusters_over_several_waves():
 
 def test_output_norm_on_the_wide_kernel_grid():
     """A grid that takes the 128-column kernel (B3 H64: 384 64-column tiles on
-    152 SMs) with the output stage through 'auto': that kernel writes o and its
-    rows' fp32 sums of squares, then the stage rewrites o; against the oracle."""
+    152 SMs) with the output stage through 'auto': one whole wave of the wide
+    kernel (152 heads), which applies the stage itself one chunk behind its
+    o, and the other 40 heads on the 64-column kernel's cluster form; four
+    chunks, the last ragged. Against the oracle, and the wide heads bit for bit
+    against the wide-only form, which takes every head."""
     B, T, H, K, V = 3, 200, 64, 128, 128
     x = make_inputs(B, T, H, K, V, dtype="bf16", seed=19, h0_std=0.1)
     gate, weight = make_output_norm(B, T, H, V, seed=19)
     d = gpu(x)
     kw = dict(gate=gate.cuda(), norm_weight=weight.cuda(), norm_eps=EPS)
     o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], **kw)
+    ow, hw = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tcw", **kw)
     torch.cuda.synchronize()
     o_ref, hf_ref = oracle(x, gate, weight)
     assert rel(o.float().cpu().numpy(), o_ref) < TOL["bf16"]
     assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
+    assert rel(ow.float().cpu().numpy(), o_ref) < TOL["bf16"]
     p = native.problem(B, T, H, K, V, torch.bfloat16, "tc")
-    assert native.launches(p)[1] == "gdn_wide_tc_kernel"
+    assert native.launches(p) == ["gdn_wy_tc_kernel", "gdn_wide_tc_kernel", "gdn_fused_tc_kernel"]
+    # heads b * H + h < 152 are the wide kernel's in both calls
+    wide = torch.arange(B * H).reshape(B, H) < 152
+    assert torch.equal(o.permute(0, 2, 1, 3)[wide], ow.permute(0, 2, 1, 3)[wide])
+    assert torch.equal(hf[wide], hw[wide])
+
+
+def test_output_norm_headline_shape_whole():
+    """The headline shape (B8 H64 T8192) with the output stage through 'auto':
+    three whole waves of the 128-column kernel with the stage inside it, the
+    other 56 heads on the 64-column kernel's cluster form, 128 chunks each;
+    against the oracle over the whole of o and h_final."""
+    B, T, H, K, V = 8, 8192, 64, 128, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=3)
+    gate, weight = make_output_norm(B, T, H, V, seed=3)
+    d = gpu(x)
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None, gate=gate.cuda(),
+                      norm_weight=weight.cuda(), norm_eps=EPS)
+    torch.cuda.synchronize()
+    del d
+    eo, eh = whole_errors(x, o, hf, lambda sub: oracle(sub, sub["gate"], weight),
+                          extra={"gate": gate})
+    assert eo < TOL["bf16"], eo
+    assert eh < TOL["bf16"], eh
 
 
 def test_output_norm_full_size_whole():
