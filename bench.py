@@ -448,12 +448,7 @@ def bench_output_norm(args, w, world, dev, flush, d):
         b.record(stream)
     torch.cuda.synchronize(dev)
     t = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n / 1e3, world, dev)
-    kernels = native.launches(p)
-    if "gdn_wide_tc_kernel" in kernels and w.V > 128:
-        # a row over several 128-column CTAs: that kernel takes every head and
-        # the stage's second pass follows it (with V = 128 the kernels are the
-        # plain call's, the stage inside them)
-        kernels = [kernels[0], "gdn_wide_tc_kernel", "gdn_out_norm_kernel"]
+    kernels = native.launches(p)   # the plain call's kernels, the stage inside them
     return {"workload": w.name + "_gated_rmsnorm", "steps_timed": n, "ms_per_step": 1e3 * t,
             "tokens_per_s": w.B * w.T * world / t, "kernels": kernels,
             "gpu_launches": len(kernels) * n,

@@ -76,12 +76,9 @@ int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_na
 // The 128-column forward kernel (gdn_tc_wide.cu), reading A from abeta, for the
 // first `heads` of the B * H (b * H + h order); whether the two-kernel form picks
 // it for this shape; the device's SM count (152 when no device is visible).
-// With the output stage (a.gate) and V = 128 it applies the stage itself; with
-// V > 128 it writes each o row's fp32 sum of squares over its 128 columns to
-// row_ss ([B, T, H, V / 128]) for wide_out_norm, the second pass that follows.
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads,
-                            float *row_ss = nullptr);
-cudaError_t wide_out_norm(const Args &a, const float *row_ss, cudaStream_t s);
+// With the output stage (a.gate) it applies the stage itself (V = 256: the
+// head's two CTAs as a cluster).
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads);
 bool tc_wide(int B, int H, int V);
 int tc_sm_count();
 // WY kernel: A diag(beta) per chunk, bf16 [B, T, H, 64], into `abeta`.

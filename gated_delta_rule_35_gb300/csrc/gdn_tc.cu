@@ -1292,16 +1292,11 @@ bool tc_supported(int K, int V, gdn_dtype dtype) {
     return dtype == GDN_BF16 && (K == 64 || K == 128) && V % kTcBV == 0 && V >= kTcBV;
 }
 
-// A diag(beta) | A' (bf16 [B, T, H, 128]), then, where the 128-column kernel
-// may run with a row over several CTAs (V > 128), its rows' sums of squares for
-// the output stage's second pass (fp32 [B, T, H, V / 128]).
+// A diag(beta) | A' (bf16 [B, T, H, 128]).
 size_t tc_abeta_bytes(int B, int T, int H) {
     return align_up(static_cast<size_t>(B) * T * H * 128 * sizeof(__nv_bfloat16));
 }
-size_t tc_workspace_bytes(int B, int T, int H, int, int V) {
-    const size_t ss = V % 128 == 0 && V > 128 ? align_up(static_cast<size_t>(B) * T * H * (V / 128) * sizeof(float)) : 0;
-    return tc_abeta_bytes(B, T, H) + ss;
-}
+size_t tc_workspace_bytes(int B, int T, int H, int, int) { return tc_abeta_bytes(B, T, H); }
 
 // Heads of the two-kernel form's plain call that the wide kernel takes: all
 // of them, or (form kTwo) only whole waves of its CTAs when the rest fit one
@@ -1317,9 +1312,7 @@ long long tc_wide_heads(TcForm form, int B, int H, int V) {
     return (heads - wide_heads) * (V / 64) <= sms ? wide_heads : heads;
 }
 
-// Kernel names of the plain call. With the output stage they are the same for
-// V = 128; for V > 128 on the wide kernel its second pass
-// (gdn_out_norm_kernel) replaces the 64-column remainder.
+// Kernel names of the call, with or without the output stage.
 int tc_launches(TcForm form, int B, int H, int V, const char **names, int max_names) {
     if (form == TcForm::kSingle) {
         if (names && max_names > 0) names[0] = "gdn_fused_tc_kernel";
@@ -1348,23 +1341,10 @@ cudaError_t tc_forward(const Args &a, void *ws, cudaStream_t s, const Marks &m, 
     if ((e = wy_tc_forward(a, ws, s)) != cudaSuccess) return e;
     if ((e = m.mark(1, s)) != cudaSuccess) return e;
     const long long heads = static_cast<long long>(a.B) * a.H;
-    if (a.gate && a.V > 128 && (form == TcForm::kWide || tc_wide(a.B, a.H, a.V))) {
-        // The output stage on a grid that takes the 128-column kernel with a
-        // row over several of its CTAs: that kernel (every head) also writes
-        // each row's fp32 sum of squares, then the stage rewrites o in place.
-        // The 64-column kernel's cluster form of the stage cannot use the wide
-        // kernel and costs 1.9x there. With V = 128 the wide kernel applies
-        // the stage itself and takes the split below.
-        float *row_ss = reinterpret_cast<float *>(static_cast<char *>(ws) + tc_abeta_bytes(a.B, a.T, a.H));
-        if ((e = wide_tc_forward(a, ws, s, heads, row_ss)) != cudaSuccess) return e;
-        if ((e = m.mark(2, s)) != cudaSuccess) return e;
-        if ((e = wide_out_norm(a, row_ss, s)) != cudaSuccess) return e;
-        return m.mark(3, s);
-    }
     if (form == TcForm::kWide || tc_wide(a.B, a.H, a.V)) {
         // whole waves on the wide kernel, the last partial one on the 64-column
-        // one (with the output stage: in the wide kernel, and in the cluster
-        // form on the 64-column one)
+        // one; the output stage runs inside either (the head's CTAs of either
+        // as a cluster when a row spans several)
         const long long wh = tc_wide_heads(form, a.B, a.H, a.V);
         if ((e = wide_tc_forward(a, ws, s, wh)) != cudaSuccess) return e;
         if (wh == heads) return m.mark(2, s);

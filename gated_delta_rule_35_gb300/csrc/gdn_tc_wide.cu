@@ -46,6 +46,9 @@ constexpr uint32_t kCBig = 0, kCHT = 192, kCWO = 320;
 // With the output stage in the kernel (V = 128): a lane's o row, rounded to
 // bf16 and packed in pairs, between its write and its normalisation.
 constexpr uint32_t kCStash = 448;
+// The stage's rows span at most two CTAs (V <= 256), a thread-block cluster of
+// V / 128.
+constexpr int kWideMaxRanks = 2;
 static_assert(kCWO + kWideBV <= kCStash && kCStash + kWideBV / 2 <= kWideTmemCols, "the stash fits");
 
 // Shared-memory map (bytes from a 1024-aligned base); every tile is 64 rows of
@@ -65,7 +68,10 @@ struct WideLayout {
     static constexpr uint32_t kG = kVG + 16384;           // decay tables, 4 chunk slots
     static constexpr uint32_t kBar = kG + 5 * 4 * 64 * 4 + 16;
     static constexpr uint32_t kNw = kBar + 256;           // output stage: norm weight (128 floats)
-    static constexpr uint32_t kBytes = kNw + kWideBV * 4;
+    // output stage with a row over a cluster: each row's partial sums of
+    // squares from every CTA of the cluster, [chunk slot (4)][rank][64 rows]
+    static constexpr uint32_t kSums = kNw + kWideBV * 4;
+    static constexpr uint32_t kBytes = kSums + 4 * kWideMaxRanks * 64 * 4;
     static_assert(kBytes + 1024 <= 232448, "fits the 227 KB of shared memory a CTA may use");
     // q / k tile of chunk parity p within a block; -w and h^T sit between them
     __host__ __device__ static constexpr uint32_t qslot(int p) { return p ? 16384 : 0; }
@@ -85,20 +91,24 @@ struct WideBars {
     uint64_t g_ready[4];                        // decay tables (4 chunk slots)
     uint64_t o_seeded, xo_ready, vn_ready, hs_ready, o_free;
     uint64_t drain;
+    // output stage over a cluster: the rows' partial sums of a chunk slot
+    // (c % 4) arrive as transactions from every CTA of the cluster
+    uint64_t norm_bar[4];
     uint32_t abort, tmem;
 };
+static_assert(sizeof(WideBars) <= 256, "the barriers fit their region");
 
-// Output stage (gated RMSNorm over V), by instance; the plain instance has
-// none of its code:
-//   kOsSums  each o row's fp32 sum of squares over the CTA's 128 columns goes to
-//            row_ss, for a second kernel (a row spans several CTAs);
-//   kOsNorm  V = 128, so a row lies in one thread's TMEM lane: the aux warp
-//            takes the row's sum of squares from the fp32 accumulator O(c),
-//            parks the row rounded to bf16 in spare TMEM columns and frees O;
-//            one chunk later, in the chunk whose W and O lie in the other lane
-//            half (its idle turn), it applies norm, weight and gate and stores
-//            o. The chain never waits for the stage's element work.
-constexpr int kOsNone = 0, kOsSums = 1, kOsNorm = 2;
+// Output stage (gated RMSNorm over V), by instance (kOsNorm with it, kOsNormX
+// with it over a cluster, kOsNone without; the plain instance has none of its
+// code, and only kOsNormX has the cluster's). The aux warp takes its
+// row's sum of squares over the CTA's 128 columns from the fp32 accumulator
+// O(c), parks the row rounded to bf16 in spare TMEM columns and frees O; one
+// chunk later, in the chunk whose W and O lie in the other lane half (its idle
+// turn), it applies norm, weight and gate and stores o. The chain never waits
+// for the stage's element work. With V = 256 (kOsNormX) the head's two CTAs
+// form a cluster and every CTA sends each row's partial sum to both (st.async
+// into a slot of chunk c % 4), and both add them in rank order.
+constexpr int kOsNone = 0, kOsNorm = 1, kOsNormX = 2;
 
 __device__ __forceinline__ float sigmoid_tanh_w(float z) {
     float t;
@@ -113,8 +123,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const float *__restrict__ g, const float *__restrict__ h0,
                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ o, int T, int H, int V,
                    float scale, uint32_t *status, int l2norm, const float *__restrict__ rk,
-                   uint64_t wlim, int stall, float *__restrict__ row_ss,
-                   const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w, float norm_eps) {
+                   uint64_t wlim, int stall, const __nv_bfloat16 *__restrict__ gate, const float *__restrict__ norm_w, float norm_eps) {
     using Lay = WideLayout<K>;
     constexpr int KB = K / 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -141,7 +150,9 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                   "the zero tiles are every other tile of the row");
     for (int i = tid; i < 4 * 512; i += kWideThreads)
         st_shared_v4(sm + Lay::kZx + (i >> 9) * 16384 + (i & 511) * 16, 0u, 0u, 0u, 0u);
-    if (OS == kOsNorm && tid < kWideBV) reinterpret_cast<float *>(sm + Lay::kNw)[tid] = norm_w[tid];
+    // the stage's first column: a row spans the CTAs of a cluster only in kOsNormX
+    const int scol0 = OS == kOsNormX ? vt * kWideBV : 0;
+    if (OS != kOsNone && tid < kWideBV) reinterpret_cast<float *>(sm + Lay::kNw)[tid] = norm_w[scol0 + tid];
     fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(&bs->tmem, kWideTmemCols);
@@ -170,6 +181,9 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bs->hs_ready, kChainWarps * 32);
         mbar_init(&bs->o_free, 64);                       // the two aux warps on O's lanes
         mbar_init(&bs->drain, 1);
+        // one local arrival (with the expected bytes) per chunk of the slot
+        if (OS == kOsNormX)
+            for (int i = 0; i < 4; ++i) mbar_init(&bs->norm_bar[i], 1);
         bs->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_q);
@@ -179,6 +193,10 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     tc_fence_before_sync();
     __syncthreads();
+    // output stage over a cluster: its barriers are initialised before any CTA
+    // of the cluster sends to them
+    const int nrank = OS == kOsNormX ? nvt : 1;
+    if (nrank > 1) cluster_sync();
     // the setup above overlaps the WY kernel's last CTAs; everything below may
     // read its output. A 64-column kernel for the remaining heads may start
     // behind this grid from here on (it reads only the WY kernel's output).
@@ -383,9 +401,9 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // with the output stage: the row's sum of squares over these columns,
             // before rounding (four partial sums; none without the stage)
             float ss[4] = {0.f, 0.f, 0.f, 0.f};
-            if (OS == kOsNorm && in) {
+            if (OS != kOsNone && in) {
                 // the gate row (256 B) is read in this warp's next idle turn
-                const __nv_bfloat16 *zr = gate + row * V;
+                const __nv_bfloat16 *zr = gate + row * V + scol0;
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(zr));
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(zr + 64));
             }
@@ -401,7 +419,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ss[e & 3] = fmaf(v[e], v[e], ss[e & 3]);
                 }
-                if constexpr (OS == kOsNorm) {
+                if constexpr (OS != kOsNone) {
                     // the same rounding as the plain store
                     uint32_t pk[16];
 #pragma unroll
@@ -412,8 +430,20 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int q = 0; q < 4; ++q) store_bf16x8_global(o + oi + bb * 32 + q * 8, v + q * 8);
                 }
             }
-            if (OS == kOsSums && in) row_ss[row * nvt + vt] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
-            if (OS == kOsNorm) rstd_pend = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / V + norm_eps);
+            if (OS != kOsNone && nrank == 1) rstd_pend = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / V + norm_eps);
+            if (OS != kOsNone && nrank > 1) {
+                // every row (in range or not) to every CTA of the cluster, this
+                // CTA's entry (its rank, vt) of the slot; one thread of the
+                // half posts the bytes its own barrier expects
+                const int slot = cc & 3;
+                if ((q4 & 1) == 0 && lane == 0) mbar_arrive_expect_tx(&bs->norm_bar[slot], nrank * 64 * 4);
+                const uint32_t dst = s_base + Lay::kSums + ((slot * kWideMaxRanks + vt) * 64 + wrow) * 4;
+                const uint32_t nb = smem_u32(&bs->norm_bar[slot]);
+                const float part = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+#pragma unroll
+                for (int r = 0; r < kWideMaxRanks; ++r)
+                    if (r < nrank) st_async_cluster_f32(mapa_shared(dst, r), part, mapa_shared(nb, r));
+            }
             const uint32_t z[16] = {};
 #pragma unroll
             for (int bb = 0; bb < kWideBV / 16; ++bb) tmem_st16(tmem + kCWO + lane_off + bb * 16, z);
@@ -426,11 +456,22 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // 32 columns a step from the TMEM stash (the tcgen05.ld is warp-wide, so
         // every lane takes part), with the gate's next 64 bytes loaded while the
         // current ones are used.
-        auto finish_o = [&](int cc) {
+        auto finish_o = [&](int cc) -> bool {
+            if (nrank > 1) {
+                // every CTA's partial sums of chunk cc's rows, added in rank order
+                const int slot = cc & 3;
+                if (!warp_all(wait_bar_cluster(&bs->norm_bar[slot], (cc >> 2) & 1, abort, wlim))) return false;
+                const float *sums = reinterpret_cast<const float *>(sm + Lay::kSums) + slot * kWideMaxRanks * 64;
+                float tot = 0.f;
+#pragma unroll
+                for (int r = 0; r < kWideMaxRanks; ++r)
+                    if (r < nrank) tot += sums[r * 64 + wrow];
+                rstd_pend = rsqrtf(tot / V + norm_eps);
+            }
             const bool in = wrow < min(64, T - cc * 64);
             const int64_t row = in ? (static_cast<int64_t>(b) * T + cc * 64 + wrow) * H + h : 0;
-            const uint4 *zp = reinterpret_cast<const uint4 *>(gate + row * V);
-            uint4 *op = reinterpret_cast<uint4 *>(o + row * V);
+            const uint4 *zp = reinterpret_cast<const uint4 *>(gate + row * V + scol0);
+            uint4 *op = reinterpret_cast<uint4 *>(o + row * V + scol0);
             const float4 *nw4 = reinterpret_cast<const float4 *>(sm + Lay::kNw);
             const float rs = rstd_pend;
             uint4 zn[4];
@@ -451,7 +492,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (!in) continue;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float4 w0 = nw4[8 * p + 2 * q], w1 = nw4[8 * p + 2 * q + 1];
+                    const float4 w0 = nw4[8 * p + 2 * q], w1 = nw4[8 * p + 2 * q + 1];   // this CTA's columns
                     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                     const uint32_t z4[4] = {z[q].x, z[q].y, z[q].z, z[q].w};
                     float y[8];
@@ -465,6 +506,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                pack_bf16(y[6], y[7]));
                 }
             }
+            return true;
         };
         auto load_g = [&](int c) {
             const int t = c * 64 + ptid;
@@ -488,7 +530,7 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const bool mine = (q4 >> 1) == (c & 1);   // W(c) and O(c) lie in these lanes
             if (mine && c >= 2) {
                 if (!(ok = write_o(c - 2))) break;
-                if (OS == kOsNorm) pend = c - 2;
+                if (OS != kOsNone) pend = c - 2;
             }
             const float g_cur = g_next, gl = gl_next, rk_cur = rk_next;
             g_next = load_g(c + 1);
@@ -538,8 +580,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_arrive(&bs->g_ready[gs]);
             if (!mine) {
                 // W(c) lies in the other lane half: this warp's idle turn
-                if (OS == kOsNorm && pend >= 0) {
-                    finish_o(pend);
+                if (OS != kOsNone && pend >= 0) {
+                    if (!(ok = finish_o(pend))) break;
                     pend = -1;
                 }
                 continue;
@@ -564,11 +606,11 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_arrive(&bs->w_ready[c & 1]);
         }
         // the last two chunks' o
-        if (OS == kOsNorm && ok && pend >= 0) finish_o(pend);
+        if (OS != kOsNone && ok && pend >= 0) ok = finish_o(pend);
         for (int cc = max(0, NT - 2); ok && cc < NT; ++cc)
             if ((q4 >> 1) == (cc & 1)) {
                 ok = write_o(cc);
-                if (OS == kOsNorm && ok) finish_o(cc);
+                if (OS != kOsNone && ok) ok = finish_o(cc);
             }
     } else {
         // ================================================================ chain group
@@ -756,6 +798,8 @@ gdn_wide_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     tc_fence_before_sync();
     __syncthreads();
+    // no CTA of a cluster leaves while another may still write its shared memory
+    if (nrank > 1) cluster_sync();
     if (tid == 0 && *abort) atomicOr(status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kWideTmemCols);
 }
@@ -771,17 +815,18 @@ int sm_count_of_device() {
 }
 
 template <int K>
-cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads, float *row_ss) {
+cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
     // the output stage: in the kernel when a row is one CTA's, else row sums
-    const int os = !a.gate ? kOsNone : a.V == kWideBV ? kOsNorm : kOsSums;
-    if (os == kOsSums && !row_ss) return cudaErrorInvalidValue;
+    const int nvt = a.V / kWideBV;
+    if (a.gate && nvt > kWideMaxRanks) return cudaErrorInvalidValue;
+    const int os = !a.gate ? kOsNone : nvt > 1 ? kOsNormX : kOsNorm;
     CUtensorMap mq, mk, mv, ma;
     if (!make_tmap_bthx(&mq, a.q, K, a.H, a.T, a.B) || !make_tmap_bthx(&mk, a.k, K, a.H, a.T, a.B) ||
         !make_tmap_bthx(&mv, a.v, a.V, a.H, a.T, a.B) || !make_tmap_bthx(&ma, abeta, 128, a.H, a.T, a.B))
         return cudaErrorInvalidValue;
     const int smem = static_cast<int>(WideLayout<K>::kBytes + 1024);
-    const auto kernel = os == kOsNorm   ? gdn_wide_tc_kernel<K, kOsNorm>
-                        : os == kOsSums ? gdn_wide_tc_kernel<K, kOsSums>
+    const auto kernel = os == kOsNormX  ? gdn_wide_tc_kernel<K, kOsNormX>
+                        : os == kOsNorm ? gdn_wide_tc_kernel<K, kOsNorm>
                                         : gdn_wide_tc_kernel<K, kOsNone>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -791,12 +836,19 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long l
     cfg.blockDim = dim3(kWideThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int nattr = 0;
     // as for gdn_fused_tc_kernel: an early start only pays with more than one wave
     if (ctas > sm_count_of_device()) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (os == kOsNormX) {
+        // the head's V / 128 CTAs share the rows' sums of squares
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = nvt;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr++].val.clusterDim.z = 1;
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
@@ -812,64 +864,17 @@ cudaError_t launch_wide(const Args &a, const void *abeta, cudaStream_t s, long l
         wlim_arg = armed;
         stall_arg = 1;
     }
-    float *ss_arg = os == kOsSums ? row_ss : nullptr;
     const __nv_bfloat16 *gate_arg = static_cast<const __nv_bfloat16 *>(a.gate);
     const float *nw_arg = a.norm_w;
     float eps_arg = a.norm_eps;
     void *args[] = {&mq, &mk, &mv, &ma, &g_arg, &h0_arg, &hf_arg, &o_arg, &T_arg, &H_arg, &V_arg,
-                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg, &ss_arg,
-                    &gate_arg, &nw_arg, &eps_arg};
+                    &scale_arg, &status_arg, &norm_arg, &rk_arg, &wlim_arg, &stall_arg, &gate_arg, &nw_arg, &eps_arg};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel), args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-// Gated RMSNorm of the rows written by the 128-column kernel: one warp per
-// (token, head) row, 8 columns per lane and step. The row's mean square comes
-// from the fp32 sums of squares that kernel took before rounding o (one per
-// 128-column tile); gate and weight apply to the rounded o, which is
-// rewritten in place.
-
-__global__ void __launch_bounds__(256)
-gdn_out_norm_kernel(__nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ gate,
-                    const float *__restrict__ w, const float *__restrict__ row_ss, long long rows, int V,
-                    float eps) {
-    const int lane = threadIdx.x & 31, nvt = V / kWideBV;
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += warps) {
-        float ss = 0.f;
-        for (int p = 0; p < nvt; ++p) ss += row_ss[r * nvt + p];
-        const float rstd = rsqrtf(ss / V + eps);
-        for (int j = lane; j < V / 8; j += 32) {
-            uint4 *op = reinterpret_cast<uint4 *>(o + r * V) + j;
-            const uint4 ov = *op, zv = reinterpret_cast<const uint4 *>(gate + r * V)[j];
-            const float4 w0 = reinterpret_cast<const float4 *>(w)[2 * j], w1 = reinterpret_cast<const float4 *>(w)[2 * j + 1];
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            const uint32_t o4[4] = {ov.x, ov.y, ov.z, ov.w}, z4[4] = {zv.x, zv.y, zv.z, zv.w};
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 a = unpack_bf16(o4[e]), z = unpack_bf16(z4[e]);
-                y[2 * e] = a.x * rstd * wv[2 * e] * sigmoid_tanh_w(z.x);
-                y[2 * e + 1] = a.y * rstd * wv[2 * e + 1] * sigmoid_tanh_w(z.y);
-            }
-            *op = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-        }
-    }
-}
-
 }  // namespace
-
-cudaError_t wide_out_norm(const Args &a, const float *row_ss, cudaStream_t s) {
-    const long long rows = static_cast<long long>(a.B) * a.T * a.H;
-    const long long blocks = (rows + 7) / 8;
-    const int grid = static_cast<int>(blocks < 16LL * sm_count_of_device() ? blocks : 16LL * sm_count_of_device());
-    gdn_out_norm_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(a.o),
-                                             static_cast<const __nv_bfloat16 *>(a.gate), a.norm_w, row_ss, rows,
-                                             a.V, a.norm_eps);
-    return cudaGetLastError();
-}
 
 bool tc_wide(int B, int H, int V) {
     // with 64-wide tiles the grid would need more than one wave of SMs; with
@@ -879,8 +884,8 @@ bool tc_wide(int B, int H, int V) {
 
 int tc_sm_count() { return sm_count_of_device(); }
 
-cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads, float *row_ss) {
-    return a.K == 128 ? launch_wide<128>(a, abeta, s, heads, row_ss) : launch_wide<64>(a, abeta, s, heads, row_ss);
+cudaError_t wide_tc_forward(const Args &a, const void *abeta, cudaStream_t s, long long heads) {
+    return a.K == 128 ? launch_wide<128>(a, abeta, s, heads) : launch_wide<64>(a, abeta, s, heads);
 }
 
 }  // namespace gdn

@@ -314,8 +314,8 @@ GDN_API int32_t gdn_decode_step_launches(const gdn_problem *p, const char **name
  * formed from the fp32 o before its one rounding to the output dtype. On the
  * tensor-core path, the heads that the 128-column forward kernel takes
  * (GDN_ALGO_TC_WIDE, or GDN_ALGO_TC / AUTO on grids that take it) get the mean
- * square from the fp32 o too, but weight and gate are applied to the o that
- * kernel rounded: one more rounding, at most one unit in the last place. */
+ * square from the fp32 o too, but weight and gate are applied to o rounded to
+ * the output dtype: one more rounding, at most one unit in the last place. */
 typedef struct {
     const void *gate;      /* [B,T,H,V] in p->dtype, required, 16-byte aligned */
     const float *weight;   /* [V] fp32, required, 16-byte aligned */
@@ -324,14 +324,10 @@ typedef struct {
 
 /* gdn_chunk_fwd with the optional output stage (norm == NULL: the plain o of
  * gdn_chunk_fwd) and optional timing markers as in gdn_chunk_fwd_profiled
- * (events == NULL: none). On the tensor-core path the 64-column kernel runs
- * the CTAs of one head's V tiles as a thread-block cluster to share the row
- * sums, and the 128-column kernel applies the stage itself when V = 128, so
- * those calls launch the kernels gdn_chunk_fwd_launches names. With V > 128 on
- * a grid that takes the 128-column kernel, that kernel takes every head and
- * the stage is a second kernel after it (gdn_wy_tc_kernel, gdn_wide_tc_kernel,
- * gdn_out_norm_kernel; the last marker is recorded when n_events allows).
- * Every other contract is gdn_chunk_fwd's. */
+ * (events == NULL: none). On the tensor-core path the forward kernels apply
+ * the stage themselves, the CTAs of one head's V tiles forming a thread-block
+ * cluster to share the row sums, so a call launches the kernels that
+ * gdn_chunk_fwd_launches names. Every other contract is gdn_chunk_fwd's. */
 GDN_API gdn_status gdn_chunk_fwd_ex(const gdn_problem *p,
                                     const void *q, const void *k, const void *v,
                                     const float *g, const float *beta, float scale,

@@ -119,14 +119,17 @@ def test_output_norm_on_the_wide_kernel_grid():
     assert torch.equal(hf[wide], hw[wide])
 
 
-def test_output_norm_headline_shape_whole():
-    """The headline shape (B8 H64 T8192) with the output stage through 'auto':
-    three whole waves of the 128-column kernel with the stage inside it, the
-    other 56 heads on the 64-column kernel's cluster form, 128 chunks each;
-    against the oracle over the whole of o and h_final."""
-    B, T, H, K, V = 8, 8192, 64, 128, 128
-    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=3)
-    gate, weight = make_output_norm(B, T, H, V, seed=3)
+@pytest.mark.parametrize("shape", [(8, 8192, 64, 128, 128, 3), (2, 16384, 32, 128, 256, 4)])
+def test_output_norm_wide_shapes_whole(shape):
+    """Full-size shapes that take the 128-column kernel, with the output stage
+    through 'auto': B8 H64 T8192 (three whole waves with the stage inside the
+    kernel, the other 56 heads on the 64-column kernel's cluster form, 128
+    chunks each) and B2 H32 T16384 V256 (two-CTA clusters of the 128-column
+    kernel sharing the row sums, 256 chunks); against the oracle over the
+    whole of o and h_final."""
+    B, T, H, K, V, seed = shape
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=seed)
+    gate, weight = make_output_norm(B, T, H, V, seed=seed)
     d = gpu(x)
     o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, None, gate=gate.cuda(),
                       norm_weight=weight.cuda(), norm_eps=EPS)
