@@ -52,8 +52,12 @@ struct WyLayout {
     static constexpr uint32_t kK = 0, kKBlk = 16384;
     static constexpr uint32_t kN = 0;
     static constexpr uint32_t kXU = 16384;                 // [X; U] stacked, then A0 (bf16)
-    // The fp32 diagonal blocks [4][16][17] live in the U half of [X; U] until
-    // X is built from them (U is written after the first merge product).
+    // The fp32 diagonal blocks live in the U half of [X; U] until X is built
+    // from them (U is written after the first merge product): each block's L
+    // transposed ([16 columns][16 rows], blocks 272 floats apart, so that a
+    // thread reads four rows of one column with one 16-byte load and the two
+    // blocks of a warp sit on different banks), then X in place, row-major
+    // with a stride of 17.
     static constexpr uint32_t kLd = kXU + 8192;
     // One 8 KB region in the [N2] half of [N1; N2], free once the first merge
     // product has read it: Y1, Y2 (read by the last product), and finally the
@@ -262,7 +266,7 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
                 if (blk == rb) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) Ld[(rb * 16 + (r & 15)) * 17 + e] = v[e];
+                    for (int e = 0; e < 16; ++e) Ld[rb * 272 + e * 16 + (r & 15)] = v[e];
                 }
                 // N1: blocks (1,0) and (3,2); N2: rows 32-63 x columns 0-31
                 const bool in1 = (rb == 1 && blk == 0) || (rb == 3 && blk == 2);
@@ -286,14 +290,21 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     {
         float x[16];
         const int blk = tid >> 4, col = tid & 15;
-        float *Lb = Ld + blk * 16 * 17;
+        float *Lb = Ld + blk * 272;
         if (tid < 64) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
 #pragma unroll
             for (int j = 0; j < 15; ++j)
 #pragma unroll
-                for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-Lb[i * 17 + j], x[j], x[i]);
+                for (int q = (j + 1) >> 2; q < 4; ++q) {
+                    // rows 4q .. 4q + 3 of column j (L's upper triangle is zero)
+                    const float4 l4 = *reinterpret_cast<const float4 *>(Lb + j * 16 + 4 * q);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q + e > j) x[4 * q + e] = fmaf(-lv[e], x[j], x[4 * q + e]);
+                }
         }
         __syncthreads();
         if (tid < 64) {
@@ -386,17 +397,23 @@ gdn_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (__syncthreads_or(fail)) goto done;
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-            float v[16];
-            load16(blk, v);
             if (tid < 64) {
                 // A diag(beta) and A diag(beta exp(g)); the second goes to the
-                // [N1; N2] tile, free since the first merge product
-                float v2[16];
+                // [N1; N2] tile, free since the first merge product (rows
+                // 64-127 of the product are not needed: warps 2-3 skip them)
+                float v[16], v2[16];
+                load16(blk, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float a = v[e];
-                    v[e] = a * b_s[blk * 16 + e];
-                    v2[e] = a * eb_s[blk * 16 + e];
+                for (int m = 0; m < 4; ++m) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(b_s + blk * 16 + 4 * m);
+                    const float4 e4 = *reinterpret_cast<const float4 *>(eb_s + blk * 16 + 4 * m);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, ee[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = v[4 * m + e];
+                        v[4 * m + e] = a * bb[e];
+                        v2[4 * m + e] = a * ee[e];
+                    }
                 }
                 st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32), v);
                 st_bf16x8(sm + Lay::kOut + sw128(r, blk * 32 + 16), v + 8);
