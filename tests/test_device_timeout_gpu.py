@@ -49,6 +49,34 @@ def test_withheld_loads_report_a_device_timeout_then_recover(algo):
     assert rel(hf.cpu().numpy(), hf_ref) < 2e-2
 
 
+@pytest.mark.parametrize("V", [128, 256])
+def test_wide_kernel_output_stage_reports_a_device_timeout_then_recovers(V):
+    """The 128-column kernel with the output stage inside it (V = 256: two-CTA
+    clusters sharing the row sums): withheld loads end every role's wait, both
+    CTAs of a cluster meet at its closing barrier, and the next call is right."""
+    from oracle import epilogue
+    from gated_delta_rule_35_gb300.inputs import make_output_norm
+    B, T, H, K = 2, 300, 3, 128
+    x = make_inputs(B, T, H, K, V, dtype="bf16", seed=90, h0_std=0.1)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    gate, weight = make_output_norm(B, T, H, V, seed=90)
+    kw = dict(gate=gate.cuda(), norm_weight=weight.cuda(), norm_eps=1e-6)
+    p = native.problem(B, T, H, K, V, torch.bfloat16, "tcw")
+    ws = torch.zeros(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    native.debug_arm_stall(LIMIT_NS)
+    chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tcw", workspace=ws, **kw)
+    assert check_device_status(ws) == native.GDN_ERR_DEVICE_TIMEOUT
+    assert check_device_status(ws) == native.GDN_OK
+    o, hf = chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], 1.0, d["h0"], algo="tcw", workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert check_device_status(ws) == native.GDN_OK
+    o_ref, hf_ref = recurrence.forward(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                       to_f64(x["g"]), to_f64(x["beta"]), 1.0, to_f64(x["h0"]))
+    o_ref = epilogue.gated_rmsnorm(o_ref, to_f64(gate), to_f64(weight), 1e-6)
+    assert rel(o.float().cpu().numpy(), o_ref) < 2e-2
+    assert rel(hf.cpu().numpy(), hf_ref) < 2e-2
+
+
 @pytest.mark.parametrize("gated", [False, True])
 def test_per_channel_form_reports_a_device_timeout_then_recovers(gated):
     """The per-channel tensor-core form's forward kernel: its first load

@@ -104,3 +104,32 @@ def test_split_forward_and_per_channel_form_replay_from_a_graph(shape, per_chann
     torch.cuda.synchronize()
     assert torch.equal(o, o_e) and torch.equal(hf, hf_e)
     assert native.check_device_status(ws) == native.GDN_OK
+
+
+@pytest.mark.parametrize("shape,algo", [((1, 130, 160, 128, 128), "tc"), ((1, 130, 3, 128, 256), "tcw")])
+def test_output_stage_on_the_wide_kernel_replays_from_a_graph(shape, algo):
+    """The output stage inside the 128-column kernel, captured and replayed:
+    the split forward (152 heads on that kernel, 8 on the 64-column kernel's
+    cluster form) and V = 256 (two-CTA clusters of the wide kernel); bit for
+    bit the eager result."""
+    B, T, H, K, V = shape
+    x = gpu(make_inputs(B, T, H, K, V, dtype="bf16", seed=54, h0_std=0.1))
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], 1.0, x["h0"])
+    gate, weight = make_output_norm(B, T, H, V, seed=54)
+    kw = dict(algo=algo, gate=gate.cuda(), norm_weight=weight.cuda())
+    p = native.problem(B, T, H, K, V, torch.bfloat16, algo)
+    o_e, hf_e = chunk_fwd(*args, **kw)
+    ws = torch.empty(native.workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(o_e)
+    hf = torch.empty_like(hf_e)
+    chunk_fwd(*args, workspace=ws, out=o, final_state=hf, **kw)   # warm-up
+    torch.cuda.synchronize()
+    o.fill_(float("nan"))
+    hf.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chunk_fwd(*args, workspace=ws, out=o, final_state=hf, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(hf, hf_e)
+    assert native.check_device_status(ws) == native.GDN_OK

@@ -58,9 +58,10 @@ def test_chunked_output_norm(algo, dtype, K, V, T):
     assert rel(hf, hf_ref) < TOL[dtype], rel(hf, hf_ref)
 
 
-@pytest.mark.parametrize("algo", ["simt", "tc"])
+@pytest.mark.parametrize("algo", ["simt", "tc", "tcw"])
 def test_front_end_and_output_stage_together(algo):
-    """Raw g, unnormalised q and k, and the gated RMSNorm in one call."""
+    """Raw g, unnormalised q and k, and the gated RMSNorm in one call (tcw: the
+    128-column kernel, which applies the stage itself)."""
     if not have_algo(algo, 128, 128, "bf16"):
         pytest.skip("not built")
     B, T, H, K, V = 2, 150, 2, 128, 128
