@@ -77,11 +77,15 @@ def test_front_end_and_output_stage_together(algo):
     assert rel(hf.cpu().numpy(), hf_ref) < TOL["bf16"]
 
 
-def test_output_norm_clusters_over_several_waves():
-    """Four-CTA clusters (V = 256), 160 CTAs on 152 SMs and 16 chunks with a
-    ragged last one: every slot of the output stage's hand-offs cycles eight
-    times, and some clusters start only as others finish."""
-    B, T, H, K, V = 2, 1000, 20, 128, 256
+@pytest.mark.parametrize("H,V,kernel", [(27, 192, "gdn_fused_tc_kernel"), (20, 256, "gdn_wide_tc_kernel")])
+def test_output_norm_clusters_over_several_waves(H, V, kernel):
+    """Clusters over more than one wave, 16 chunks with a ragged last one, so
+    every slot of the output stage's hand-offs cycles several times: V = 192
+    on the 64-column kernel (three-CTA clusters, 162 CTAs on 152 SMs, some
+    clusters starting only as others finish) and V = 256 on the 128-column
+    kernel (two-CTA clusters, 80 CTAs)."""
+    B, T, K = 2, 1000, 128
+    assert native.launches(native.problem(B, T, H, K, V, torch.bfloat16, "tc"))[1] == kernel
     x = make_inputs(B, T, H, K, V, dtype="bf16", seed=17, h0_std=0.1)
     gate, weight = make_output_norm(B, T, H, V, seed=17)
     d = gpu(x)
