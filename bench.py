@@ -132,8 +132,11 @@ def ncu_traffic(kernel, workload):
     f = ROOT / "profiles" / "dram_traffic.json"
     if not f.exists():
         return None
-    rec = json.loads(f.read_text()).get(kernel)
-    if not rec or rec.get("workload") != workload:
+    recs = json.loads(f.read_text()).get(kernel)
+    # one record, or a list of them (one per workload)
+    recs = recs if isinstance(recs, list) else [recs] if recs else []
+    rec = next((r for r in recs if r.get("workload") == workload), None)
+    if rec is None:
         return None
     src = KERNEL_SOURCE.get(kernel)
     if not src or rec.get("source_sha") != source_sha(src):

@@ -96,3 +96,30 @@ def test_design_traffic_from_the_committed_records():
         assert abs(r["design_traffic_frac_of_hbm"] - sum(recs) / 2e-3 / 6800e9) < 1e-12
     assert bench.pipeline_roofline(w, 2e-3, peaks, False, ["no_such_kernel"])["design_traffic"] is None
     assert "design_traffic" not in bench.pipeline_roofline(w, 2e-3, peaks, False)
+
+
+def test_traffic_records_by_workload_and_source(tmp_path, monkeypatch):
+    """A kernel's ncu records may be one object or a list, one per workload:
+    the bench takes the record of its workload, and none once the kernel's
+    source no longer has the recorded hash."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = tmp_path / "k.cu"
+    src.write_text("// kernel source\n")
+    sha = bench.hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps({
+        "one": {"workload": "w1", "source_sha": sha, "dram_bytes_per_launch": 5},
+        "many": [{"workload": "w1", "source_sha": sha, "dram_bytes_per_launch": 7},
+                 {"workload": "w2", "source_sha": sha, "dram_bytes_per_launch": 11}],
+        "stale": {"workload": "w1", "source_sha": "0" * 16, "dram_bytes_per_launch": 13}}))
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    monkeypatch.setattr(bench, "KERNEL_SOURCE", {"one": "k.cu", "many": "k.cu", "stale": "k.cu"})
+    assert bench.ncu_traffic("one", "w1") == 5 and bench.ncu_traffic("one", "w2") is None
+    assert bench.ncu_traffic("many", "w1") == 7 and bench.ncu_traffic("many", "w2") == 11
+    assert bench.ncu_traffic("many", "w3") is None
+    assert bench.ncu_traffic("stale", "w1") is None
+    assert bench.ncu_traffic("one+many", "w1") == 12
+    assert bench.ncu_traffic("one+many", "w2") is None
+    assert bench.ncu_traffic("absent", "w1") is None
